@@ -1,0 +1,265 @@
+"""CPU oracle for the FP8 linear layer -- test infrastructure only.
+
+Only the test-suite, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
+``bench.py`` may import this package.  The product path (the CUDA library and
+its binding) never does, and this package never imports the product.
+
+The arithmetic lives in ``fp8_oracle.c`` (plain loops, fp64 where a sum is
+formed); this module only compiles it with ``gcc`` and marshals numpy arrays.
+Every function cites the passage of the FP8-training pages it restates in the
+C source.
+
+Pins (what ties each part to something other than itself) are the
+``-m "not gpu"`` tests ``tests/test_oracle_*.py``.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import platform
+import subprocess
+import threading
+
+import numpy as np
+
+E4M3, E5M2 = 0, 1
+SCALE_FP32, SCALE_POW2 = 0, 1
+GRAN_1x128, GRAN_128x128, GRAN_TENSOR = 0, 1, 2
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "fp8_oracle.c")
+_BUILD = os.path.join(_HERE, "_build")
+_LIB = os.path.join(_BUILD, f"liboracle_{platform.machine()}.so")
+_lock = threading.Lock()
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle with gcc (no fast-math, no FMA contraction)."""
+    os.makedirs(_BUILD, exist_ok=True)
+    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
+        tmp = _LIB + f".tmp{os.getpid()}"
+        cmd = ["gcc", "-std=c11", "-O2", "-ffp-contract=off", "-fno-fast-math", "-fPIC",
+               "-shared", "-o", tmp, _SRC, "-lm"]
+        subprocess.run(cmd, check=True)
+        os.replace(tmp, _LIB)
+    return _LIB
+
+
+class Operand(ctypes.Structure):
+    _fields_ = [("data", ctypes.c_void_p), ("ld", ctypes.c_int64),
+                ("transposed", ctypes.c_int32), ("fmt", ctypes.c_int32),
+                ("gran", ctypes.c_int32), ("pad_", ctypes.c_int32),
+                ("scales", ctypes.c_void_p)]
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            lib = ctypes.CDLL(build())
+            i64, i32, vp, f32 = ctypes.c_int64, ctypes.c_int32, ctypes.c_void_p, ctypes.c_float
+            lib.fp8o_decode.argtypes = [ctypes.c_uint32, ctypes.c_int]
+            lib.fp8o_decode.restype = ctypes.c_double
+            lib.fp8o_fmax.argtypes = [ctypes.c_int]
+            lib.fp8o_fmax.restype = ctypes.c_double
+            lib.fp8o_encode.argtypes = [f32, ctypes.c_int]
+            lib.fp8o_encode.restype = ctypes.c_uint32
+            lib.fp8o_encode_array.argtypes = [vp, i64, ctypes.c_int, vp]
+            lib.fp8o_encode_array.restype = None
+            lib.fp8o_bf16_to_f32.argtypes = [ctypes.c_uint16]
+            lib.fp8o_bf16_to_f32.restype = f32
+            lib.fp8o_block_scale.argtypes = [f32, ctypes.c_int, ctypes.c_int]
+            lib.fp8o_block_scale.restype = f32
+            lib.fp8o_quantize_1x128.argtypes = [vp, i64, i64, i64, ctypes.c_int, ctypes.c_int, vp, i64, vp]
+            lib.fp8o_quantize_1x128.restype = None
+            lib.fp8o_quantize_128x128.argtypes = [vp, i64, i64, i64, ctypes.c_int, ctypes.c_int, vp, i64, vp]
+            lib.fp8o_quantize_128x128.restype = None
+            lib.fp8o_quantize_tensor.argtypes = [vp, i64, ctypes.c_int, f32, vp, vp]
+            lib.fp8o_quantize_tensor.restype = None
+            lib.fp8o_amax_history_update.argtypes = [vp, vp, i32, f32, ctypes.c_int, i32, vp]
+            lib.fp8o_amax_history_update.restype = None
+            lib.fp8o_gemm.argtypes = [i64, i64, i64, ctypes.POINTER(Operand), ctypes.POINTER(Operand),
+                                      i64, vp, i64, vp, vp, vp]
+            lib.fp8o_gemm.restype = ctypes.c_int
+            lib.fp8o_grouped_gemm.argtypes = [i32, vp, i64, i64, i64, ctypes.POINTER(Operand),
+                                              ctypes.POINTER(Operand), i64, vp, i64, vp, vp, vp]
+            lib.fp8o_grouped_gemm.restype = ctypes.c_int
+            _lib = lib
+    return _lib
+
+
+def _ptr(a: np.ndarray) -> int:
+    assert a.flags["C_CONTIGUOUS"] or a.ndim == 0
+    return a.ctypes.data
+
+
+def _bf16(x) -> np.ndarray:
+    x = np.ascontiguousarray(x)
+    if x.dtype != np.uint16:
+        raise TypeError("oracle inputs are bf16 bit patterns (numpy uint16)")
+    return x
+
+
+# ------------------------------------------------------------------ formats
+def decode(code: int, fmt: int) -> float:
+    return _load().fp8o_decode(int(code) & 0xFF, fmt)
+
+
+def decode_table(fmt: int) -> np.ndarray:
+    """fp64 value of each of the 256 codes (NaN for NaN codes)."""
+    return np.array([decode(c, fmt) for c in range(256)], dtype=np.float64)
+
+
+def fmax(fmt: int) -> float:
+    return _load().fp8o_fmax(fmt)
+
+
+def encode(v: float, fmt: int) -> int:
+    return int(_load().fp8o_encode(ctypes.c_float(v), fmt))
+
+
+def encode_array(v: np.ndarray, fmt: int) -> np.ndarray:
+    """Element-wise encoder over an fp32 array."""
+    flat = np.ascontiguousarray(np.asarray(v, dtype=np.float32).ravel())
+    out = np.empty(flat.shape, dtype=np.uint8)
+    _load().fp8o_encode_array(_ptr(flat), flat.size, fmt, _ptr(out))
+    return out.reshape(np.shape(v))
+
+
+def bf16_to_f32(h: int) -> float:
+    return _load().fp8o_bf16_to_f32(int(h))
+
+
+def block_scale(amax: float, fmt: int, mode: int) -> float:
+    return float(_load().fp8o_block_scale(ctypes.c_float(amax), fmt, mode))
+
+
+# ------------------------------------------------------------- quantizers
+def quantize_1x128(x: np.ndarray, fmt: int = E4M3, mode: int = SCALE_FP32):
+    """x: [rows, cols] bf16 bits -> (q [rows, cols] u8, scales [ceil(cols/128), rows] f32)."""
+    x = _bf16(x)
+    rows, cols = x.shape
+    q = np.empty((rows, cols), dtype=np.uint8)
+    s = np.empty(((cols + 127) // 128, rows), dtype=np.float32)
+    _load().fp8o_quantize_1x128(_ptr(x), rows, cols, cols, fmt, mode, _ptr(q), cols, _ptr(s))
+    return q, s
+
+
+def quantize_128x128(w: np.ndarray, fmt: int = E4M3, mode: int = SCALE_FP32):
+    """w: [rows, cols] bf16 bits -> (q, scales [ceil(rows/128), ceil(cols/128)] f32)."""
+    w = _bf16(w)
+    rows, cols = w.shape
+    q = np.empty((rows, cols), dtype=np.uint8)
+    s = np.empty(((rows + 127) // 128, (cols + 127) // 128), dtype=np.float32)
+    _load().fp8o_quantize_128x128(_ptr(w), rows, cols, cols, fmt, mode, _ptr(q), cols, _ptr(s))
+    return q, s
+
+
+def quantize_tensor(x: np.ndarray, fmt: int, scale: float):
+    """Per-tensor quantization with a given dequant scale -> (q, amax)."""
+    x = _bf16(x)
+    q = np.empty(x.shape, dtype=np.uint8)
+    amax = np.zeros(1, dtype=np.float32)
+    _load().fp8o_quantize_tensor(_ptr(x), x.size, fmt, ctypes.c_float(scale), _ptr(q), _ptr(amax))
+    return q, float(amax[0])
+
+
+class DelayedState:
+    """Per-tensor delayed-scaling state: amax history, head, scale in use."""
+
+    def __init__(self, history_len: int, fmt: int, margin: int = 0):
+        self.history = np.zeros(history_len, dtype=np.float32)
+        self.head = np.zeros(1, dtype=np.int32)
+        self.scale = np.ones(1, dtype=np.float32)
+        self.fmt, self.margin = fmt, margin
+
+    def update(self, amax: float) -> float:
+        _load().fp8o_amax_history_update(_ptr(self.history), _ptr(self.head), len(self.history),
+                                         ctypes.c_float(amax), self.fmt, self.margin, _ptr(self.scale))
+        return float(self.scale[0])
+
+    def step(self, x: np.ndarray):
+        """Quantize with the scale in use, then fold this step's amax in."""
+        q, amax = quantize_tensor(x, self.fmt, float(self.scale[0]))
+        self.update(amax)
+        return q, amax
+
+
+# ------------------------------------------------------------------- GEMM
+def operand(data: np.ndarray, fmt: int, gran: int, scales: np.ndarray, transposed: bool = False):
+    data = np.ascontiguousarray(data, dtype=np.uint8)
+    scales = np.ascontiguousarray(scales, dtype=np.float32)
+    op = Operand(data=_ptr(data), ld=data.shape[-1], transposed=int(transposed), fmt=fmt,
+                 gran=gran, pad_=0, scales=_ptr(scales))
+    op._keep = (data, scales)
+    return op
+
+
+def _sel(sel, n):
+    if sel is None:
+        return n, None, None
+    a = np.ascontiguousarray(sel, dtype=np.int64)
+    return a.size, a, _ptr(a)
+
+
+def gemm(M: int, N: int, K: int, A: Operand, B: Operand, rows=None, cols=None):
+    """fp64 y and sum|terms| for the selected outputs of deq(A) deq(B)^T."""
+    nr, r_arr, r_p = _sel(rows, M)
+    nc, c_arr, c_p = _sel(cols, N)
+    y = np.empty((nr, nc), dtype=np.float64)
+    ya = np.empty((nr, nc), dtype=np.float64)
+    rc = _load().fp8o_gemm(M, N, K, ctypes.byref(A), ctypes.byref(B), nr, r_p, nc, c_p,
+                           _ptr(y), _ptr(ya))
+    if rc:
+        raise ValueError("oracle gemm: unsupported operand combination or index out of range")
+    return y, ya
+
+
+def grouped_gemm(offsets: np.ndarray, a_rows: int, N: int, K: int, A: Operand, B: Operand,
+                 rows=None, cols=None):
+    """Grouped product; a_rows = rows of A as stored (>= offsets[-1])."""
+    off = np.ascontiguousarray(offsets, dtype=np.int32)
+    G = off.size - 1
+    nr, r_arr, r_p = _sel(rows, int(off[-1]))
+    nc, c_arr, c_p = _sel(cols, N)
+    y = np.empty((nr, nc), dtype=np.float64)
+    ya = np.empty((nr, nc), dtype=np.float64)
+    rc = _load().fp8o_grouped_gemm(G, _ptr(off), a_rows, N, K, ctypes.byref(A), ctypes.byref(B),
+                                   nr, r_p, nc, c_p, _ptr(y), _ptr(ya))
+    if rc:
+        raise ValueError("oracle grouped gemm: unsupported operand combination")
+    return y, ya
+
+
+# ------------------------------------------------------- acceptance rules
+def check_f32(y: np.ndarray, y_ref: np.ndarray, yabs: np.ndarray, rel: float = 1e-5):
+    """fp32 output bound: |y - y_ref| <= rel * sum|terms| (sum 0 -> y must be 0).
+    Returns a boolean mask of elements that FAIL."""
+    y = np.asarray(y, dtype=np.float64)
+    return ~(np.abs(y - y_ref) <= rel * yabs)
+
+
+def _bf16_round(v: np.ndarray) -> np.ndarray:
+    """fp64 -> nearest bf16 (via fp32, both nearest-even), as bit patterns."""
+    import torch
+    t = torch.from_numpy(np.asarray(v, dtype=np.float64)).to(torch.float32).to(torch.bfloat16)
+    return t.view(torch.int16).numpy().view(np.uint16)
+
+
+def _ordinal(b: np.ndarray) -> np.ndarray:
+    """bf16 bit pattern -> integer that is monotone in the value (+0 and -0 both 0)."""
+    b = b.astype(np.int64)
+    mag = b & 0x7FFF
+    return np.where(b & 0x8000, -mag, mag)
+
+
+def check_bf16(y_bits: np.ndarray, y_ref: np.ndarray, yabs: np.ndarray, rel: float = 1e-5):
+    """bf16 output: within one bf16 ordinal step of the bf16 rounding of any
+    value inside the fp32 bound [y_ref - rel*abs, y_ref + rel*abs].  Away from
+    cancellation this is "within 1 ulp of bf16(y_ref)".  Returns FAIL mask."""
+    tol = rel * yabs
+    lo = _ordinal(_bf16_round(y_ref - tol)) - 1
+    hi = _ordinal(_bf16_round(y_ref + tol)) + 1
+    o = _ordinal(np.asarray(y_bits, dtype=np.uint16))
+    return ~((o >= lo) & (o <= hi))

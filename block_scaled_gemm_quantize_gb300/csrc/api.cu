@@ -1,0 +1,278 @@
+// api.cu -- the C ABI (include/fp8bs.h): argument validation, TMA tensor-map
+// construction and kernel launches.  No device memory is allocated here.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+
+#include "../../include/fp8bs.h"
+#include "gemm_kernels.h"
+#include "quant_kernels.h"
+
+namespace {
+
+thread_local char g_err[512] = "";
+
+int fail(int code, const char* fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_err, sizeof(g_err), fmt, ap);
+    va_end(ap);
+    return code;
+}
+
+int cuda_fail(cudaError_t e, const char* where) {
+    return fail(FP8BS_ERR_CUDA, "%s: %s (%s)", where, cudaGetErrorName(e), cudaGetErrorString(e));
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool aligned4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
+bool valid_fmt(int32_t f) { return f == FP8BS_E4M3 || f == FP8BS_E5M2; }
+bool valid_mode(int32_t m) { return m == FP8BS_SCALE_FP32 || m == FP8BS_SCALE_POW2; }
+
+// Shared checks of the two block quantizers.
+int check_block_quant(const char* fn, const void* x, int64_t rows, int64_t cols, int64_t ld_x,
+                      int32_t fmt, int32_t mode, const uint8_t* q, int64_t ld_q,
+                      const float* scales) {
+    if (rows < 0 || cols < 0) return fail(FP8BS_ERR_INVALID_ARG, "%s: negative size", fn);
+    if (!valid_fmt(fmt) || !valid_mode(mode))
+        return fail(FP8BS_ERR_INVALID_ARG, "%s: bad format %d or scale mode %d", fn, fmt, mode);
+    if (rows == 0 || cols == 0) return FP8BS_OK;
+    if (!x || !q || !scales) return fail(FP8BS_ERR_INVALID_ARG, "%s: null pointer", fn);
+    if (ld_x < cols || ld_q < cols)
+        return fail(FP8BS_ERR_INVALID_ARG, "%s: leading dimension smaller than cols", fn);
+    if (cols % 128) return fail(FP8BS_ERR_UNSUPPORTED, "%s: cols %% 128 != 0 (cols=%lld)", fn, (long long)cols);
+    if (!aligned16(x) || !aligned16(q) || (ld_x * 2) % 16 || ld_q % 16 || !aligned4(scales))
+        return fail(FP8BS_ERR_MISALIGNED, "%s: x/q must be 16-byte aligned with 16-byte row pitch", fn);
+    return 1;  // proceed
+}
+
+// ------------------------------------------------------------ tensor maps
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+cudaError_t g_encode_err = cudaSuccess;
+
+int get_encoder() {
+    std::call_once(g_encode_once, [] {
+        cudaDriverEntryPointQueryResult q;
+        void* fn = nullptr;
+        g_encode_err = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
+                                                        cudaEnableDefault, &q);
+        if (g_encode_err == cudaSuccess && q == cudaDriverEntryPointSuccess)
+            g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    });
+    if (!g_encode) return fail(FP8BS_ERR_CUDA, "cuTensorMapEncodeTiled unavailable (%s)",
+                               cudaGetErrorString(g_encode_err));
+    return FP8BS_OK;
+}
+
+// 2-D uint8 tensor [outer][inner] with row pitch `pitch` bytes; box
+// {128, box_outer}, 128-byte swizzle, out-of-bounds elements read as zero.
+int make_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer, uint64_t pitch,
+             uint32_t box_outer) {
+    cuuint64_t dims[2] = {inner, outer};
+    cuuint64_t strides[1] = {pitch};
+    cuuint32_t box[2] = {128, box_outer};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides,
+                          box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS)
+        return fail(FP8BS_ERR_CUDA, "cuTensorMapEncodeTiled failed (CUresult %d)", (int)r);
+    return FP8BS_OK;
+}
+
+int sm_count() {
+    int dev = 0, n = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    return n;
+}
+
+int check_operand(const char* fn, const char* name, const fp8bs_operand* o, int64_t rows,
+                  int64_t K, bool is_b, bool grouped) {
+    if (!o) return fail(FP8BS_ERR_INVALID_ARG, "%s: %s is null", fn, name);
+    if (!o->data || !o->scales) return fail(FP8BS_ERR_INVALID_ARG, "%s: %s data/scales null", fn, name);
+    if (!valid_fmt(o->fmt)) return fail(FP8BS_ERR_INVALID_ARG, "%s: %s bad format", fn, name);
+    if (o->gran < 0 || o->gran > 2 || o->reserved != 0)
+        return fail(FP8BS_ERR_INVALID_ARG, "%s: %s bad granularity", fn, name);
+    if (o->transposed != 0 && o->transposed != 1)
+        return fail(FP8BS_ERR_INVALID_ARG, "%s: %s bad transposed flag", fn, name);
+    if (o->gran == FP8BS_GRAN_1x128 && (is_b || o->transposed))
+        return fail(FP8BS_ERR_UNSUPPORTED, "%s: %s 1x128 scales only on a non-transposed A", fn, name);
+    if (grouped && o->transposed)
+        return fail(FP8BS_ERR_UNSUPPORTED, "%s: %s must be non-transposed in a grouped product", fn, name);
+    if (grouped && !is_b && o->gran == FP8BS_GRAN_128x128)
+        return fail(FP8BS_ERR_UNSUPPORTED, "%s: grouped A takes 1x128 or per-tensor scales", fn);
+    const int64_t inner = o->transposed ? rows : K;
+    if (o->ld < inner) return fail(FP8BS_ERR_INVALID_ARG, "%s: %s ld too small", fn, name);
+    if (!aligned16(o->data) || o->ld % 16)
+        return fail(FP8BS_ERR_MISALIGNED, "%s: %s data must be 16-byte aligned, ld %% 16 == 0", fn, name);
+    if (!aligned4(o->scales)) return fail(FP8BS_ERR_MISALIGNED, "%s: %s scales not 4-byte aligned", fn, name);
+    return FP8BS_OK;
+}
+
+int run_gemm(const char* fn, int32_t G, const int32_t* offsets, int64_t a_rows, int64_t M,
+             int64_t N, int64_t K, const fp8bs_operand* A, const fp8bs_operand* B, int32_t mode,
+             void* Y, int64_t ld_y, int32_t out_dtype, cudaStream_t stream) {
+    const bool grouped = offsets != nullptr;
+    if (M < 0 || N < 0 || K < 0 || a_rows < 0) return fail(FP8BS_ERR_INVALID_ARG, "%s: negative size", fn);
+    if (!valid_mode(mode)) return fail(FP8BS_ERR_INVALID_ARG, "%s: bad scale mode", fn);
+    if (out_dtype != FP8BS_OUT_F32 && out_dtype != FP8BS_OUT_BF16)
+        return fail(FP8BS_ERR_INVALID_ARG, "%s: bad output dtype", fn);
+    if (grouped && (G < 1 || G > fp8bs::kMaxGroups))
+        return fail(FP8BS_ERR_INVALID_ARG, "%s: num_groups must be in [1, %d]", fn, fp8bs::kMaxGroups);
+    if (M == 0 || N == 0) return FP8BS_OK;
+    if (!Y) return fail(FP8BS_ERR_INVALID_ARG, "%s: Y is null", fn);
+    if (ld_y < N) return fail(FP8BS_ERR_INVALID_ARG, "%s: ld_y < N", fn);
+    const int64_t esz = out_dtype == FP8BS_OUT_BF16 ? 2 : 4;
+    if (!aligned16(Y) || (ld_y * esz) % 16)
+        return fail(FP8BS_ERR_MISALIGNED, "%s: Y must be 16-byte aligned with 16-byte row pitch", fn);
+    if (K == 0) {  // empty contraction: Y = 0
+        cudaError_t e = cudaMemset2DAsync(Y, ld_y * esz, 0, N * esz, M, stream);
+        return e == cudaSuccess ? FP8BS_OK : cuda_fail(e, fn);
+    }
+    if (K % 128) return fail(FP8BS_ERR_UNSUPPORTED, "%s: K %% 128 != 0 (K=%lld)", fn, (long long)K);
+    if (N % 8) return fail(FP8BS_ERR_UNSUPPORTED, "%s: N %% 8 != 0", fn);
+    int rc;
+    if ((rc = check_operand(fn, "A", A, M, K, false, grouped)) != FP8BS_OK) return rc;
+    if ((rc = check_operand(fn, "B", B, N, K, true, grouped)) != FP8BS_OK) return rc;
+    if (a_rows > (int64_t)INT32_MAX - 256 || N * (grouped ? G : 1) > (int64_t)INT32_MAX - 256 ||
+        K > (int64_t)INT32_MAX)
+        return fail(FP8BS_ERR_UNSUPPORTED, "%s: dimension beyond 2^31", fn);
+    if ((rc = get_encoder()) != FP8BS_OK) return rc;
+
+    const int BN = fp8bs::gemm_tile_n(), BM = fp8bs::gemm_tile_m();
+    const bool a_mn = A->transposed, b_mn = B->transposed;
+    CUtensorMap tmA, tmB;
+    if (a_mn) rc = make_map(&tmA, A->data, M, K, A->ld, 128);
+    else rc = make_map(&tmA, A->data, K, a_rows, A->ld, 128);
+    if (rc) return rc;
+    const int64_t b_rows_total = grouped ? (int64_t)G * N : N;
+    if (b_mn) rc = make_map(&tmB, B->data, N, K, B->ld, 128);
+    else rc = make_map(&tmB, B->data, K, b_rows_total, B->ld, BN);
+    if (rc) return rc;
+
+    fp8bs::GemmParams p;
+    memset(&p, 0, sizeof(p));
+    p.M = M;
+    p.N = N;
+    p.K = K;
+    p.a_rows = a_rows;
+    p.a_rblocks = (M + 127) / 128;
+    p.b_rblocks = (N + 127) / 128;
+    p.b_scale_group_stride = B->gran == FP8BS_GRAN_128x128 ? ((N + 127) / 128) * (K / 128) : 0;
+    p.sa = A->scales;
+    p.sb = B->scales;
+    p.offsets = offsets;
+    p.y = Y;
+    p.ldy = ld_y;
+    p.num_groups = grouped ? G : 1;
+    p.b_rows_per_group = grouped ? static_cast<int32_t>(N) : 0;
+    p.a_gran = A->gran;
+    p.b_gran = B->gran;
+    p.tiles_n = static_cast<int32_t>((N + BN - 1) / BN);
+    p.promote = (A->gran == FP8BS_GRAN_TENSOR && B->gran == FP8BS_GRAN_TENSOR) ? 0 : 1;
+    p.out_bf16 = out_dtype == FP8BS_OUT_BF16;
+    p.idesc = fp8bs::make_idesc_f8f6f4(A->fmt, B->fmt, a_mn, b_mn, b_mn ? 128 : BN);
+
+    // upper bound on tiles (the grouped count is only known on the device)
+    const int64_t slots = grouped ? (a_rows + BM - 1) / BM + G : (M + BM - 1) / BM;
+    const int64_t tiles = slots * p.tiles_n;
+    if (tiles > (int64_t)INT32_MAX) return fail(FP8BS_ERR_UNSUPPORTED, "%s: too many tiles", fn);
+    const int sms = sm_count();
+    if (sms <= 0) return fail(FP8BS_ERR_CUDA, "%s: cannot query the device", fn);
+    const int grid = static_cast<int>(tiles < sms ? tiles : sms);
+    if (grid <= 0) return FP8BS_OK;
+    cudaError_t e = fp8bs::launch_fp8_gemm(tmA, tmB, p, a_mn, b_mn, grid, stream);
+    return e == cudaSuccess ? FP8BS_OK : cuda_fail(e, fn);
+}
+
+}  // namespace
+
+extern "C" {
+
+int fp8bs_version(void) { return 1; }
+
+const char* fp8bs_last_error(void) { return g_err; }
+
+int fp8_quantize_1x128(const void* x, int64_t rows, int64_t cols, int64_t ld_x, int32_t fmt,
+                       int32_t mode, uint8_t* q, int64_t ld_q, float* scales,
+                       fp8bs_stream_t stream) {
+    int rc = check_block_quant("fp8_quantize_1x128", x, rows, cols, ld_x, fmt, mode, q, ld_q, scales);
+    if (rc <= 0) return rc;
+    cudaError_t e = fp8bs::launch_quant_1x128(static_cast<const uint16_t*>(x), rows, cols, ld_x, fmt,
+                                              mode, q, ld_q, scales, (cudaStream_t)stream);
+    return e == cudaSuccess ? FP8BS_OK : cuda_fail(e, "fp8_quantize_1x128");
+}
+
+int fp8_quantize_128x128(const void* w, int64_t rows, int64_t cols, int64_t ld_w, int32_t fmt,
+                         int32_t mode, uint8_t* q, int64_t ld_q, float* scales,
+                         fp8bs_stream_t stream) {
+    int rc = check_block_quant("fp8_quantize_128x128", w, rows, cols, ld_w, fmt, mode, q, ld_q, scales);
+    if (rc <= 0) return rc;
+    cudaError_t e = fp8bs::launch_quant_128x128(static_cast<const uint16_t*>(w), rows, cols, ld_w,
+                                                fmt, mode, q, ld_q, scales, (cudaStream_t)stream);
+    return e == cudaSuccess ? FP8BS_OK : cuda_fail(e, "fp8_quantize_128x128");
+}
+
+int fp8_quantize_tensor_delayed(const void* x, int64_t numel, int32_t fmt, const float* scale,
+                                uint8_t* q, float* amax_out, fp8bs_stream_t stream) {
+    const char* fn = "fp8_quantize_tensor_delayed";
+    if (numel < 0) return fail(FP8BS_ERR_INVALID_ARG, "%s: negative size", fn);
+    if (!valid_fmt(fmt)) return fail(FP8BS_ERR_INVALID_ARG, "%s: bad format", fn);
+    if (!scale || !amax_out) return fail(FP8BS_ERR_INVALID_ARG, "%s: null scale/amax", fn);
+    if (numel > 0 && (!x || !q)) return fail(FP8BS_ERR_INVALID_ARG, "%s: null pointer", fn);
+    if (!aligned4(scale) || !aligned4(amax_out) || (numel > 0 && (!aligned16(x) || !aligned16(q))))
+        return fail(FP8BS_ERR_MISALIGNED, "%s: x/q must be 16-byte aligned", fn);
+    cudaError_t e = fp8bs::launch_quant_tensor(static_cast<const uint16_t*>(x), numel, fmt, scale, q,
+                                               amax_out, (cudaStream_t)stream);
+    return e == cudaSuccess ? FP8BS_OK : cuda_fail(e, fn);
+}
+
+int fp8_amax_history_update(float* history, int32_t* head, int32_t history_len, const float* amax,
+                            int32_t fmt, int32_t margin, float* scale, fp8bs_stream_t stream) {
+    const char* fn = "fp8_amax_history_update";
+    if (!history || !head || !amax || !scale) return fail(FP8BS_ERR_INVALID_ARG, "%s: null pointer", fn);
+    if (history_len < 1) return fail(FP8BS_ERR_INVALID_ARG, "%s: history_len < 1", fn);
+    if (!valid_fmt(fmt)) return fail(FP8BS_ERR_INVALID_ARG, "%s: bad format", fn);
+    if (margin < -126 || margin > 126) return fail(FP8BS_ERR_INVALID_ARG, "%s: margin outside [-126, 126]", fn);
+    if (!aligned4(history) || !aligned4(head) || !aligned4(amax) || !aligned4(scale))
+        return fail(FP8BS_ERR_MISALIGNED, "%s: scalars must be 4-byte aligned", fn);
+    cudaError_t e = fp8bs::launch_amax_history(history, head, history_len, amax, fmt, margin, scale,
+                                               (cudaStream_t)stream);
+    return e == cudaSuccess ? FP8BS_OK : cuda_fail(e, fn);
+}
+
+int fp8_block_gemm(int64_t M, int64_t N, int64_t K, const fp8bs_operand* A,
+                   const fp8bs_operand* B, int32_t mode, void* Y, int64_t ld_y, int32_t out_dtype,
+                   fp8bs_stream_t stream) {
+    return run_gemm("fp8_block_gemm", 1, nullptr, M, M, N, K, A, B, mode, Y, ld_y, out_dtype,
+                    (cudaStream_t)stream);
+}
+
+int fp8_grouped_block_gemm(int32_t num_groups, const int32_t* row_offsets, int64_t a_rows,
+                           int64_t N, int64_t K, const fp8bs_operand* A, const fp8bs_operand* B,
+                           int32_t mode, void* Y, int64_t ld_y, int32_t out_dtype,
+                           fp8bs_stream_t stream) {
+    if (!row_offsets) return fail(FP8BS_ERR_INVALID_ARG, "fp8_grouped_block_gemm: null row_offsets");
+    if (!aligned4(row_offsets)) return fail(FP8BS_ERR_MISALIGNED, "fp8_grouped_block_gemm: offsets");
+    return run_gemm("fp8_grouped_block_gemm", num_groups, row_offsets, a_rows, a_rows, N, K, A, B,
+                    mode, Y, ld_y, out_dtype, (cudaStream_t)stream);
+}
+
+int fp8bs_device_status(fp8bs_stream_t stream) {
+    cudaError_t e = cudaStreamSynchronize((cudaStream_t)stream);
+    if (e != cudaSuccess) return cuda_fail(e, "fp8bs_device_status");
+    int st = 0;
+    e = fp8bs::read_and_clear_status(&st);
+    if (e != cudaSuccess) return cuda_fail(e, "fp8bs_device_status");
+    if (st != 0) return fail(FP8BS_ERR_DEVICE_TIMEOUT, "a kernel gave up on a bounded device wait");
+    return FP8BS_OK;
+}
+
+}  // extern "C"

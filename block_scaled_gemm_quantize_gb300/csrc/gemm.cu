@@ -1,0 +1,421 @@
+// gemm.cu -- block-scaled FP8 GEMM on sm_103a tensor cores (tcgen05 + TMA + TMEM).
+//
+// Y = deq(A) . deq(B)^T with fp32 accumulation: the product of the FP8 linear
+// layer ("NVIDIA NeMo RL logra una aceleracion del 48%...", hotbookzone.com,
+// "El avance tecnico": 1x128 activation tiles and 128x128 weight tiles, E4M3,
+// linear layers in FP8 math) for fprop, dgrad, wgrad and the grouped
+// (mixture-of-experts) form.
+//
+// Kernel design (one persistent CTA per SM, 3 warpgroups = 12 warps):
+//   warp 0      TMA producer: per 128-deep K block, one 128x128 A tile and
+//               one 256x128 B tile (8-bit, 128-byte swizzle) into a 4-stage
+//               shared-memory ring.
+//   warp 1      TMEM owner and MMA issuer: 4 x tcgen05.mma.kind::f8f6f4
+//               (M=128, N=256, K=32) per K block into a TMEM partial buffer.
+//   warps 2,3   idle (they complete the first warpgroup).
+//   warps 4..11 epilogue ("promotion"): each thread owns one output row (its
+//               TMEM lane) and 128 columns; per K block it loads the fp32
+//               partial from TMEM and folds it into fp32 registers with that
+//               block's two scales: acc = fma(partial, sA * sB, acc).
+// Register split (setmaxnreg): the block launches with 168 registers per
+// thread (384 x 168 = 64512); the first warpgroup releases down to 72 and the
+// two epilogue warpgroups grow to 216: 128 x 72 + 256 x 216 = 64512.
+// (An MN-major B runs as two N=128 MMAs per K step.)
+// Two TMEM partial buffers (2 x 256 columns) let the MMAs of block kb+1 run
+// while block kb is promoted.  When both operands have one scale per tensor
+// the whole K accumulates in TMEM and is scaled once ("promote every K").
+// Operands may be stored K-major or MN-major (transposed storage, used by
+// dgrad/wgrad); the instruction descriptor's major bits and the shared-memory
+// descriptor strides select the layout.
+//
+// Every mbarrier wait is bounded (a few seconds of %globaltimer); a role
+// that gives up records FP8BS_ERR_DEVICE_TIMEOUT in g_status, waits (bounded)
+// for its own asynchronous work and leaves; TMEM is always freed.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <cstdint>
+
+#include "gemm_kernels.h"
+#include "ptx_sm100.cuh"
+
+namespace fp8bs {
+
+__device__ int g_status;  // 0 = ok, else a negative fp8bs status
+
+namespace {
+
+constexpr int BM = 128, BN = 256, BK = 128;
+constexpr int STAGES = 4;
+constexpr uint32_t A_STAGE = BM * BK;   // 16 KiB
+constexpr uint32_t B_STAGE = BN * BK;   // 32 KiB
+constexpr uint32_t STAGE_BYTES = A_STAGE + B_STAGE;
+constexpr int NUM_THREADS = 384;
+constexpr int EPI_WARP0 = 4;
+constexpr int REGS_LOW = 72, REGS_HIGH = 216;   // 128*72 + 256*216 == 384*168
+constexpr int NUM_EPI_WARPS = 8;
+constexpr uint32_t TMEM_COLS = 512;
+constexpr int RASTER_M = 16;            // m-slots per rasterization group
+constexpr uint64_t WAIT_LIMIT_NS = 4000000000ull;
+constexpr uint64_t DRAIN_LIMIT_NS = 200000000ull;
+
+// Shared memory: [align pad][A ring][B ring][barriers][tmem addr][group tables]
+constexpr uint32_t BAR_OFF = STAGES * STAGE_BYTES;
+constexpr int NUM_BARS = 2 * STAGES + 4 + 1;   // full, empty, tfull[2], tempty[2], done
+constexpr uint32_t TMEMSLOT_OFF = BAR_OFF + NUM_BARS * 8;
+constexpr uint32_t TABLE_OFF = (TMEMSLOT_OFF + 16 + 15) & ~15u;
+constexpr uint32_t SMEM_BYTES = 1024 + TABLE_OFF + 2 * (kMaxGroups + 1) * 4;
+
+__device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = global_timer_ns();
+    uint32_t n = 0;
+    while (true) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((++n & 63u) == 0 && global_timer_ns() - t0 > limit_ns) return false;
+    }
+}
+
+__device__ __forceinline__ bool wait_or_flag(uint32_t bar, uint32_t parity) {
+    if (wait_bounded(bar, parity, WAIT_LIMIT_NS)) return true;
+    atomicExch(&g_status, kStatusDeviceTimeout);
+    return false;
+}
+
+struct Tile {
+    int g, row0, row_end, nt;
+};
+
+// Tile t -> (group, first row, row limit, n-tile).  Tiles are rasterized in
+// groups of RASTER_M m-slots: consecutive tiles walk the m-slots of a group
+// first, then the n-tiles, so the CTAs in flight share A and B tiles in L2.
+__device__ __forceinline__ Tile decode_tile(int t, int total_slots, int tiles_n, int G,
+                                            const int* s_slot, const int* s_off) {
+    const int per = RASTER_M * tiles_n;
+    const int gm = t / per;
+    const int r = t - gm * per;
+    const int slot0 = gm * RASTER_M;
+    const int gsz = min(RASTER_M, total_slots - slot0);
+    const int nt = r / gsz;
+    const int slot = slot0 + (r - nt * gsz);
+    int lo = 0, hi = G;  // largest g with s_slot[g] <= slot
+    while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (s_slot[mid] <= slot) lo = mid; else hi = mid;
+    }
+    Tile tl;
+    tl.g = lo;
+    tl.row0 = s_off[lo] + (slot - s_slot[lo]) * BM;
+    tl.row_end = s_off[lo + 1];
+    tl.nt = nt;
+    return tl;
+}
+
+__device__ __forceinline__ float ld_scale(const float* p) { return __ldg(p); }
+
+template <bool A_MN, bool B_MN>
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+    k_fp8_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+               const GemmParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    uint8_t* smem = smem_raw + ((1024u - (raw & 1023u)) & 1023u);
+    const uint32_t sbase = smem_u32(smem);
+    const uint32_t sA = sbase;
+    const uint32_t sB = sbase + STAGES * A_STAGE;
+    const uint32_t bars = sbase + BAR_OFF;
+    auto full_bar = [&](int s) { return bars + 8u * s; };
+    auto empty_bar = [&](int s) { return bars + 8u * (STAGES + s); };
+    auto tfull_bar = [&](int b) { return bars + 8u * (2 * STAGES + b); };
+    auto tempty_bar = [&](int b) { return bars + 8u * (2 * STAGES + 2 + b); };
+    const uint32_t done_bar = bars + 8u * (2 * STAGES + 4);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + TMEMSLOT_OFF);
+    int* s_off = reinterpret_cast<int*>(smem + TABLE_OFF);
+    int* s_slot = s_off + (kMaxGroups + 1);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int G = p.num_groups;
+
+    if (warp == 0 && lane == 0) {
+        tma_prefetch_desc(&tmA);
+        tma_prefetch_desc(&tmB);
+        for (int s = 0; s < STAGES; s++) {
+            mbar_init(full_bar(s), 1);
+            mbar_init(empty_bar(s), 1);
+        }
+        for (int b = 0; b < 2; b++) {
+            mbar_init(tfull_bar(b), 1);
+            mbar_init(tempty_bar(b), NUM_EPI_WARPS);
+        }
+        mbar_init(done_bar, 1);
+        fence_mbar_init();
+        fence_proxy_async_smem();
+    }
+    if (warp == 1) tmem_alloc(smem_u32(tmem_slot), TMEM_COLS);
+    // group table: row offsets and the prefix count of 128-row m-slots
+    // (row offsets are clamped into [0, a_rows], so no tile ever stores
+    // outside Y whatever the device table holds)
+    for (int i = threadIdx.x; i <= G; i += NUM_THREADS) {
+        const int64_t o = p.offsets ? static_cast<int64_t>(p.offsets[i]) : (i == 0 ? 0 : p.M);
+        s_off[i] = static_cast<int>(o < 0 ? 0 : (o > p.a_rows ? p.a_rows : o));
+    }
+    __syncthreads();
+    if (warp == 2) {
+        int carry = 0;
+        if (lane == 0) s_slot[0] = 0;
+        for (int base = 0; base < G; base += 32) {
+            const int g = base + lane;
+            int cnt = 0;
+            if (g < G) {
+                const int rows = max(0, s_off[g + 1] - s_off[g]);
+                cnt = (rows + BM - 1) / BM;
+            }
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int v = __shfl_up_sync(0xFFFFFFFFu, cnt, o);
+                if (lane >= o) cnt += v;
+            }
+            if (g < G) s_slot[g + 1] = carry + cnt;
+            carry += __shfl_sync(0xFFFFFFFFu, cnt, 31);
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+    const int total_slots = s_slot[G];
+    const int total_tiles = total_slots * p.tiles_n;
+    const int nkb = static_cast<int>(p.K / BK);
+    const int P = p.promote ? 1 : nkb;  // K blocks per TMEM partial
+
+    if (warp < EPI_WARP0) {
+      asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(REGS_LOW));
+      if (warp == 0) {
+        // ------------------------------------------------------ producer
+        if (lane == 0) {
+            int stage = 0;
+            uint32_t phase = 0;
+            bool ok = true;
+            int issued = 0;
+            for (int t = blockIdx.x; ok && t < total_tiles; t += gridDim.x) {
+                const Tile tl = decode_tile(t, total_slots, p.tiles_n, G, s_slot, s_off);
+                const int a_row = tl.row0;
+                const int b_row = tl.g * p.b_rows_per_group + tl.nt * BN;
+                for (int kb = 0; kb < nkb; kb++) {
+                    if (!wait_or_flag(empty_bar(stage), phase ^ 1u)) { ok = false; break; }
+                    mbar_arrive_expect_tx(full_bar(stage), STAGE_BYTES);
+                    const int kc = kb * BK;
+                    const uint32_t dA = sA + stage * A_STAGE, dB = sB + stage * B_STAGE;
+                    if (A_MN) tma_load_2d(dA, &tmA, a_row, kc, full_bar(stage));
+                    else tma_load_2d(dA, &tmA, kc, a_row, full_bar(stage));
+                    if (B_MN) {
+                        tma_load_2d(dB, &tmB, b_row, kc, full_bar(stage));
+                        tma_load_2d(dB + B_STAGE / 2, &tmB, b_row + 128, kc, full_bar(stage));
+                    } else {
+                        tma_load_2d(dB, &tmB, kc, b_row, full_bar(stage));
+                    }
+                    issued++;
+                    if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+                }
+            }
+            if (!ok) {
+                // drain: wait for the copies this thread issued on each stage
+                for (int i = 0; i < STAGES && i < issued; i++) {
+                    if (--stage < 0) { stage = STAGES - 1; phase ^= 1u; }
+                    wait_bounded(full_bar(stage), phase, DRAIN_LIMIT_NS);
+                }
+            }
+        }
+    } else if (warp == 1) {
+        // ---------------------------------------------------------- MMA
+        if (lane == 0) {
+            int stage = 0;
+            uint32_t phase = 0, chunk = 0;
+            bool ok = true, issued_mma = false;
+            for (int t = blockIdx.x; ok && t < total_tiles; t += gridDim.x) {
+                for (int kb = 0; kb < nkb; kb++) {
+                    const uint32_t buf = chunk & 1u;
+                    if (kb % P == 0) {
+                        if (!wait_or_flag(tempty_bar(buf), ((chunk >> 1) & 1u) ^ 1u)) { ok = false; break; }
+                    }
+                    if (!wait_or_flag(full_bar(stage), phase)) { ok = false; break; }
+                    tc_fence_after();
+                    const uint32_t d = tmem_base + buf * BN;
+                    const uint32_t aS = sA + stage * A_STAGE, bS = sB + stage * B_STAGE;
+#pragma unroll
+                    for (int k4 = 0; k4 < BK / 32; k4++) {
+                        // K-major: 32 K-bytes further inside the 128-byte swizzled row,
+                        // 8-row groups 1024 B apart (SBO).  MN-major: 32 K-rows further
+                        // (4 swizzle atoms of 8 K-rows x 128 B, 1024 B apart); every
+                        // MN-major descriptor spans a single 128-wide atom, so its
+                        // MN-atom stride is never used and both offsets are 1024.
+                        const uint64_t ad = A_MN ? smem_desc_sw128(aS + k4 * 4096, 1024, 1024)
+                                                 : smem_desc_sw128(aS + k4 * 32, 16, 1024);
+                        const uint32_t acc = (k4 > 0 || kb % P != 0) ? 1u : 0u;
+                        if (B_MN) {
+                            // two N=128 halves, one TMA box each
+                            mma_f8f6f4(d, ad, smem_desc_sw128(bS + k4 * 4096, 1024, 1024),
+                                       p.idesc, acc);
+                            mma_f8f6f4(d + 128, ad,
+                                       smem_desc_sw128(bS + B_STAGE / 2 + k4 * 4096, 1024, 1024),
+                                       p.idesc, acc);
+                        } else {
+                            mma_f8f6f4(d, ad, smem_desc_sw128(bS + k4 * 32, 16, 1024), p.idesc, acc);
+                        }
+                        issued_mma = true;
+                    }
+                    mma_commit(empty_bar(stage));
+                    if (kb % P == P - 1) {
+                        mma_commit(tfull_bar(buf));
+                        chunk++;
+                    }
+                    if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+                }
+            }
+            // after a timeout, let the MMAs already issued finish before TMEM
+            // is released (on the normal path the epilogue consumed them all)
+            if (!ok && issued_mma) {
+                mma_commit(done_bar);
+                wait_bounded(done_bar, 0, DRAIN_LIMIT_NS);
+            }
+        }
+      }
+    } else {
+        asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(REGS_HIGH));
+        // ----------------------------------------------------- epilogue
+        const int quarter = warp & 3;           // TMEM lanes 32*quarter ..
+        const int half = (warp - EPI_WARP0) >> 2;  // columns 128*half ..
+        const int lrow = quarter * 32 + lane;
+        uint32_t chunk = 0;
+        bool ok = true;
+        const int64_t nkb64 = nkb;
+        for (int t = blockIdx.x; ok && t < total_tiles; t += gridDim.x) {
+            const Tile tl = decode_tile(t, total_slots, p.tiles_n, G, s_slot, s_off);
+            const int64_t row = static_cast<int64_t>(tl.row0) + lrow;
+            const bool row_ok = row < tl.row_end;
+            const int64_t srow = row < p.a_rows ? row : p.a_rows - 1;   // clamp for scale reads
+            const int64_t col0 = static_cast<int64_t>(tl.nt) * BN + half * 128;
+            const int64_t nb = min(col0, p.N - 1) / 128;                // weight row-block
+            // scale pointers for this (row, column block); advanced per K block
+            const float* pa;
+            int64_t sa_step;
+            if (p.a_gran == 0) { pa = p.sa + srow; sa_step = p.a_rows; }
+            else if (p.a_gran == 1) {
+                if (A_MN) { pa = p.sa + srow / 128; sa_step = p.a_rblocks; }
+                else { pa = p.sa + (srow / 128) * nkb64; sa_step = 1; }
+            } else { pa = p.sa; sa_step = 0; }
+            const float* pb;
+            int64_t sb_step;
+            if (p.b_gran == 1) {
+                if (B_MN) { pb = p.sb + nb; sb_step = p.b_rblocks; }
+                else { pb = p.sb + tl.g * p.b_scale_group_stride + nb * nkb64; sb_step = 1; }
+            } else { pb = p.sb; sb_step = 0; }
+
+            float acc[128];
+#pragma unroll
+            for (int i = 0; i < 128; i++) acc[i] = 0.0f;
+            float sa_next = ld_scale(pa), sb_next = ld_scale(pb);
+            for (int kb = 0; kb < nkb; kb += P) {
+                const float s = sa_next * sb_next;
+                if (kb + P < nkb) {
+                    sa_next = ld_scale(pa + (kb + P) * sa_step);
+                    sb_next = ld_scale(pb + (kb + P) * sb_step);
+                }
+                const uint32_t buf = chunk & 1u;
+                ok = __all_sync(0xFFFFFFFFu, wait_or_flag(tfull_bar(buf), (chunk >> 1) & 1u));
+                if (!ok) break;
+                tc_fence_after();
+                const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
+                                       buf * BN + half * 128;
+#pragma unroll
+                for (int j = 0; j < 4; j++) {
+                    uint32_t r[32];
+                    tmem_ld_32x32b_x32(taddr + j * 32, r);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int i = 0; i < 32; i++)
+                        acc[j * 32 + i] = __fmaf_rn(__uint_as_float(r[i]), s, acc[j * 32 + i]);
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(tempty_bar(buf));
+                chunk++;
+            }
+            if (!ok) break;
+            if (row_ok) {
+                if (p.out_bf16) {
+                    uint16_t* y = reinterpret_cast<uint16_t*>(p.y) + row * p.ldy + col0;
+#pragma unroll
+                    for (int j = 0; j < 128; j += 8) {
+                        if (col0 + j < p.N) {
+                            uint32_t w[4];
+#pragma unroll
+                            for (int i = 0; i < 4; i++) {
+                                __nv_bfloat162 h = __floats2bfloat162_rn(acc[j + 2 * i], acc[j + 2 * i + 1]);
+                                w[i] = *reinterpret_cast<uint32_t*>(&h);
+                            }
+                            *reinterpret_cast<uint4*>(y + j) = make_uint4(w[0], w[1], w[2], w[3]);
+                        }
+                    }
+                } else {
+                    float* y = reinterpret_cast<float*>(p.y) + row * p.ldy + col0;
+#pragma unroll
+                    for (int j = 0; j < 128; j += 4) {
+                        if (col0 + j < p.N)
+                            *reinterpret_cast<float4*>(y + j) =
+                                make_float4(acc[j], acc[j + 1], acc[j + 2], acc[j + 3]);
+                    }
+                }
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem_base, TMEM_COLS);
+    }
+}
+
+}  // namespace
+
+uint32_t gemm_smem_bytes() { return SMEM_BYTES; }
+
+// kind::f8f6f4 instruction descriptor: D fp32 (bits 4-5 = 1), A/B formats
+// (bits 7-9, 10-12: E4M3 = 0, E5M2 = 1), A/B major (bits 15, 16: 1 = MN),
+// N >> 3 (bits 17-22), M >> 4 (bits 24-28).
+uint32_t make_idesc_f8f6f4(int a_fmt, int b_fmt, bool a_mn, bool b_mn, int n) {
+    uint32_t d = 0;
+    d |= 1u << 4;
+    d |= static_cast<uint32_t>(a_fmt & 7) << 7;
+    d |= static_cast<uint32_t>(b_fmt & 7) << 10;
+    d |= (a_mn ? 1u : 0u) << 15;
+    d |= (b_mn ? 1u : 0u) << 16;
+    d |= static_cast<uint32_t>(n >> 3) << 17;
+    d |= static_cast<uint32_t>(BM >> 4) << 24;
+    return d;
+}
+
+int gemm_tile_n() { return BN; }
+int gemm_tile_m() { return BM; }
+
+cudaError_t launch_fp8_gemm(const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmParams& p,
+                            bool a_mn, bool b_mn, int grid, cudaStream_t st) {
+    auto k = a_mn ? (b_mn ? k_fp8_gemm<true, true> : k_fp8_gemm<true, false>)
+                  : (b_mn ? k_fp8_gemm<false, true> : k_fp8_gemm<false, false>);
+    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    k<<<grid, NUM_THREADS, SMEM_BYTES, st>>>(tmA, tmB, p);
+    return cudaGetLastError();
+}
+
+cudaError_t read_and_clear_status(int* status) {
+    int zero = 0;
+    cudaError_t e = cudaMemcpyFromSymbol(status, g_status, sizeof(int));
+    if (e != cudaSuccess) return e;
+    return cudaMemcpyToSymbol(g_status, &zero, sizeof(int));
+}
+
+}  // namespace fp8bs

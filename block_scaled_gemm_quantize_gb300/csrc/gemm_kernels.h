@@ -1,0 +1,41 @@
+// gemm_kernels.h -- launch interface of the tcgen05 FP8 GEMM (gemm.cu),
+// called by the C ABI layer after argument validation.
+#pragma once
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cstdint>
+
+namespace fp8bs {
+
+constexpr int kMaxGroups = 1024;
+constexpr int kStatusDeviceTimeout = -5;
+
+struct GemmParams {
+    int64_t M, N, K;          // logical product size (M = rows of A as stored)
+    int64_t a_rows;           // rows of A as stored: 1x128 scale table stride
+    int64_t a_rblocks;        // ceil(M / 128): transposed 128x128 A scale stride
+    int64_t b_rblocks;        // ceil(N / 128): transposed 128x128 B scale stride
+    int64_t b_scale_group_stride;  // floats between groups' B scale tables
+    const float* sa;
+    const float* sb;
+    const int32_t* offsets;   // device [num_groups + 1] or null (one group [0, M))
+    void* y;
+    int64_t ldy;
+    int32_t num_groups;
+    int32_t b_rows_per_group; // rows of the B tensor map per group (grouped: N)
+    int32_t a_gran, b_gran;   // fp8bs_granularity
+    int32_t tiles_n;
+    int32_t promote;          // 1: scale per 128-K block; 0: one scale per tensor pair
+    int32_t out_bf16;
+    uint32_t idesc;
+};
+
+uint32_t gemm_smem_bytes();
+uint32_t make_idesc_f8f6f4(int a_fmt, int b_fmt, bool a_mn, bool b_mn, int n);
+int gemm_tile_n();
+int gemm_tile_m();
+cudaError_t launch_fp8_gemm(const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmParams& p,
+                            bool a_mn, bool b_mn, int grid, cudaStream_t st);
+cudaError_t read_and_clear_status(int* status);
+
+}  // namespace fp8bs

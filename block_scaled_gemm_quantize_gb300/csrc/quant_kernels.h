@@ -1,0 +1,18 @@
+// quant_kernels.h -- launchers of the quantizer kernels (quant.cu), called
+// by the C ABI layer after argument validation.
+#pragma once
+#include <cuda_runtime.h>
+#include <cstdint>
+
+namespace fp8bs {
+cudaError_t launch_quant_1x128(const uint16_t* x, int64_t rows, int64_t cols, int64_t ldx,
+                               int fmt, int mode, uint8_t* q, int64_t ldq, float* scales,
+                               cudaStream_t st);
+cudaError_t launch_quant_128x128(const uint16_t* w, int64_t rows, int64_t cols, int64_t ldw,
+                                 int fmt, int mode, uint8_t* q, int64_t ldq, float* scales,
+                                 cudaStream_t st);
+cudaError_t launch_quant_tensor(const uint16_t* x, int64_t n, int fmt, const float* scale,
+                                uint8_t* q, float* amax_out, cudaStream_t st);
+cudaError_t launch_amax_history(float* history, int32_t* head, int32_t L, const float* amax,
+                                int fmt, int32_t margin, float* scale, cudaStream_t st);
+}  // namespace fp8bs

@@ -1,0 +1,215 @@
+/*
+ * fp8bs.h -- C ABI of the GB300 (sm_103a) FP8 linear-layer library.
+ *
+ * The method: the FP8 linear layer of block-scaled FP8 training.  Linear
+ * layers run their products in FP8 while attention, normalisation and
+ * non-linear layers stay in bf16; weights are block-quantized to E4M3 with
+ * 128x128 tiles and activations with 1x128 tiles ("NVIDIA NeMo RL logra una
+ * aceleracion del 48%...", hotbookzone.com, section "El avance tecnico").
+ * E4M3 (up to +-448) carries forward activations and weights and E5M2 the
+ * gradients; per-tensor delayed scaling takes the scale from the amax history
+ * of earlier iterations ("Infraestructura de Entrenamiento FP8", introl.com,
+ * sections "El panorama de la precision numerica" and "Transformer Engine: la
+ * base de software").
+ *
+ * Conventions (all entry points):
+ *   - Every pointer is a DEVICE pointer unless stated otherwise.  The caller
+ *     allocates and owns every buffer; the library never allocates device
+ *     memory, frees it or keeps a pointer after the call returns.
+ *   - Calls are asynchronous on `stream` (a cudaStream_t; NULL = the legacy
+ *     default stream).  A return value other than FP8BS_OK means nothing was
+ *     launched; fp8bs_last_error() then describes the problem.
+ *   - bf16 inputs are raw bf16 bit patterns (2 bytes per element).
+ *   - FP8 data are raw 8-bit codes.  E4M3 is the "FN" variant (no infinities,
+ *     max 448, NaN = S.1111.111); E5M2 has IEEE infinities, max 57344.
+ *   - Scales are DEQUANTIZATION multipliers: value = decode(code) * scale.
+ *   - Encoding rounds to nearest, ties to even, and saturates finite overflow
+ *     and infinities to +-max; the element computed is fp32(x * fp32(1/s)).
+ *   - Alignment: data pointers 16-byte aligned, leading dimensions (in
+ *     bytes) multiples of 16; otherwise FP8BS_ERR_MISALIGNED.
+ *   - Contraction lengths (columns of a quantized matrix, K of a product) must
+ *     be multiples of 128; otherwise FP8BS_ERR_UNSUPPORTED.  Empty inputs
+ *     (a zero dimension) are valid and launch nothing, except a product with
+ *     K == 0, which writes zeros to Y.
+ *   - Device-side waits are bounded; a kernel that gives up records it in a
+ *     per-process status word read by fp8bs_device_status().
+ */
+#ifndef FP8BS_H
+#define FP8BS_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* fp8bs_stream_t;   /* same type as cudaStream_t */
+
+enum fp8bs_status {
+    FP8BS_OK = 0,
+    FP8BS_ERR_INVALID_ARG = -1,     /* null pointer, bad enum, bad size */
+    FP8BS_ERR_UNSUPPORTED = -2,     /* valid request this library does not run */
+    FP8BS_ERR_MISALIGNED = -3,      /* pointer or leading dimension alignment */
+    FP8BS_ERR_CUDA = -4,            /* CUDA runtime/driver error (message kept) */
+    FP8BS_ERR_DEVICE_TIMEOUT = -5   /* a bounded device-side wait expired */
+};
+
+enum fp8bs_format { FP8BS_E4M3 = 0, FP8BS_E5M2 = 1 };
+enum fp8bs_scale_mode { FP8BS_SCALE_FP32 = 0, FP8BS_SCALE_POW2 = 1 };
+enum fp8bs_out_dtype { FP8BS_OUT_F32 = 0, FP8BS_OUT_BF16 = 1 };
+enum fp8bs_granularity { FP8BS_GRAN_1x128 = 0, FP8BS_GRAN_128x128 = 1, FP8BS_GRAN_TENSOR = 2 };
+
+/* ------------------------------------------------------------ quantizers */
+
+/*
+ * Activation quantizer, one scale per 1x128 tile ("1x128" granularity for
+ * activations, hotbookzone.com "El avance tecnico").
+ *   x      [rows][ld_x] bf16, the 128-element tiles run along each row.
+ *   q      [rows][ld_q] 8-bit codes (output).
+ *   scales [cols/128][rows] fp32, rows contiguous (output).
+ * Per tile: amax = max|x|; s = amax/fmax in fp32 (mode FP32; amax == 0 gives
+ * 1, floor 2^-126) or the smallest power of two 2^e, e in [-126, 127], with
+ * amax <= fmax * 2^e (mode POW2; the power-of-two option of hotbookzone.com
+ * "Por que esto es importante..."); q = enc(x * (1/s)).
+ * fmt selects E4M3 (fmax 448) or E5M2 (fmax 57344).
+ * Errors: INVALID_ARG (nulls, rows/cols < 0, ld < cols, bad enum),
+ * UNSUPPORTED (cols % 128), MISALIGNED (x, q not 16-byte aligned, ld_x*2 or
+ * ld_q not a multiple of 16, scales not 4-byte aligned).
+ */
+int fp8_quantize_1x128(const void* x, int64_t rows, int64_t cols, int64_t ld_x,
+                       int32_t fmt, int32_t mode,
+                       uint8_t* q, int64_t ld_q, float* scales, fp8bs_stream_t stream);
+
+/*
+ * Weight quantizer, one scale per 128x128 tile ("128x128" granularity for
+ * weights, hotbookzone.com "El avance tecnico").  Weights are re-quantized
+ * after every optimizer step ("Ganancias de rendimiento en el mundo real").
+ *   w      [rows][ld_w] bf16;  q [rows][ld_q] codes (output);
+ *   scales [ceil(rows/128)][cols/128] fp32 (output).
+ * A last row-tile with fewer than 128 rows covers only the rows that exist.
+ * Scale and element rules as fp8_quantize_1x128, over the whole tile.
+ * Errors as fp8_quantize_1x128.
+ */
+int fp8_quantize_128x128(const void* w, int64_t rows, int64_t cols, int64_t ld_w,
+                         int32_t fmt, int32_t mode,
+                         uint8_t* q, int64_t ld_q, float* scales, fp8bs_stream_t stream);
+
+/*
+ * Per-tensor delayed-scaling quantizer ("Escalado diferido", introl.com
+ * "Estrategias de escalado y estabilidad"; recipe of "Transformer Engine: la
+ * base de software").  Quantizes with the scale already in use, built from
+ * earlier steps only, and measures this step's amax for the history:
+ *   q[i] = enc(x[i] * fp32(1 / *scale));  *amax_out = max_i |x[i]|.
+ *   x        [numel] bf16, contiguous;  q [numel] codes (output);
+ *   scale    device scalar, the dequantization scale in use (read);
+ *   amax_out device scalar (written, not accumulated).
+ * The hybrid recipe uses fmt E5M2 for gradients and E4M3 for activations
+ * and weights.  Errors: INVALID_ARG, MISALIGNED (x, q 16-byte aligned).
+ */
+int fp8_quantize_tensor_delayed(const void* x, int64_t numel, int32_t fmt,
+                                const float* scale, uint8_t* q, float* amax_out,
+                                fp8bs_stream_t stream);
+
+/*
+ * Delayed-scaling state update (fields margin, amax_history_len and
+ * amax_compute_algo = "max" of the recipe on introl.com "Transformer Engine:
+ * la base de software"):
+ *   history[*head] = *amax; *head = (*head + 1) % history_len;
+ *   amax_h = max(history[0..history_len));
+ *   t = fp32(fp32(amax_h / fmax) * 2^margin);
+ *   if amax_h > 0 and t is finite: *scale = max(t, 2^-126), else unchanged.
+ *   history [history_len] fp32, head int32 scalar, scale fp32 scalar: all
+ *   device memory, read and written in place; amax: device scalar (read).
+ * A fresh state is history = 0, head = 0, scale = 1.
+ * Errors: INVALID_ARG (nulls, history_len < 1, margin outside [-126, 126]).
+ */
+int fp8_amax_history_update(float* history, int32_t* head, int32_t history_len,
+                            const float* amax, int32_t fmt, int32_t margin,
+                            float* scale, fp8bs_stream_t stream);
+
+/* ---------------------------------------------------------------- GEMM */
+
+/*
+ * One FP8 operand of Y = deq(A) . deq(B)^T.  Logical shape [rows][K]
+ * (rows = M for A, N for B).
+ *   transposed = 0: stored [rows][ld], K contiguous ("K-major").
+ *   transposed = 1: stored [K][ld], rows contiguous ("MN-major"), as in the
+ *                   backward products (dgrad reads W and wgrad reads dY and X
+ *                   across their stored rows).
+ * Scale tables (fp32), in the orientation of the stored matrix:
+ *   GRAN_1x128   (transposed = 0 only, A only): [K/128][rows]
+ *   GRAN_128x128, transposed = 0: [ceil(rows/128)][K/128]
+ *   GRAN_128x128, transposed = 1: [K/128][ceil(rows/128)]
+ *   GRAN_TENSOR: one value.
+ */
+typedef struct {
+    const uint8_t* data;
+    int64_t ld;            /* elements (= bytes) between stored rows */
+    int32_t transposed;
+    int32_t fmt;           /* fp8bs_format */
+    int32_t gran;          /* fp8bs_granularity */
+    int32_t reserved;      /* must be 0 */
+    const float* scales;
+} fp8bs_operand;
+
+/*
+ * Block-scaled FP8 product with fp32 accumulation (the FP8 linear layer's
+ * product, hotbookzone.com "El avance tecnico"):
+ *   Y[m][n] = sum_k decode(A[m][k]) sA(m,k) * decode(B[n][k]) sB(n,k)
+ * fprop: A = Xq (1x128), B = Wq (128x128).  dgrad: A = dYq, B = Wq stored
+ * transposed.  wgrad: A = dYq^T, B = Xq^T, both stored transposed.
+ * A and B may use different formats (E5M2 gradients x E4M3 weights).
+ * Partial products of each 128-long K block are accumulated in fp32 and
+ * promoted with that block's two scales into an fp32 accumulator.
+ *   mode = POW2 declares that every scale is an exact power of two in
+ *   [2^-126, 2^127] (from the POW2 quantizers); the result is the same sum.
+ *   Y [M][ld_y], fp32 or bf16 (round to nearest even), written, not
+ *   accumulated.
+ * Errors: INVALID_ARG, UNSUPPORTED (K % 128, N % 8, GRAN_1x128 on B or on a
+ * transposed operand), MISALIGNED (data 16-byte aligned, ld % 16, Y 16-byte
+ * aligned with ld_y * element size a multiple of 16).
+ */
+int fp8_block_gemm(int64_t M, int64_t N, int64_t K,
+                   const fp8bs_operand* A, const fp8bs_operand* B,
+                   int32_t mode, void* Y, int64_t ld_y, int32_t out_dtype,
+                   fp8bs_stream_t stream);
+
+/*
+ * Grouped product for mixture-of-experts expert GEMMs (the FP8 recipe on a
+ * mixture-of-experts model, hotbookzone.com "Ganancias de rendimiento en el
+ * mundo real"): for each group g the rows [row_offsets[g], row_offsets[g+1])
+ * of A are multiplied by expert g's weights.
+ *   row_offsets     device int32 [num_groups + 1], non-decreasing,
+ *                   row_offsets[0] = 0, row_offsets[G] <= a_rows.
+ *   a_rows          rows of A as stored (its 1x128 scale table is
+ *                   [K/128][a_rows]); sizes the launch on the host.
+ *   A               [a_rows][K], transposed = 0, GRAN_1x128 or GRAN_TENSOR.
+ *   B               [G][N][K] stored as one [G*N][ld] matrix, transposed = 0,
+ *                   GRAN_128x128 (scales [G][ceil(N/128)][K/128]) or
+ *                   GRAN_TENSOR (one value for all groups).
+ *   Y               [a_rows][ld_y]; rows outside every group are not written.
+ * Errors as fp8_block_gemm; num_groups in [1, 1024].
+ */
+int fp8_grouped_block_gemm(int32_t num_groups, const int32_t* row_offsets, int64_t a_rows,
+                           int64_t N, int64_t K,
+                           const fp8bs_operand* A, const fp8bs_operand* B,
+                           int32_t mode, void* Y, int64_t ld_y, int32_t out_dtype,
+                           fp8bs_stream_t stream);
+
+/* ------------------------------------------------------------ diagnostics */
+
+/* Message for the last non-OK status returned on the calling host thread. */
+const char* fp8bs_last_error(void);
+
+/* Synchronizes `stream`, then returns FP8BS_ERR_DEVICE_TIMEOUT if any kernel
+ * of this library gave up on a bounded wait since the last call (and clears
+ * the record), FP8BS_ERR_CUDA on a CUDA error, else FP8BS_OK. */
+int fp8bs_device_status(fp8bs_stream_t stream);
+
+/* Library version, for the binding's load check. */
+int fp8bs_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* FP8BS_H */

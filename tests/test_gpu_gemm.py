@@ -1,0 +1,193 @@
+"""Parity of the tcgen05 block-scaled GEMM with the oracle.
+
+Inputs are quantized by the ORACLE and uploaded, so the GEMM is checked on
+its own.  fp32 output: |y - y_ref| <= 1e-5 * sum_k |terms| per element;
+bf16 output: within one bf16 step of the rounding of a value inside that
+bound (see oracle.check_bf16)."""
+import numpy as np
+import pytest
+
+import block_scaled_gemm_quantize_gb300 as fp8
+import oracle as orc
+from block_scaled_gemm_quantize_gb300 import inputs
+from helpers import dev, host, stratified
+
+pytestmark = pytest.mark.gpu
+REL = 1e-5
+
+
+def _quant(bits, gran, fmt, mode):
+    if gran == orc.GRAN_1x128:
+        return orc.quantize_1x128(bits, fmt, mode)
+    if gran == orc.GRAN_128x128:
+        return orc.quantize_128x128(bits, fmt, mode)
+    amax = float(np.abs(inputs.bits_to_f32(bits)).max())
+    s = orc.block_scale(amax, fmt, mode)
+    q, _ = orc.quantize_tensor(bits, fmt, s)
+    return q, np.float32([s])
+
+
+def _check(y_dev, y_ref, yabs, out_dtype, rows=None, cols=None):
+    y = host(y_dev)
+    if rows is not None:
+        y = y[np.ix_(rows, cols)]
+    if out_dtype == fp8.OUT_F32:
+        bad = orc.check_f32(y, y_ref, yabs, REL)
+    else:
+        bad = orc.check_bf16(y.view(np.uint16), y_ref, yabs, REL)
+    n_bad = int(bad.sum())
+    if n_bad:
+        i = np.argwhere(bad)[0]
+        yv = y[tuple(i)]
+        raise AssertionError(f"{n_bad}/{bad.size} outside tolerance; first {tuple(i)}: "
+                             f"got {yv} ref {y_ref[tuple(i)]} abs {yabs[tuple(i)]}")
+
+
+def _case(M, N, K, a_gran, b_gran, fa=orc.E4M3, fb=orc.E4M3, mode=orc.SCALE_FP32,
+          a_t=False, b_t=False, seed=0):
+    a = inputs.activations(M, K, seed=seed)
+    b = inputs.gaussian((N, K), 0.02, seed=seed + 1)
+    qa, sa = _quant(a, a_gran, fa, mode)
+    qb, sb = _quant(b, b_gran, fb, mode)
+    # storage of transposed operands: the matrix [K][rows], scale tables in
+    # the stored orientation (a 128x128 table transposes with the matrix)
+    sqa, ssa = (qa.T.copy(), sa.T.copy() if a_gran == orc.GRAN_128x128 else sa) if a_t else (qa, sa)
+    sqb, ssb = (qb.T.copy(), sb.T.copy() if b_gran == orc.GRAN_128x128 else sb) if b_t else (qb, sb)
+    A_o = orc.operand(sqa, fa, a_gran, ssa, transposed=a_t)
+    B_o = orc.operand(sqb, fb, b_gran, ssb, transposed=b_t)
+    A_d = fp8.operand(dev(sqa), dev(ssa), fa, a_gran, a_t)
+    B_d = fp8.operand(dev(sqb), dev(ssb), fb, b_gran, b_t)
+    return A_o, B_o, A_d, B_d
+
+
+@pytest.mark.parametrize("out", [fp8.OUT_F32, fp8.OUT_BF16])
+def test_tiny_config(out):
+    """256x256x512, X 1x128 / W 128x128 E4M3, fp32 scales, full output."""
+    M, N, K = 256, 256, 512
+    A_o, B_o, A_d, B_d = _case(M, N, K, orc.GRAN_1x128, orc.GRAN_128x128)
+    y_ref, yabs = orc.gemm(M, N, K, A_o, B_o)
+    y = fp8.fp8_block_gemm(A_d, B_d, M, N, K, out)
+    _check(y, y_ref, yabs, out)
+
+
+@pytest.mark.parametrize("M,N,K", [(1, 128, 128), (127, 256, 256), (129, 384, 640),
+                                   (300, 520, 512), (513, 1024, 384), (64, 8, 128)])
+@pytest.mark.parametrize("mode", [orc.SCALE_FP32, orc.SCALE_POW2])
+def test_ragged_shapes(M, N, K, mode):
+    A_o, B_o, A_d, B_d = _case(M, N, K, orc.GRAN_1x128, orc.GRAN_128x128, mode=mode, seed=M)
+    y_ref, yabs = orc.gemm(M, N, K, A_o, B_o)
+    for out in (fp8.OUT_F32, fp8.OUT_BF16):
+        _check(fp8.fp8_block_gemm(A_d, B_d, M, N, K, out, mode), y_ref, yabs, out)
+
+
+@pytest.mark.parametrize("a_gran,b_gran", [(orc.GRAN_128x128, orc.GRAN_128x128),
+                                           (orc.GRAN_TENSOR, orc.GRAN_128x128),
+                                           (orc.GRAN_1x128, orc.GRAN_TENSOR),
+                                           (orc.GRAN_TENSOR, orc.GRAN_TENSOR)])
+def test_granularities(a_gran, b_gran):
+    M, N, K = 200, 512, 1024
+    A_o, B_o, A_d, B_d = _case(M, N, K, a_gran, b_gran, seed=7)
+    y_ref, yabs = orc.gemm(M, N, K, A_o, B_o)
+    _check(fp8.fp8_block_gemm(A_d, B_d, M, N, K, fp8.OUT_F32), y_ref, yabs, fp8.OUT_F32)
+
+
+@pytest.mark.parametrize("fa,fb", [(orc.E5M2, orc.E4M3), (orc.E4M3, orc.E5M2), (orc.E5M2, orc.E5M2)])
+def test_mixed_formats(fa, fb):
+    M, N, K = 256, 256, 768
+    A_o, B_o, A_d, B_d = _case(M, N, K, orc.GRAN_1x128, orc.GRAN_128x128, fa=fa, fb=fb, seed=11)
+    y_ref, yabs = orc.gemm(M, N, K, A_o, B_o)
+    _check(fp8.fp8_block_gemm(A_d, B_d, M, N, K, fp8.OUT_F32), y_ref, yabs, fp8.OUT_F32)
+
+
+@pytest.mark.parametrize("a_t,b_t,a_gran,b_gran", [
+    (False, True, orc.GRAN_1x128, orc.GRAN_128x128),     # dgrad, blockwise
+    (False, True, orc.GRAN_TENSOR, orc.GRAN_TENSOR),     # dgrad, per-tensor
+    (True, True, orc.GRAN_TENSOR, orc.GRAN_TENSOR),      # wgrad, per-tensor
+    (True, True, orc.GRAN_128x128, orc.GRAN_128x128),    # wgrad, 128x128
+    (True, False, orc.GRAN_TENSOR, orc.GRAN_128x128),
+])
+def test_transposed_operands(a_t, b_t, a_gran, b_gran):
+    M, N, K = 384, 512, 640
+    A_o, B_o, A_d, B_d = _case(M, N, K, a_gran, b_gran, fa=orc.E5M2, a_t=a_t, b_t=b_t, seed=13)
+    y_ref, yabs = orc.gemm(M, N, K, A_o, B_o)
+    _check(fp8.fp8_block_gemm(A_d, B_d, M, N, K, fp8.OUT_F32), y_ref, yabs, fp8.OUT_F32)
+
+
+def test_k_zero_writes_zeros():
+    import torch
+    A = fp8.operand(torch.zeros((4, 16), dtype=torch.uint8, device="cuda"),
+                    torch.ones((1, 4), device="cuda"), gran=fp8.GRAN_1x128)
+    B = fp8.operand(torch.zeros((8, 16), dtype=torch.uint8, device="cuda"),
+                    torch.ones((1, 1), device="cuda"), gran=fp8.GRAN_128x128)
+    y = torch.full((4, 8), 7.0, device="cuda")
+    fp8.fp8_block_gemm(A, B, 4, 8, 0, fp8.OUT_F32, y=y)
+    assert torch.count_nonzero(y).item() == 0
+
+
+def test_grouped_small():
+    G, N, K = 6, 384, 512
+    loads = np.array([0, 300, 1, 0, 129, 40])
+    off = np.zeros(G + 1, np.int32)
+    off[1:] = np.cumsum(loads)
+    T = int(off[-1])
+    a_rows = T + 5
+    x = inputs.activations(a_rows, K, seed=31)
+    w = inputs.gaussian((G * N, K), 0.02, seed=32)
+    qa, sa = orc.quantize_1x128(x)
+    qw = np.empty((G * N, K), np.uint8)
+    sw = np.empty((G, (N + 127) // 128, K // 128), np.float32)
+    for g in range(G):
+        qw[g * N:(g + 1) * N], sw[g] = orc.quantize_128x128(w[g * N:(g + 1) * N])
+    A_o = orc.operand(qa, orc.E4M3, orc.GRAN_1x128, sa)
+    B_o = orc.operand(qw, orc.E4M3, orc.GRAN_128x128, sw)
+    y_ref, yabs = orc.grouped_gemm(off, a_rows, N, K, A_o, B_o, rows=np.arange(T))
+    import torch
+    y = torch.full((a_rows, N), float("nan"), device="cuda")
+    fp8.fp8_grouped_block_gemm(dev(off), fp8.operand(dev(qa), dev(sa)),
+                               fp8.operand(dev(qw), dev(sw), gran=fp8.GRAN_128x128),
+                               a_rows, N, K, fp8.OUT_F32, y=y)
+    yh = host(y)
+    bad = orc.check_f32(yh[:T], y_ref, yabs, REL)
+    assert not bad.any(), int(bad.sum())
+    assert np.all(np.isnan(yh[T:]))            # rows outside every group untouched
+
+
+def test_back_to_back_calls_and_side_stream():
+    import torch
+    M, N, K = 300, 512, 512
+    A_o, B_o, A_d, B_d = _case(M, N, K, orc.GRAN_1x128, orc.GRAN_128x128, seed=41)
+    y_ref, yabs = orc.gemm(M, N, K, A_o, B_o)
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        ys = [fp8.fp8_block_gemm(A_d, B_d, M, N, K, fp8.OUT_F32) for _ in range(3)]
+    s.synchronize()
+    for y in ys:
+        _check(y, y_ref, yabs, fp8.OUT_F32)
+    fp8.device_status()
+
+
+# ------------------------------------------------------------ full sizes
+LLAMA8B = [("qkv", 6144, 4096), ("o", 4096, 4096), ("gate_up", 28672, 4096), ("down", 4096, 14336)]
+
+
+@pytest.mark.parametrize("name,N,K", LLAMA8B)
+def test_llama31_8b_linears_sampled(name, N, K):
+    """Full Llama-3.1-8B-shaped fprop linears (M=8192, fp32 scales, bf16 out as
+    the benchmark runs them), checked on one sampled row per 128-row block and
+    one sampled column per 256-column block."""
+    M = 8192
+    x = inputs.activations(M, K, seed=1000 + K)
+    w = inputs.gaussian((N, K), 0.02, seed=2000 + N)
+    qa, sa = orc.quantize_1x128(x)
+    qb, sb = orc.quantize_128x128(w)
+    A_o = orc.operand(qa, orc.E4M3, orc.GRAN_1x128, sa)
+    B_o = orc.operand(qb, orc.E4M3, orc.GRAN_128x128, sb)
+    rng = np.random.default_rng(N + K)
+    rows = stratified(M, 128, rng)
+    cols = stratified(N, 256, rng, extra=(N - 8,))
+    y_ref, yabs = orc.gemm(M, N, K, A_o, B_o, rows=rows, cols=cols)
+    A_d = fp8.operand(dev(qa), dev(sa))
+    B_d = fp8.operand(dev(qb), dev(sb), gran=fp8.GRAN_128x128)
+    for out in (fp8.OUT_BF16, fp8.OUT_F32):
+        y = fp8.fp8_block_gemm(A_d, B_d, M, N, K, out)
+        _check(y, y_ref, yabs, out, rows, cols)

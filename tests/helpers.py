@@ -13,7 +13,11 @@ def dev(a: np.ndarray):
 
 
 def host(t) -> np.ndarray:
-    return t.detach().cpu().numpy()
+    import torch
+    t = t.detach()
+    if t.dtype == torch.bfloat16:          # numpy has no bf16: return the bit patterns
+        return t.view(torch.int16).cpu().numpy().view(np.uint16)
+    return t.cpu().numpy()
 
 
 def f32_bits(a) -> np.ndarray:

@@ -105,13 +105,15 @@ class Clocks:
 
 
 # ------------------------------------------------------------ workload
-def make_inputs(device, seed=0):
+def make_inputs(device, seed=0, only=None):
     """Synthetic bf16 inputs on the device, per linear: X [M, K], W [N, K]."""
     import torch
     g = torch.Generator(device=device)
     M = WORKLOAD["M"]
     bufs = []
     for i, (name, N, K) in enumerate(WORKLOAD["linears"]):
+        if only and name != only:
+            continue
         g.manual_seed(seed * 1000 + i)
         x = torch.randn((M, K), generator=g, device=device, dtype=torch.float32)
         n_out = int(round(0.01 * K))
@@ -255,7 +257,7 @@ def run_ours(args):
     fp8.lib()
     peaks = _peaks()
 
-    bufs = make_inputs(device, seed=rank)
+    bufs = make_inputs(device, seed=rank, only=args.only)
     step = Step(bufs, fp8, device)
     nlin = len(step.items)
 
@@ -366,7 +368,9 @@ def run_ours(args):
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": ws, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "e4m3 (fp32 accumulate, bf16 out)", "data": "synthetic",
-        "config": {"workload": WORKLOAD["name"], "M": M, "linears": WORKLOAD["linears"],
+        "config": {"workload": WORKLOAD["name"] + (f" ({args.only} only)" if args.only else ""),
+                   "M": M, "linears": [list(l) for l in WORKLOAD["linears"]
+                                       if not args.only or l[0] == args.only],
                    "scales": "fp32 1x128 (X) / 128x128 (W)", "out": "bf16",
                    "l2": "inputs larger than L2 (each step streams ~1.2 GB)",
                    "parallelism": f"replicas x{ws}"},
@@ -400,6 +404,8 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--only", choices=[l[0] for l in WORKLOAD["linears"]], default=None,
+                    help="run a single linear of the workload (profiling)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

@@ -9,7 +9,7 @@
 #include <cstring>
 #include <mutex>
 
-#include "../../include/fp8bs.h"
+#include "fp8bs.h"
 #include "gemm_kernels.h"
 #include "quant_kernels.h"
 
@@ -178,7 +178,7 @@ int run_gemm(const char* fn, int32_t G, const int32_t* offsets, int64_t a_rows, 
     p.tiles_n = static_cast<int32_t>((N + BN - 1) / BN);
     p.promote = (A->gran == FP8BS_GRAN_TENSOR && B->gran == FP8BS_GRAN_TENSOR) ? 0 : 1;
     p.out_bf16 = out_dtype == FP8BS_OUT_BF16;
-    p.idesc = fp8bs::make_idesc_f8f6f4(A->fmt, B->fmt, a_mn, b_mn, b_mn ? 128 : BN);
+    p.idesc = fp8bs::make_idesc_f8f6f4(A->fmt, B->fmt, a_mn, b_mn, b_mn ? 128 : fp8bs::gemm_mma_n());
 
     // upper bound on tiles (the grouped count is only known on the device)
     const int64_t slots = grouped ? (a_rows + BM - 1) / BM + G : (M + BM - 1) / BM;

@@ -10,19 +10,22 @@
 //   warp 0      TMA producer: per 128-deep K block, one 128x128 A tile and
 //               one 256x128 B tile (8-bit, 128-byte swizzle) into a 4-stage
 //               shared-memory ring.
-//   warp 1      TMEM owner and MMA issuer: 4 x tcgen05.mma.kind::f8f6f4
-//               (M=128, N=256, K=32) per K block into a TMEM partial buffer.
+//   warp 1      TMEM owner and MMA issuer: per K block, two N=128 halves of
+//               4 x tcgen05.mma.kind::f8f6f4 (M=128, N=128, K=32), each half
+//               into its own 128-column TMEM partial buffer.
 //   warps 2,3   idle (they complete the first warpgroup).
 //   warps 4..11 epilogue ("promotion"): each thread owns one output row (its
 //               TMEM lane) and 128 columns; per K block it loads the fp32
 //               partial from TMEM and folds it into fp32 registers with that
-//               block's two scales: acc = fma(partial, sA * sB, acc).
+//               block's two scales: acc = fma(partial, sA * sB, acc), two
+//               columns per packed f32x2 FMA.
 // Register split (setmaxnreg): the block launches with 168 registers per
 // thread (384 x 168 = 64512); the first warpgroup releases down to 72 and the
 // two epilogue warpgroups grow to 216: 128 x 72 + 256 x 216 = 64512.
-// (An MN-major B runs as two N=128 MMAs per K step.)
-// Two TMEM partial buffers (2 x 256 columns) let the MMAs of block kb+1 run
-// while block kb is promoted.  When both operands have one scale per tensor
+// TMEM holds a 4-deep ring of 128-column partial buffers (half 0 and half 1
+// of two K blocks); each epilogue warpgroup follows its own half, so three
+// MMA groups (~768 tensor cycles) cover the commit -> promote -> release
+// round trip before a buffer is needed again.  When both operands have one scale per tensor
 // the whole K accumulates in TMEM and is scaled once ("promote every K").
 // Operands may be stored K-major or MN-major (transposed storage, used by
 // dgrad/wgrad); the instruction descriptor's major bits and the shared-memory
@@ -55,13 +58,35 @@ constexpr int EPI_WARP0 = 4;
 constexpr int REGS_LOW = 72, REGS_HIGH = 216;   // 128*72 + 256*216 == 384*168
 constexpr int NUM_EPI_WARPS = 8;
 constexpr uint32_t TMEM_COLS = 512;
-constexpr int RASTER_M = 16;            // m-slots per rasterization group
+#ifndef FP8BS_RASTER_M
+#define FP8BS_RASTER_M 16
+#endif
+constexpr int RASTER_M = FP8BS_RASTER_M;   // m-slots per rasterization group
+#ifndef FP8BS_EPI_LOADS
+#define FP8BS_EPI_LOADS 1
+#endif
+constexpr int EPI_LOADS = FP8BS_EPI_LOADS;   // TMEM loads (x32 columns) per wait
+#ifndef FP8BS_SPF
+#define FP8BS_SPF 8
+#endif
+constexpr int SPF = FP8BS_SPF;               // scale prefetch distance (chunks)
+#ifndef FP8BS_FFMA2
+#define FP8BS_FFMA2 1                        // packed f32x2 promotion FMAs
+#endif
 constexpr uint64_t WAIT_LIMIT_NS = 4000000000ull;
 constexpr uint64_t DRAIN_LIMIT_NS = 200000000ull;
 
 // Shared memory: [align pad][A ring][B ring][barriers][tmem addr][group tables]
 constexpr uint32_t BAR_OFF = STAGES * STAGE_BYTES;
-constexpr int NUM_BARS = 2 * STAGES + 4 + 1;   // full, empty, tfull[2], tempty[2], done
+#ifndef FP8BS_HALVES
+#define FP8BS_HALVES 1
+#endif
+// Each K block's MMAs run as HALVES slices of N = 256 / HALVES columns, each
+// into its own TMEM buffer of a ring of 512 / MMA_N buffers.
+constexpr int HALVES = FP8BS_HALVES;
+constexpr int MMA_N = BN / HALVES;
+constexpr int TBUFS = 512 / MMA_N;
+constexpr int NUM_BARS = 2 * STAGES + 2 * TBUFS + 1;   // full, empty, tfull, tempty, done
 constexpr uint32_t TMEMSLOT_OFF = BAR_OFF + NUM_BARS * 8;
 constexpr uint32_t TABLE_OFF = (TMEMSLOT_OFF + 16 + 15) & ~15u;
 constexpr uint32_t SMEM_BYTES = 1024 + TABLE_OFF + 2 * (kMaxGroups + 1) * 4;
@@ -127,8 +152,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     auto full_bar = [&](int s) { return bars + 8u * s; };
     auto empty_bar = [&](int s) { return bars + 8u * (STAGES + s); };
     auto tfull_bar = [&](int b) { return bars + 8u * (2 * STAGES + b); };
-    auto tempty_bar = [&](int b) { return bars + 8u * (2 * STAGES + 2 + b); };
-    const uint32_t done_bar = bars + 8u * (2 * STAGES + 4);
+    auto tempty_bar = [&](int b) { return bars + 8u * (2 * STAGES + TBUFS + b); };
+    const uint32_t done_bar = bars + 8u * (2 * STAGES + 2 * TBUFS);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + TMEMSLOT_OFF);
     int* s_off = reinterpret_cast<int*>(smem + TABLE_OFF);
     int* s_slot = s_off + (kMaxGroups + 1);
@@ -144,9 +169,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             mbar_init(full_bar(s), 1);
             mbar_init(empty_bar(s), 1);
         }
-        for (int b = 0; b < 2; b++) {
+        for (int b = 0; b < TBUFS; b++) {
             mbar_init(tfull_bar(b), 1);
-            mbar_init(tempty_bar(b), NUM_EPI_WARPS);
+            mbar_init(tempty_bar(b), NUM_EPI_WARPS / HALVES);   // the warps reading it
         }
         mbar_init(done_bar, 1);
         fence_mbar_init();
@@ -231,45 +256,52 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         // ---------------------------------------------------------- MMA
         if (lane == 0) {
             int stage = 0;
-            uint32_t phase = 0, chunk = 0;
+            uint32_t phase = 0, group = 0;   // group = promotion group (P K blocks)
             bool ok = true, issued_mma = false;
             for (int t = blockIdx.x; ok && t < total_tiles; t += gridDim.x) {
                 for (int kb = 0; kb < nkb; kb++) {
-                    const uint32_t buf = chunk & 1u;
-                    if (kb % P == 0) {
-                        if (!wait_or_flag(tempty_bar(buf), ((chunk >> 1) & 1u) ^ 1u)) { ok = false; break; }
-                    }
                     if (!wait_or_flag(full_bar(stage), phase)) { ok = false; break; }
-                    tc_fence_after();
-                    const uint32_t d = tmem_base + buf * BN;
                     const uint32_t aS = sA + stage * A_STAGE, bS = sB + stage * B_STAGE;
+                    // two N=128 halves per K block, each into its own 128-column
+                    // TMEM buffer of a 4-deep ring (chunk c = 2 * group + half)
 #pragma unroll
-                    for (int k4 = 0; k4 < BK / 32; k4++) {
-                        // K-major: 32 K-bytes further inside the 128-byte swizzled row,
-                        // 8-row groups 1024 B apart (SBO).  MN-major: 32 K-rows further
-                        // (4 swizzle atoms of 8 K-rows x 128 B, 1024 B apart); every
-                        // MN-major descriptor spans a single 128-wide atom, so its
-                        // MN-atom stride is never used and both offsets are 1024.
-                        const uint64_t ad = A_MN ? smem_desc_sw128(aS + k4 * 4096, 1024, 1024)
-                                                 : smem_desc_sw128(aS + k4 * 32, 16, 1024);
-                        const uint32_t acc = (k4 > 0 || kb % P != 0) ? 1u : 0u;
-                        if (B_MN) {
-                            // two N=128 halves, one TMA box each
-                            mma_f8f6f4(d, ad, smem_desc_sw128(bS + k4 * 4096, 1024, 1024),
-                                       p.idesc, acc);
-                            mma_f8f6f4(d + 128, ad,
-                                       smem_desc_sw128(bS + B_STAGE / 2 + k4 * 4096, 1024, 1024),
-                                       p.idesc, acc);
-                        } else {
-                            mma_f8f6f4(d, ad, smem_desc_sw128(bS + k4 * 32, 16, 1024), p.idesc, acc);
+                    for (int h = 0; h < HALVES; h++) {
+                        const uint32_t c = HALVES * group + h, buf = c % TBUFS;
+                        if (kb % P == 0) {
+                            if (!wait_or_flag(tempty_bar(buf), ((c / TBUFS) & 1u) ^ 1u)) { ok = false; break; }
                         }
-                        issued_mma = true;
+                        tc_fence_after();
+                        const uint32_t d = tmem_base + buf * MMA_N;
+#pragma unroll
+                        for (int k4 = 0; k4 < BK / 32; k4++) {
+                            // K-major: 32 K-bytes further inside the 128-byte swizzled
+                            // row, 8-row groups 1024 B apart (SBO); half h starts 128
+                            // rows (16 KiB) in.  MN-major: 32 K-rows further (4 swizzle
+                            // atoms of 8 K-rows x 128 B, 1024 B apart), half h is the
+                            // second TMA box; every MN-major descriptor spans a single
+                            // 128-wide atom, so its MN-atom stride is never used and
+                            // both offsets are 1024.
+                            const uint64_t ad = A_MN ? smem_desc_sw128(aS + k4 * 4096, 1024, 1024)
+                                                     : smem_desc_sw128(aS + k4 * 32, 16, 1024);
+                            const uint32_t acc = (k4 > 0 || kb % P != 0) ? 1u : 0u;
+                            if (B_MN) {   // one 128-wide TMA box per MMA (see above)
+#pragma unroll
+                                for (int q = 0; q < MMA_N / 128; q++)
+                                    mma_f8f6f4(d + q * 128, ad,
+                                               smem_desc_sw128(bS + (h * MMA_N / 128 + q) * (B_STAGE / 2) +
+                                                                   k4 * 4096, 1024, 1024),
+                                               p.idesc, acc);
+                            } else {
+                                mma_f8f6f4(d, ad, smem_desc_sw128(bS + h * (B_STAGE / 2) + k4 * 32, 16, 1024),
+                                           p.idesc, acc);
+                            }
+                            issued_mma = true;
+                        }
+                        if (kb % P == P - 1) mma_commit(tfull_bar(buf));
                     }
+                    if (!ok) break;
                     mma_commit(empty_bar(stage));
-                    if (kb % P == P - 1) {
-                        mma_commit(tfull_bar(buf));
-                        chunk++;
-                    }
+                    if (kb % P == P - 1) group++;
                     if (++stage == STAGES) { stage = 0; phase ^= 1u; }
                 }
             }
@@ -312,35 +344,67 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 else { pb = p.sb + tl.g * p.b_scale_group_stride + nb * nkb64; sb_step = 1; }
             } else { pb = p.sb; sb_step = 0; }
 
-            float acc[128];
+            uint64_t acc[64];   // 128 fp32 accumulators as packed pairs
 #pragma unroll
-            for (int i = 0; i < 128; i++) acc[i] = 0.0f;
-            float sa_next = ld_scale(pa), sb_next = ld_scale(pb);
-            for (int kb = 0; kb < nkb; kb += P) {
-                const float s = sa_next * sb_next;
-                if (kb + P < nkb) {
-                    sa_next = ld_scale(pa + (kb + P) * sa_step);
-                    sb_next = ld_scale(pb + (kb + P) * sb_step);
+            for (int i = 0; i < 64; i++) acc[i] = 0;
+            // Scales: a ring of SPF register slots, slot i holding chunk
+            // (kb0 + i); the K-block loop is unrolled by SPF so each slot is
+            // refilled (SPF chunks ahead) right after use, with no register
+            // copies that would wait on the load early.
+            float sa_r[SPF], sb_r[SPF];
+#pragma unroll
+            for (int i = 0; i < SPF; i++) {
+                const int kbi = min(i * P, nkb - 1);
+                sa_r[i] = ld_scale(pa + kbi * sa_step);
+                sb_r[i] = ld_scale(pb + kbi * sb_step);
+            }
+            for (int kb0 = 0; ok && kb0 < nkb; kb0 += SPF * P) {
+#pragma unroll
+                for (int i = 0; i < SPF; i++) {
+                    const int kb = kb0 + i * P;
+                    if (kb >= nkb) break;
+                    const float s = sa_r[i] * sb_r[i];
+                    const uint64_t s2 = pack_f32x2(__float_as_uint(s), __float_as_uint(s));
+                    if (kb + SPF * P < nkb) {
+                        sa_r[i] = ld_scale(pa + (kb + SPF * P) * sa_step);
+                        sb_r[i] = ld_scale(pb + (kb + SPF * P) * sb_step);
+                    }
+                    const uint32_t c = HALVES * chunk + (HALVES == 2 ? half : 0), buf = c % TBUFS;
+                    ok = __all_sync(0xFFFFFFFFu, wait_or_flag(tfull_bar(buf), (c / TBUFS) & 1u));
+                    if (!ok) break;
+                    tc_fence_after();
+                    const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
+                                           buf * MMA_N + (HALVES == 1 ? half * 128 : 0);
+                    // EPI_LOADS x 32 columns in flight per wait (one TMEM round
+                    // trip); the buffer is handed back right after the last load
+#pragma unroll
+                    for (int j = 0; j < 4; j += EPI_LOADS) {
+                        uint32_t r[EPI_LOADS][32];
+#pragma unroll
+                        for (int u = 0; u < EPI_LOADS; u++) tmem_ld_32x32b_x32(taddr + (j + u) * 32, r[u]);
+                        tmem_wait_ld();
+                        if (j + EPI_LOADS >= 4) {
+                            tc_fence_before();
+                            __syncwarp();
+                            if (lane == 0) mbar_arrive(tempty_bar(buf));
+                        }
+#pragma unroll
+                        for (int u = 0; u < EPI_LOADS; u++) {
+#pragma unroll
+                            for (int q = 0; q < 16; q++) {
+#if FP8BS_FFMA2
+                                fma_f32x2(acc[(j + u) * 16 + q], pack_f32x2(r[u][2 * q], r[u][2 * q + 1]), s2);
+#else
+                                float2 a = unpack_f32x2(acc[(j + u) * 16 + q]);
+                                a.x = __fmaf_rn(__uint_as_float(r[u][2 * q]), s, a.x);
+                                a.y = __fmaf_rn(__uint_as_float(r[u][2 * q + 1]), s, a.y);
+                                acc[(j + u) * 16 + q] = pack_f32x2(__float_as_uint(a.x), __float_as_uint(a.y));
+#endif
+                            }
+                        }
+                    }
+                    chunk++;
                 }
-                const uint32_t buf = chunk & 1u;
-                ok = __all_sync(0xFFFFFFFFu, wait_or_flag(tfull_bar(buf), (chunk >> 1) & 1u));
-                if (!ok) break;
-                tc_fence_after();
-                const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
-                                       buf * BN + half * 128;
-#pragma unroll
-                for (int j = 0; j < 4; j++) {
-                    uint32_t r[32];
-                    tmem_ld_32x32b_x32(taddr + j * 32, r);
-                    tmem_wait_ld();
-#pragma unroll
-                    for (int i = 0; i < 32; i++)
-                        acc[j * 32 + i] = __fmaf_rn(__uint_as_float(r[i]), s, acc[j * 32 + i]);
-                }
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(tempty_bar(buf));
-                chunk++;
             }
             if (!ok) break;
             if (row_ok) {
@@ -352,7 +416,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                             uint32_t w[4];
 #pragma unroll
                             for (int i = 0; i < 4; i++) {
-                                __nv_bfloat162 h = __floats2bfloat162_rn(acc[j + 2 * i], acc[j + 2 * i + 1]);
+                                const float2 f = unpack_f32x2(acc[j / 2 + i]);
+                                __nv_bfloat162 h = __floats2bfloat162_rn(f.x, f.y);
                                 w[i] = *reinterpret_cast<uint32_t*>(&h);
                             }
                             *reinterpret_cast<uint4*>(y + j) = make_uint4(w[0], w[1], w[2], w[3]);
@@ -362,9 +427,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     float* y = reinterpret_cast<float*>(p.y) + row * p.ldy + col0;
 #pragma unroll
                     for (int j = 0; j < 128; j += 4) {
-                        if (col0 + j < p.N)
-                            *reinterpret_cast<float4*>(y + j) =
-                                make_float4(acc[j], acc[j + 1], acc[j + 2], acc[j + 3]);
+                        if (col0 + j < p.N) {
+                            const float2 a = unpack_f32x2(acc[j / 2]), b = unpack_f32x2(acc[j / 2 + 1]);
+                            *reinterpret_cast<float4*>(y + j) = make_float4(a.x, a.y, b.x, b.y);
+                        }
                     }
                 }
             }
@@ -399,6 +465,7 @@ uint32_t make_idesc_f8f6f4(int a_fmt, int b_fmt, bool a_mn, bool b_mn, int n) {
 }
 
 int gemm_tile_n() { return BN; }
+int gemm_mma_n() { return MMA_N; }
 int gemm_tile_m() { return BM; }
 
 cudaError_t launch_fp8_gemm(const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmParams& p,

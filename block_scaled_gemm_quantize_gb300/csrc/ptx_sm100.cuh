@@ -125,6 +125,22 @@ __device__ __forceinline__ void tmem_wait_ld() {
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
 
+// Packed fp32 pairs (sm_100 family f32x2 arithmetic): one instruction does
+// two independent, individually rounded fp32 FMAs.
+__device__ __forceinline__ uint64_t pack_f32x2(uint32_t lo, uint32_t hi) {
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "r"(lo), "r"(hi));
+    return r;
+}
+__device__ __forceinline__ void fma_f32x2(uint64_t& acc, uint64_t a, uint64_t b) {
+    asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(acc) : "l"(a), "l"(b));
+}
+__device__ __forceinline__ float2 unpack_f32x2(uint64_t v) {
+    float2 f;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(f.x), "=f"(f.y) : "l"(v));
+    return f;
+}
+
 // Shared-memory matrix descriptor (tcgen05 form): start address, leading and
 // stride byte offsets (16-byte units), descriptor version 1 at bits 46-47,
 // swizzle mode at bits 61-63 (2 = 128-byte swizzle).

@@ -86,6 +86,22 @@ int make_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer, u
     return FP8BS_OK;
 }
 
+// Output tensor [rows][N] of bf16 or fp32 with row pitch `pitch` bytes; box
+// 32 rows x 64 bytes, 64-byte swizzle (matches the epilogue's staging slabs).
+int make_out_map(CUtensorMap* m, void* base, bool bf16, uint64_t N, uint64_t rows, uint64_t pitch) {
+    cuuint64_t dims[2] = {N, rows};
+    cuuint64_t strides[1] = {pitch};
+    cuuint32_t box[2] = {bf16 ? 32u : 16u, 32u};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = g_encode(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2,
+                          base, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                          CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS)
+        return fail(FP8BS_ERR_CUDA, "cuTensorMapEncodeTiled (output) failed (CUresult %d)", (int)r);
+    return FP8BS_OK;
+}
+
 int sm_count() {
     int dev = 0, n = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return 0;
@@ -157,8 +173,13 @@ int run_gemm(const char* fn, int32_t G, const int32_t* offsets, int64_t a_rows, 
     else rc = make_map(&tmB, B->data, K, b_rows_total, B->ld, BN);
     if (rc) return rc;
 
+    CUtensorMap tmY;
+    if ((rc = make_out_map(&tmY, Y, out_dtype == FP8BS_OUT_BF16, N, a_rows, ld_y * esz)) != FP8BS_OK)
+        return rc;
+
     fp8bs::GemmParams p;
     memset(&p, 0, sizeof(p));
+    p.tma_store = 1;
     p.M = M;
     p.N = N;
     p.K = K;
@@ -188,7 +209,7 @@ int run_gemm(const char* fn, int32_t G, const int32_t* offsets, int64_t a_rows, 
     if (sms <= 0) return fail(FP8BS_ERR_CUDA, "%s: cannot query the device", fn);
     const int grid = static_cast<int>(tiles < sms ? tiles : sms);
     if (grid <= 0) return FP8BS_OK;
-    cudaError_t e = fp8bs::launch_fp8_gemm(tmA, tmB, p, a_mn, b_mn, grid, stream);
+    cudaError_t e = fp8bs::launch_fp8_gemm(tmA, tmB, tmY, p, a_mn, b_mn, grid, stream);
     return e == cudaSuccess ? FP8BS_OK : cuda_fail(e, fn);
 }
 

@@ -89,7 +89,11 @@ constexpr int TBUFS = 512 / MMA_N;
 constexpr int NUM_BARS = 2 * STAGES + 2 * TBUFS + 1;   // full, empty, tfull, tempty, done
 constexpr uint32_t TMEMSLOT_OFF = BAR_OFF + NUM_BARS * 8;
 constexpr uint32_t TABLE_OFF = (TMEMSLOT_OFF + 16 + 15) & ~15u;
-constexpr uint32_t SMEM_BYTES = 1024 + TABLE_OFF + 2 * (kMaxGroups + 1) * 4;
+// output staging: one 2 KiB slab per epilogue warp (32 rows x 64 B, 64-B swizzle)
+constexpr uint32_t OUT_SLAB = 2048;
+constexpr uint32_t OUT_OFF = (TABLE_OFF + 2 * (kMaxGroups + 1) * 4 + 1023) & ~1023u;
+constexpr uint32_t SMEM_BYTES = 1024 + OUT_OFF + NUM_EPI_WARPS * OUT_SLAB;
+static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 
 __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
     if (mbar_try_wait(bar, parity)) return true;
@@ -141,7 +145,7 @@ __device__ __forceinline__ float ld_scale(const float* p) { return __ldg(p); }
 template <bool A_MN, bool B_MN>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     k_fp8_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-               const GemmParams p) {
+               const __grid_constant__ CUtensorMap tmY, const GemmParams p) {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     uint8_t* smem = smem_raw + ((1024u - (raw & 1023u)) & 1023u);
@@ -407,7 +411,47 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 }
             }
             if (!ok) break;
-            if (row_ok) {
+            // ---- store: TMA bulk stores of 32 x 64-byte slabs when this warp's
+            // 32 rows all belong to the tile's group (TMA clips only at the
+            // tensor edge), otherwise masked direct stores
+            const int64_t wrow0 = static_cast<int64_t>(tl.row0) + quarter * 32;
+            if (p.tma_store && (p.offsets == nullptr || wrow0 + 32 <= tl.row_end)) {
+                const uint32_t slab = sbase + OUT_OFF + (warp - EPI_WARP0) * OUT_SLAB;
+                const uint32_t rbase = slab + lane * 64;
+                const uint32_t sw = (lane >> 1) & 3;          // 64-B swizzle: chunk ^= (row/2)%4
+                const int passes = p.out_bf16 ? 4 : 8;        // 32 bf16 or 16 fp32 columns each
+#pragma unroll
+                for (int ps = 0; ps < 8; ps++) {
+                    if (ps >= passes) break;
+                    if (lane == 0) bulk_wait_group_read0();   // slab free again
+                    __syncwarp();
+#pragma unroll
+                    for (int c = 0; c < 4; c++) {
+                        uint32_t w[4];
+                        if (p.out_bf16) {
+#pragma unroll
+                            for (int i = 0; i < 4; i++) {
+                                const float2 f = unpack_f32x2(acc[ps * 16 + c * 4 + i]);
+                                __nv_bfloat162 h = __floats2bfloat162_rn(f.x, f.y);
+                                w[i] = *reinterpret_cast<uint32_t*>(&h);
+                            }
+                        } else {
+                            const float2 a = unpack_f32x2(acc[ps * 8 + c * 2]);
+                            const float2 b = unpack_f32x2(acc[ps * 8 + c * 2 + 1]);
+                            w[0] = __float_as_uint(a.x); w[1] = __float_as_uint(a.y);
+                            w[2] = __float_as_uint(b.x); w[3] = __float_as_uint(b.y);
+                        }
+                        st_shared_v4(rbase + ((c ^ sw) << 4), w[0], w[1], w[2], w[3]);
+                    }
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+                        tma_store_2d(&tmY, slab, static_cast<int32_t>(col0 + ps * (p.out_bf16 ? 32 : 16)),
+                                     static_cast<int32_t>(wrow0));
+                        bulk_commit_group();
+                    }
+                }
+            } else if (row_ok) {
                 if (p.out_bf16) {
                     uint16_t* y = reinterpret_cast<uint16_t*>(p.y) + row * p.ldy + col0;
 #pragma unroll
@@ -435,6 +479,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 }
             }
         }
+        if (lane == 0) bulk_wait_group0();   // every store of this warp has landed
     }
 
     tc_fence_before();
@@ -468,13 +513,13 @@ int gemm_tile_n() { return BN; }
 int gemm_mma_n() { return MMA_N; }
 int gemm_tile_m() { return BM; }
 
-cudaError_t launch_fp8_gemm(const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmParams& p,
-                            bool a_mn, bool b_mn, int grid, cudaStream_t st) {
+cudaError_t launch_fp8_gemm(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmY,
+                            const GemmParams& p, bool a_mn, bool b_mn, int grid, cudaStream_t st) {
     auto k = a_mn ? (b_mn ? k_fp8_gemm<true, true> : k_fp8_gemm<true, false>)
                   : (b_mn ? k_fp8_gemm<false, true> : k_fp8_gemm<false, false>);
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
     if (e != cudaSuccess) return e;
-    k<<<grid, NUM_THREADS, SMEM_BYTES, st>>>(tmA, tmB, p);
+    k<<<grid, NUM_THREADS, SMEM_BYTES, st>>>(tmA, tmB, tmY, p);
     return cudaGetLastError();
 }
 

@@ -27,6 +27,7 @@ struct GemmParams {
     int32_t tiles_n;
     int32_t promote;          // 1: scale per 128-K block; 0: one scale per tensor pair
     int32_t out_bf16;
+    int32_t tma_store;        // 1: tmY describes Y (box 32 rows x 64 B, 64-B swizzle)
     uint32_t idesc;
 };
 
@@ -35,8 +36,8 @@ uint32_t make_idesc_f8f6f4(int a_fmt, int b_fmt, bool a_mn, bool b_mn, int n);
 int gemm_tile_n();
 int gemm_mma_n();   // N of one tcgen05.mma (a K-major B); an MN-major B always uses 128
 int gemm_tile_m();
-cudaError_t launch_fp8_gemm(const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmParams& p,
-                            bool a_mn, bool b_mn, int grid, cudaStream_t st);
+cudaError_t launch_fp8_gemm(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmY,
+                            const GemmParams& p, bool a_mn, bool b_mn, int grid, cudaStream_t st);
 cudaError_t read_and_clear_status(int* status);
 
 }  // namespace fp8bs

@@ -113,42 +113,41 @@ __device__ __forceinline__ void quant8(const float (&f)[8], float r, uint32_t& l
 // ---------------------------------------------------------------- 1x128
 // A half-warp owns one 1x128 tile: 16 lanes x 8 bf16 (one 16-byte load per
 // lane), a 4-step shuffle-xor amax inside the half-warp, one 8-byte store per
-// lane (128 contiguous code bytes per tile) and one scale store.  Tiles are
-// numbered column-block-major (tile = kb * rows + r) so the 16 half-warps of
-// a CTA write 16 consecutive scales; each thread keeps U loads in flight.
+// lane (128 contiguous code bytes per tile) and one scale store.  Grid: y =
+// K block, x = group of 16*U rows; the 16 half-warps of a CTA take 16
+// consecutive rows, so each of the U rounds writes 16 consecutive scales, and
+// each thread keeps U loads in flight.
 template <int FMT, int MODE, int U>
 __global__ void __launch_bounds__(256) k_quant_1x128(const uint16_t* __restrict__ x, int64_t rows,
-                                                    int64_t ldx, int64_t ntiles,
-                                                    uint8_t* __restrict__ q, int64_t ldq,
+                                                    int64_t ldx, uint8_t* __restrict__ q, int64_t ldq,
                                                     float* __restrict__ scales) {
     const int l16 = threadIdx.x & 15;
     const int hw = threadIdx.x >> 4;
-    const int64_t base = static_cast<int64_t>(blockIdx.x) * (16 * U) + hw;
+    const int64_t kb = blockIdx.y;
+    const int64_t r0 = static_cast<int64_t>(blockIdx.x) * (16 * U) + hw;
+    const uint16_t* xk = x + kb * 128 + l16 * 8;
     uint4 v[U];
-    int64_t r_[U], kb_[U];
 #pragma unroll
     for (int i = 0; i < U; i++) {
-        const int64_t t = base + 16 * i;
-        kb_[i] = t / rows;
-        r_[i] = t - kb_[i] * rows;
+        const int64_t r = r0 + 16 * i;
         v[i] = make_uint4(0, 0, 0, 0);
-        if (t < ntiles) v[i] = ld_stream_v4(x + r_[i] * ldx + kb_[i] * 128 + l16 * 8);
+        if (r < rows) v[i] = ld_stream_v4(xk + r * ldx);
     }
 #pragma unroll
     for (int i = 0; i < U; i++) {
-        const bool valid = base + 16 * i < ntiles;
+        const int64_t r = r0 + 16 * i;
         float f[8];
         unpack8(v[i], f);
         float m = amax8(f);
 #pragma unroll
         for (int o = 8; o >= 1; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
-        if (valid) {
+        if (r < rows) {
             const float s = block_scale<FMT, MODE>(m);
-            const float r = __frcp_rn(s);
+            const float rc = __frcp_rn(s);
             uint32_t lo, hi;
-            quant8<FMT>(f, r, lo, hi);
-            st_v2(q + r_[i] * ldq + kb_[i] * 128 + l16 * 8, lo, hi);
-            if (l16 == 0) scales[kb_[i] * rows + r_[i]] = s;
+            quant8<FMT>(f, rc, lo, hi);
+            st_v2(q + r * ldq + kb * 128 + l16 * 8, lo, hi);
+            if (l16 == 0) scales[kb * rows + r] = s;
         }
     }
 }
@@ -158,8 +157,11 @@ __global__ void __launch_bounds__(256) k_quant_1x128(const uint16_t* __restrict_
 // the 16-byte chunk (t % 16) of rows t/16 + 16 i, i < 8 (a half-warp covers
 // one 256-byte row segment).  CTA amax (shuffles + shared memory), one
 // scale, then convert and store -- a single pass over the tile.
+#ifndef FP8BS_Q128_MINB
+#define FP8BS_Q128_MINB 3
+#endif
 template <int FMT, int MODE>
-__global__ void __launch_bounds__(256) k_quant_128x128(const uint16_t* __restrict__ w, int64_t rows,
+__global__ void __launch_bounds__(256, FP8BS_Q128_MINB) k_quant_128x128(const uint16_t* __restrict__ w, int64_t rows,
                                                       int64_t ldw, int64_t nkb,
                                                       uint8_t* __restrict__ q, int64_t ldq,
                                                       float* __restrict__ scales) {
@@ -291,19 +293,25 @@ __global__ void __launch_bounds__(256) k_amax_history(float* __restrict__ histor
 
 // ------------------------------------------------------------ launchers
 namespace {
-constexpr int kU1 = 4;   // tiles in flight per half-warp (1x128)
-constexpr int kUT = 8;   // vectors in flight per thread (per-tensor)
+#ifndef FP8BS_U1
+#define FP8BS_U1 4
+#endif
+constexpr int kU1 = FP8BS_U1;   // tiles in flight per half-warp (1x128)
+#ifndef FP8BS_UT
+#define FP8BS_UT 8
+#endif
+constexpr int kUT = FP8BS_UT;   // vectors in flight per thread (per-tensor)
 }  // namespace
 
 cudaError_t launch_quant_1x128(const uint16_t* x, int64_t rows, int64_t cols, int64_t ldx,
                                int fmt, int mode, uint8_t* q, int64_t ldq, float* scales,
                                cudaStream_t st) {
-    const int64_t ntiles = rows * (cols / 128);
-    const int64_t grid = (ntiles + 16 * kU1 - 1) / (16 * kU1);
-    if (grid > 0x7FFFFFFF) return cudaErrorInvalidValue;
+    const int64_t gx = (rows + 16 * kU1 - 1) / (16 * kU1), gy = cols / 128;
+    if (gx > 0x7FFFFFFF || gy > 65535) return cudaErrorInvalidValue;
     auto k = fmt == 0 ? (mode == 0 ? k_quant_1x128<0, 0, kU1> : k_quant_1x128<0, 1, kU1>)
                       : (mode == 0 ? k_quant_1x128<1, 0, kU1> : k_quant_1x128<1, 1, kU1>);
-    k<<<static_cast<unsigned>(grid), 256, 0, st>>>(x, rows, ldx, ntiles, q, ldq, scales);
+    k<<<dim3(static_cast<unsigned>(gx), static_cast<unsigned>(gy)), 256, 0, st>>>(x, rows, ldx, q, ldq,
+                                                                                 scales);
     return cudaGetLastError();
 }
 

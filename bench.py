@@ -1,15 +1,21 @@
 #!/usr/bin/env python
 """Benchmark of the FP8 linear layer on GB300: block quantization + block-scaled
-FP8 GEMM, reported as quant+GEMM TFLOP/s of the Llama-3.1-8B-shaped fprop
-linears (M = 8192 tokens; QKV 4096->6144, O 4096->4096, gate+up 4096->28672,
-down 14336->4096; X per 1x128, W per 128x128, E4M3, fp32 scales, bf16 out).
+FP8 GEMM, reported as quant+GEMM TFLOP/s.
 
-One step = for each linear: quantize X (1x128), re-quantize W (128x128, the
-weights change every optimizer step), GEMM -> Y bf16.  Inputs are synthetic
-(seeded, X ~ N(0,1) with 1% outlier channels x20, W ~ N(0, 0.02)), resident
-in HBM; the step streams ~1.2 GB, larger than the 129 MB L2.
+Default workload (the JSON line the contract asks for): the Llama-3.1-8B-shaped
+fprop linears (M = 8192 tokens; QKV 4096->6144, O 4096->4096, gate+up
+4096->28672, down 14336->4096; X per 1x128, W per 128x128, E4M3, fp32 scales,
+bf16 out).  One step = for each linear: quantize X (1x128), re-quantize W
+(128x128, the weights change every optimizer step), GEMM -> Y.
 
-  python bench.py [--steps K] [--warmup W] [--impl ours|reference]
+Other workloads (--workload): llama2-7b-fprop (pow2 scales, M=4096),
+llama3.1-8b-mlp-bwd (per-tensor delayed E5M2 dY, dgrad + wgrad on transposed
+operands), qwen3-30b-a3b-moe (grouped expert GEMMs).
+
+Inputs are synthetic (seeded), resident in HBM; every step streams more than
+the 129 MB L2.
+
+  python bench.py [--steps K] [--warmup W] [--impl ours|reference] [--workload NAME]
 Under torchrun (--gpus N) every rank runs the same workload on its own GPU
 (independent replicas, weak scaling); rank 0 prints one JSON line.
 """
@@ -22,6 +28,7 @@ import subprocess
 import sys
 import threading
 import time
+from collections import defaultdict
 
 import numpy as np
 
@@ -30,7 +37,6 @@ sys.path.insert(0, ROOT)
 
 from block_scaled_gemm_quantize_gb300 import inputs as W_  # noqa: E402
 
-WORKLOAD = W_.LLAMA31_8B_FPROP
 METRIC = "block-scaled FP8 linear TFLOPS (quant+GEMM) and % of GB300 dense FP8 peak"
 FP8_OVER_BF16 = 2.0      # nominal dense fp8 / bf16 tensor ratio (4.5 / 2.25 PFLOP/s)
 
@@ -46,10 +52,8 @@ def _peaks():
 
 
 def _dist():
-    ws = int(os.environ.get("WORLD_SIZE", "1"))
-    rank = int(os.environ.get("RANK", "0"))
-    local = int(os.environ.get("LOCAL_RANK", "0"))
-    return ws, rank, local
+    return (int(os.environ.get("WORLD_SIZE", "1")), int(os.environ.get("RANK", "0")),
+            int(os.environ.get("LOCAL_RANK", "0")))
 
 
 class Clocks:
@@ -104,120 +108,271 @@ class Clocks:
                 "power_w_max": max(pw) if pw else None}
 
 
-# ------------------------------------------------------------ workload
-def make_inputs(device, seed=0, only=None):
-    """Synthetic bf16 inputs on the device, per linear: X [M, K], W [N, K]."""
-    import torch
-    g = torch.Generator(device=device)
-    M = WORKLOAD["M"]
-    bufs = []
-    for i, (name, N, K) in enumerate(WORKLOAD["linears"]):
-        if only and name != only:
-            continue
-        g.manual_seed(seed * 1000 + i)
-        x = torch.randn((M, K), generator=g, device=device, dtype=torch.float32)
-        n_out = int(round(0.01 * K))
-        cols = torch.randperm(K, generator=g, device=device)[:n_out]
-        x[:, cols] *= 20.0
-        w = torch.randn((N, K), generator=g, device=device, dtype=torch.float32) * 0.02
-        bufs.append((name, N, K, x.to(torch.bfloat16), w.to(torch.bfloat16)))
-        del x, w
-    return bufs
+class Rec:
+    """Per-phase CUDA events on the launching (current) stream."""
 
-
-class Step:
-    """Preallocated quant+GEMM pass over every linear of the workload."""
-
-    def __init__(self, bufs, fp8, device):
+    def __init__(self):
         import torch
-        self.fp8, self.items = fp8, []
-        M = WORKLOAD["M"]
-        for name, N, K, x, w in bufs:
-            qx = torch.empty((M, K), dtype=torch.uint8, device=device)
-            sx = torch.empty((K // 128, M), dtype=torch.float32, device=device)
-            qw = torch.empty((N, K), dtype=torch.uint8, device=device)
-            sw = torch.empty(((N + 127) // 128, K // 128), dtype=torch.float32, device=device)
-            y = torch.empty((M, N), dtype=torch.bfloat16, device=device)
-            A = fp8.operand(qx, sx, fp8.E4M3, fp8.GRAN_1x128)
-            B = fp8.operand(qw, sw, fp8.E4M3, fp8.GRAN_128x128)
-            self.items.append(dict(name=name, N=N, K=K, x=x, w=w, qx=qx, sx=sx, qw=qw, sw=sw, y=y,
-                                   A=A, B=B))
-        self.M = M
-        self.flops = sum(2.0 * M * it["N"] * it["K"] for it in self.items)
+        self.torch, self.ev = torch, []
+
+    def __call__(self, kind, fn):
+        e0 = self.torch.cuda.Event(enable_timing=True)
+        e1 = self.torch.cuda.Event(enable_timing=True)
+        e0.record()
+        fn()
+        e1.record()
+        self.ev.append((kind, e0, e1))
+
+    def totals(self):
+        t = defaultdict(float)
+        for kind, e0, e1 in self.ev:
+            t[kind] += e0.elapsed_time(e1)
+        return t
+
+
+def _run(rec, kind, fn):
+    if rec is None:
+        fn()
+    else:
+        rec(kind, fn)
+
+
+def _randn(g, shape, device, std=1.0):
+    import torch
+    return torch.randn(shape, generator=g, device=device, dtype=torch.float32) * std
+
+
+def _activations(g, M, K, device):
+    """N(0,1) with round(1% of K) outlier channels x20 (bf16)."""
+    import torch
+    x = _randn(g, (M, K), device)
+    cols = torch.randperm(K, generator=g, device=device)[: int(round(0.01 * K))]
+    x[:, cols] *= 20.0
+    return x.to(torch.bfloat16)
+
+
+# ------------------------------------------------------------- workloads
+class Fprop:
+    """quant X (1x128) + quant W (128x128) + GEMM for each linear."""
+
+    def __init__(self, cfg, fp8, device, seed=0, only=None):
+        import torch
+        self.cfg, self.fp8 = cfg, fp8
+        self.mode = fp8.SCALE_POW2 if cfg["scale_mode"] == "pow2" else fp8.SCALE_FP32
+        M = self.M = cfg["M"]
+        g = torch.Generator(device=device)
+        self.items = []
+        for i, (name, N, K) in enumerate(cfg["linears"]):
+            if only and name != only:
+                continue
+            g.manual_seed(seed * 1000 + i)
+            x = _activations(g, M, K, device)
+            w = (_randn(g, (N, K), device, 0.02)).to(torch.bfloat16)
+            it = dict(name=name, N=N, K=K, x=x, w=w,
+                      qx=torch.empty((M, K), dtype=torch.uint8, device=device),
+                      sx=torch.empty((K // 128, M), dtype=torch.float32, device=device),
+                      qw=torch.empty((N, K), dtype=torch.uint8, device=device),
+                      sw=torch.empty(((N + 127) // 128, K // 128), dtype=torch.float32, device=device),
+                      y=torch.empty((M, N), dtype=torch.bfloat16, device=device))
+            it["A"] = fp8.operand(it["qx"], it["sx"], fp8.E4M3, fp8.GRAN_1x128)
+            it["B"] = fp8.operand(it["qw"], it["sw"], fp8.E4M3, fp8.GRAN_128x128)
+            self.items.append(it)
+        self.units = [(it["name"], 2.0 * M * it["N"] * it["K"],
+                       M * it["K"] * 3 + 4 * M * (it["K"] // 128) + it["N"] * it["K"] * 3
+                       + 4 * ((it["N"] + 127) // 128) * (it["K"] // 128)) for it in self.items]
+        self.flops = sum(u[1] for u in self.units)
         self.launches = 3 * len(self.items)
+        self.config = {"workload": cfg["name"] + (f" ({only} only)" if only else ""), "M": M,
+                       "linears": [[it["name"], it["N"], it["K"]] for it in self.items],
+                       "scales": f"{cfg['scale_mode']} 1x128 (X) / 128x128 (W)", "out": "bf16"}
 
-    def run(self, ev=None):
+    def step(self, rec=None):
+        fp8, M, mode = self.fp8, self.M, self.mode
+        for it in self.items:
+            _run(rec, "quant:" + it["name"], lambda it=it: (
+                fp8.fp8_quantize_1x128(it["x"], fp8.E4M3, mode, q=it["qx"], scales=it["sx"]),
+                fp8.fp8_quantize_128x128(it["w"], fp8.E4M3, mode, q=it["qw"], scales=it["sw"])))
+            _run(rec, "gemm:" + it["name"], lambda it=it: fp8.fp8_block_gemm(
+                it["A"], it["B"], M, it["N"], it["K"], fp8.OUT_BF16, mode, y=it["y"]))
+
+    def host_io(self):
+        return [it["x"] for it in self.items] + [it["w"] for it in self.items], [it["y"] for it in self.items]
+
+
+class MlpBwd:
+    """Backward of the Llama-3.1-8B MLP under the hybrid delayed recipe: per
+    linear, dY (E5M2, per-tensor delayed) is quantized with the scale in use,
+    dgrad dX = dY W (W stored transposed for the product) and wgrad
+    dW = dY^T X (dY, X transposed) run with per-tensor scales, then the amax
+    history of dY advances.  X and W are E4M3 per-tensor delayed (quantized
+    once, as the forward pass leaves them)."""
+
+    def __init__(self, cfg, fp8, device, seed=0, only=None):
+        import torch
+        self.fp8, self.M = fp8, cfg["M"]
+        M = self.M
+        g = torch.Generator(device=device)
+        self.items = []
+        for i, (name, n_out, k_in) in enumerate(cfg["linears"]):
+            if only and name != only:
+                continue
+            g.manual_seed(seed * 1000 + 100 + i)
+            # Student-t(nu) = N(0,1) / sqrt(chi2(nu)/nu), from the seeded generator
+            z = _randn(g, (M, n_out), device)
+            chi = sum(_randn(g, (M, n_out), device) ** 2 for _ in range(int(cfg["dy_nu"])))
+            dy = (z / torch.sqrt(chi / cfg["dy_nu"]) * cfg["dy_scale"]).to(torch.bfloat16)
+            del z, chi
+            x = _activations(g, M, k_in, device)
+            w = _randn(g, (n_out, k_in), device, 0.02).to(torch.bfloat16)
+            st_dy = fp8.DelayedScaling(cfg["history_len"], fp8.E5M2, cfg["margin"], device=device)
+            st_x = fp8.DelayedScaling(cfg["history_len"], fp8.E4M3, cfg["margin"], device=device)
+            st_w = fp8.DelayedScaling(cfg["history_len"], fp8.E4M3, cfg["margin"], device=device)
+            qx = st_x.quantize(x)           # one step gives X and W a measured scale
+            qw = st_w.quantize(w)
+            qx = st_x.quantize(x, q=qx, update=False)
+            qw = st_w.quantize(w, q=qw, update=False)
+            it = dict(name=name, n_out=n_out, k_in=k_in, dy=dy, st_dy=st_dy,
+                      qdy=torch.empty((M, n_out), dtype=torch.uint8, device=device), qx=qx, qw=qw,
+                      dx=torch.empty((M, k_in), dtype=torch.bfloat16, device=device),
+                      dw=torch.empty((n_out, k_in), dtype=torch.float32, device=device))
+            E4, E5, T = fp8.E4M3, fp8.E5M2, fp8.GRAN_TENSOR
+            it["A_dg"] = fp8.operand(it["qdy"], st_dy.scale, E5, T)                   # [M][n_out]
+            it["B_dg"] = fp8.operand(qw, st_w.scale, E4, T, transposed=True)          # W^T
+            it["A_wg"] = fp8.operand(it["qdy"], st_dy.scale, E5, T, transposed=True)  # dY^T
+            it["B_wg"] = fp8.operand(qx, st_x.scale, E4, T, transposed=True)          # X^T
+            self.items.append(it)
+        self.units = []
+        for it in self.items:
+            f = 2.0 * M * it["n_out"] * it["k_in"]
+            self.units += [(it["name"] + ".dgrad", f, 0), (it["name"] + ".wgrad", f, 0)]
+        self.quant_bytes = sum(3 * M * it["n_out"] + 4 for it in self.items)
+        self.flops = sum(u[1] for u in self.units)
+        self.launches = 4 * len(self.items)     # delayed quant, history, dgrad, wgrad
+        self.config = {"workload": cfg["name"] + (f" ({only} only)" if only else ""), "M": M,
+                       "linears": [[it["name"], it["n_out"], it["k_in"]] for it in self.items],
+                       "scales": "per-tensor delayed (dY E5M2, X/W E4M3), history "
+                                 f"{cfg['history_len']}, margin {cfg['margin']}",
+                       "out": "dX bf16, dW fp32"}
+
+    def step(self, rec=None):
         fp8, M = self.fp8, self.M
-        for i, it in enumerate(self.items):
-            if ev is not None:
-                ev[i][0].record()
-            fp8.fp8_quantize_1x128(it["x"], fp8.E4M3, fp8.SCALE_FP32, q=it["qx"], scales=it["sx"])
-            fp8.fp8_quantize_128x128(it["w"], fp8.E4M3, fp8.SCALE_FP32, q=it["qw"], scales=it["sw"])
-            if ev is not None:
-                ev[i][1].record()
-            fp8.fp8_block_gemm(it["A"], it["B"], M, it["N"], it["K"], fp8.OUT_BF16, fp8.SCALE_FP32,
-                               y=it["y"])
-            if ev is not None:
-                ev[i][2].record()
+        for it in self.items:
+            _run(rec, "quant:" + it["name"], lambda it=it: it["st_dy"].quantize(it["dy"], q=it["qdy"],
+                                                                               update=False))
+            _run(rec, "gemm:" + it["name"] + ".dgrad", lambda it=it: fp8.fp8_block_gemm(
+                it["A_dg"], it["B_dg"], M, it["k_in"], it["n_out"], fp8.OUT_BF16, y=it["dx"]))
+            _run(rec, "gemm:" + it["name"] + ".wgrad", lambda it=it: fp8.fp8_block_gemm(
+                it["A_wg"], it["B_wg"], it["n_out"], it["k_in"], M, fp8.OUT_F32, y=it["dw"]))
+            _run(rec, "quant:" + it["name"], lambda it=it: it["st_dy"].update())
+
+    def host_io(self):
+        return [it["dy"] for it in self.items], [it["dx"] for it in self.items] + [it["dw"] for it in self.items]
 
 
-def quant_bytes(M, N, K):
-    """Algorithmic bytes of the two quantizers of one linear: bf16 read,
-    one code byte written, one fp32 scale per 1x128 / 128x128 tile."""
-    x = M * K * 3 + 4 * M * (K // 128)
-    w = N * K * 3 + 4 * ((N + 127) // 128) * (K // 128)
-    return x + w
+class MoE:
+    """Qwen3-30B-A3B-style expert GEMMs: 8192 tokens x top-8 of 128 experts
+    (Zipf(1.1) loads), gate+up 2048->1536 and down 768->2048 per expert as two
+    grouped block-scaled GEMMs over the expert-sorted rows."""
+
+    def __init__(self, cfg, fp8, device, seed=0, only=None):
+        import torch
+        self.fp8 = fp8
+        loads, off = W_.moe_routing(cfg["tokens"], cfg["experts"], cfg["topk"], cfg["zipf_a"], seed=seed)
+        self.T = T = int(off[-1])
+        G, H, I = cfg["experts"], cfg["hidden"], cfg["gate_up_n"]
+        self.off = torch.from_numpy(off).to(device)
+        g = torch.Generator(device=device)
+        g.manual_seed(seed * 1000 + 500)
+        self.items = []
+        for name, N, K in (("gate_up", I, H), ("down", H, cfg["down_k"])):
+            if only and name != only:
+                continue
+            x = _randn(g, (T, K), device).to(torch.bfloat16)
+            w = _randn(g, (G * N, K), device, 0.02).to(torch.bfloat16)
+            it = dict(name=name, N=N, K=K, x=x, w=w,
+                      qx=torch.empty((T, K), dtype=torch.uint8, device=device),
+                      sx=torch.empty((K // 128, T), dtype=torch.float32, device=device),
+                      qw=torch.empty((G * N, K), dtype=torch.uint8, device=device),
+                      sw=torch.empty((G * N // 128, K // 128), dtype=torch.float32, device=device),
+                      y=torch.empty((T, N), dtype=torch.bfloat16, device=device))
+            it["A"] = fp8.operand(it["qx"], it["sx"], fp8.E4M3, fp8.GRAN_1x128)
+            it["B"] = fp8.operand(it["qw"], it["sw"], fp8.E4M3, fp8.GRAN_128x128)
+            self.items.append(it)
+        self.units = [(it["name"], 2.0 * T * it["N"] * it["K"],
+                       3 * T * it["K"] + 3 * G * it["N"] * it["K"]) for it in self.items]
+        self.flops = sum(u[1] for u in self.units)
+        self.launches = 3 * len(self.items)
+        self.config = {"workload": cfg["name"] + (f" ({only} only)" if only else ""), "rows": T,
+                       "experts": G, "max_rows": int(loads.max()), "min_rows": int(loads.min()),
+                       "linears": [[it["name"], it["N"], it["K"]] for it in self.items],
+                       "scales": "fp32 1x128 (X) / 128x128 (W)", "out": "bf16"}
+
+    def step(self, rec=None):
+        fp8, T = self.fp8, self.T
+        for it in self.items:
+            # the stacked [G*N][K] weights quantize per expert tile since N % 128 == 0
+            _run(rec, "quant:" + it["name"], lambda it=it: (
+                fp8.fp8_quantize_1x128(it["x"], q=it["qx"], scales=it["sx"]),
+                fp8.fp8_quantize_128x128(it["w"], q=it["qw"], scales=it["sw"])))
+            _run(rec, "gemm:" + it["name"], lambda it=it: fp8.fp8_grouped_block_gemm(
+                self.off, it["A"], it["B"], T, it["N"], it["K"], fp8.OUT_BF16, y=it["y"]))
+
+    def host_io(self):
+        return [it["x"] for it in self.items] + [it["w"] for it in self.items], [it["y"] for it in self.items]
+
+
+WORKLOADS = {"llama3.1-8b-fprop": (Fprop, W_.LLAMA31_8B_FPROP),
+             "llama2-7b-fprop": (Fprop, W_.LLAMA2_7B_FPROP),
+             "tiny-fprop": (Fprop, W_.TINY_FPROP),
+             "llama3.1-8b-mlp-bwd": (MlpBwd, W_.LLAMA31_8B_MLP_BWD),
+             "qwen3-30b-a3b-moe": (MoE, W_.QWEN3_30B_MOE)}
 
 
 # ------------------------------------------------------------ CPU oracle
-def cpu_oracle_sample(rows_x, w_bits, xs_bits, rows=8):
-    """Time the oracle on a bounded sample: per linear, quantize the full W
-    (128x128) and `rows` rows of X (1x128), and compute those rows of Y in
-    fp64.  Returns (seconds, flops of the sample)."""
+def cpu_oracle_sample(wl, rows=8):
+    """Time the oracle on a bounded sample of an fprop workload: per linear,
+    quantize the full W (128x128) and `rows` rows of X (1x128), and compute
+    those rows of Y in fp64.  Returns (seconds, flops of the sample)."""
+    import torch
     import oracle as orc
+    xs = [it["x"][:rows].contiguous().view(torch.int16).cpu().numpy().view(np.uint16) for it in wl.items]
+    ws = [it["w"].contiguous().view(torch.int16).cpu().numpy().view(np.uint16) for it in wl.items]
+    mode = orc.SCALE_POW2 if wl.mode == wl.fp8.SCALE_POW2 else orc.SCALE_FP32
     t0 = time.perf_counter()
     flops = 0.0
-    for x, w in zip(xs_bits, w_bits):
+    for x, w in zip(xs, ws):
         N, K = w.shape
-        qw, sw = orc.quantize_128x128(w)
-        qx, sx = orc.quantize_1x128(x[:rows])
-        A = orc.operand(qx, orc.E4M3, orc.GRAN_1x128, sx)
-        B = orc.operand(qw, orc.E4M3, orc.GRAN_128x128, sw)
-        orc.gemm(rows, N, K, A, B)
+        qw, sw = orc.quantize_128x128(w, orc.E4M3, mode)
+        qx, sx = orc.quantize_1x128(x, orc.E4M3, mode)
+        orc.gemm(rows, N, K, orc.operand(qx, orc.E4M3, orc.GRAN_1x128, sx),
+                 orc.operand(qw, orc.E4M3, orc.GRAN_128x128, sw))
         flops += 2.0 * rows * N * K
     return time.perf_counter() - t0, flops
-
-
-def host_sample(bufs, rows):
-    import torch
-    xs, ws = [], []
-    for _, N, K, x, w in bufs:
-        xs.append(x[:rows].contiguous().view(torch.int16).cpu().numpy().view(np.uint16))
-        ws.append(w.contiguous().view(torch.int16).cpu().numpy().view(np.uint16))
-    return xs, ws
 
 
 # ------------------------------------------------------------------ arms
 def run_reference(args):
     """The oracle as it stands on this host's cores; each step is a bounded
-    sample of the workload (per linear: 128 rows of W quantized 128x128, 4 rows
-    of X quantized 1x128, those 4 rows x 128 columns of Y in fp64)."""
+    sample of the fprop workload (per linear: 128 W rows quantized 128x128,
+    4 X rows quantized 1x128, those 4 rows x 128 columns of Y in fp64)."""
     ws, rank, _ = _dist()
     if rank != 0:
         return 0
     import oracle as orc
-    rng = np.random.default_rng(0)
-    lin = []
-    for name, N, K in WORKLOAD["linears"]:
-        x = W_.activations(4, K, seed=1)
-        w = W_.gaussian((128, K), 0.02, seed=2)
-        lin.append((x, w, K))
+    cls, cfg = WORKLOADS[args.workload]
+    if cls is not Fprop:
+        print(json.dumps({"impl": "reference", "unavailable":
+                          "the reference arm samples the fprop workloads only"}), flush=True)
+        return 0
+    mode = orc.SCALE_POW2 if cfg["scale_mode"] == "pow2" else orc.SCALE_FP32
+    lin = [(W_.activations(4, K, seed=1), W_.gaussian((128, K), 0.02, seed=2), K)
+           for _, N, K in cfg["linears"]]
 
     def step():
         f = 0.0
         for x, w, K in lin:
-            qw, sw = orc.quantize_128x128(w)
-            qx, sx = orc.quantize_1x128(x)
+            qw, sw = orc.quantize_128x128(w, orc.E4M3, mode)
+            qx, sx = orc.quantize_1x128(x, orc.E4M3, mode)
             orc.gemm(4, 128, K, orc.operand(qx, orc.E4M3, orc.GRAN_1x128, sx),
                      orc.operand(qw, orc.E4M3, orc.GRAN_128x128, sw))
             f += 2.0 * 4 * 128 * K
@@ -236,8 +391,8 @@ def run_reference(args):
             "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "impl": "reference",
-            "config": {"workload": WORKLOAD["name"], "M": WORKLOAD["M"],
-                       "linears": WORKLOAD["linears"], "sample": sample},
+            "config": {"workload": cfg["name"], "M": cfg["M"], "linears": cfg["linears"],
+                       "sample": sample},
             "cpu_baseline": {"value": val, "unit": "TFLOP/s", "cores": 1, "kind": "oracle",
                              "sample": sample},
             "e2e": {"value": val, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
@@ -256,10 +411,8 @@ def run_ours(args):
     device = torch.device("cuda", local)
     fp8.lib()
     peaks = _peaks()
-
-    bufs = make_inputs(device, seed=rank, only=args.only)
-    step = Step(bufs, fp8, device)
-    nlin = len(step.items)
+    cls, cfg = WORKLOADS[args.workload]
+    wl = cls(cfg, fp8, device, seed=rank, only=args.only)
 
     def barrier():
         if ws > 1:
@@ -275,12 +428,11 @@ def run_ours(args):
         return float(t.item())
 
     for _ in range(args.warmup):
-        step.run()
+        wl.step()
     torch.cuda.synchronize()
 
-    # --- timed region: K steps, per-kernel events on the launching stream
-    evs = [[[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(nlin)]
-           for _ in range(args.steps)]
+    # --- timed region: K steps, per-phase events on the launching stream
+    rec = Rec()
     clocks = Clocks(local)
     clocks.start()
     time.sleep(0.3)
@@ -289,53 +441,49 @@ def run_ours(args):
     t_start = torch.cuda.Event(enable_timing=True)
     t_end = torch.cuda.Event(enable_timing=True)
     t_start.record()
-    for k in range(args.steps):
-        step.run(evs[k])
+    for _ in range(args.steps):
+        wl.step(rec)
     t_end.record()
     torch.cuda.synchronize()
     barrier()
     clk = clocks.stop()
     fp8.device_status()
     ms = max_over_ranks(t_start.elapsed_time(t_end)) / args.steps
+    tot = {k: v / args.steps for k, v in rec.totals().items()}
 
-    gemm_ms = np.zeros(nlin)
-    quant_ms = np.zeros(nlin)
-    for k in range(args.steps):
-        for i in range(nlin):
-            quant_ms[i] += evs[k][i][0].elapsed_time(evs[k][i][1])
-            gemm_ms[i] += evs[k][i][1].elapsed_time(evs[k][i][2])
-    gemm_ms /= args.steps
-    quant_ms /= args.steps
-    M = WORKLOAD["M"]
-    per_linear = []
-    for i, it in enumerate(step.items):
-        fl = 2.0 * M * it["N"] * it["K"]
-        qb = quant_bytes(M, it["N"], it["K"])
-        per_linear.append({"linear": it["name"], "M": M, "N": it["N"], "K": it["K"],
-                           "gemm_us": gemm_ms[i] * 1e3, "gemm_tflops": fl / gemm_ms[i] / 1e9,
-                           "quant_us": quant_ms[i] * 1e3, "quant_gbs": qb / quant_ms[i] / 1e6})
-    gemm_flops = sum(2.0 * M * it["N"] * it["K"] for it in step.items)
-    achieved = gemm_flops / gemm_ms.sum() / 1e9                     # TFLOP/s
+    per = []
+    gemm_ms = 0.0
+    gemm_flops = 0.0
+    for name, fl, qb in wl.units:
+        g = tot.get("gemm:" + name, 0.0)
+        q = tot.get("quant:" + name, 0.0)
+        gemm_ms += g
+        gemm_flops += fl
+        e = {"unit": name, "gemm_us": g * 1e3, "gemm_tflops": fl / g / 1e9 if g else None}
+        if q:
+            e.update({"quant_us": q * 1e3, "quant_gbs": qb / q / 1e6 if qb else None})
+        per.append(e)
+    quant_ms = sum(v for k, v in tot.items() if k.startswith("quant:"))
+    qbytes = getattr(wl, "quant_bytes", None) or sum(u[2] for u in wl.units)
+    achieved = gemm_flops / gemm_ms / 1e9
     fp8_peak = FP8_OVER_BF16 * peaks["bf16_sustained"]
-    qbytes = sum(quant_bytes(M, it["N"], it["K"]) for it in step.items)
-    quant_gbs = qbytes / quant_ms.sum() / 1e6
+    quant_gbs = qbytes / quant_ms / 1e6 if quant_ms else None
 
     # --- end to end through host buffers (pinned), copies inside the timed region
     e2e = None
     if not args.no_e2e:
-        hx = [it["x"].cpu().pin_memory() for it in step.items]
-        hw = [it["w"].cpu().pin_memory() for it in step.items]
-        hy = [torch.empty(it["y"].shape, dtype=it["y"].dtype).pin_memory() for it in step.items]
-        h2d = sum(t.numel() * 2 for t in hx + hw)
-        d2h = sum(t.numel() * 2 for t in hy)
+        ins, outs = wl.host_io()
+        h_in = [t.cpu().pin_memory() for t in ins]
+        h_out = [torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in outs]
+        h2d = sum(t.numel() * t.element_size() for t in h_in)
+        d2h = sum(t.numel() * t.element_size() for t in h_out)
 
         def e2e_step():
-            for i, it in enumerate(step.items):
-                it["x"].copy_(hx[i], non_blocking=True)
-                it["w"].copy_(hw[i], non_blocking=True)
-            step.run()
-            for i, it in enumerate(step.items):
-                hy[i].copy_(it["y"], non_blocking=True)
+            for h, d in zip(h_in, ins):
+                d.copy_(h, non_blocking=True)
+            wl.step()
+            for h, d in zip(h_out, outs):
+                h.copy_(d, non_blocking=True)
 
         e2e_steps = max(3, min(args.steps, 20))
         for _ in range(3):
@@ -350,30 +498,27 @@ def run_ours(args):
         b.record()
         torch.cuda.synchronize()
         e2e_ms = max_over_ranks(a.elapsed_time(b)) / e2e_steps
-        e2e = {"value": step.flops * ws / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+        e2e = {"value": wl.flops * ws / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
                "steps": e2e_steps}
 
     cpu = None
-    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
-        xs, wsb = host_sample(bufs, rows=8)
-        secs, fl = cpu_oracle_sample(None, wsb, xs, rows=8)
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline and cls is Fprop:
+        secs, fl = cpu_oracle_sample(wl, rows=8)
         cpu = {"value": fl / secs / 1e12, "unit": "TFLOP/s", "cores": 1, "kind": "oracle",
                "seconds": secs,
                "sample": "per linear: full W quantized 128x128, 8 X rows quantized 1x128, "
                          "8 full rows of Y in fp64 (single-threaded C oracle)"}
 
-    value = step.flops * ws / (ms * 1e-3) / 1e12
+    value = wl.flops * ws / (ms * 1e-3) / 1e12
+    config = dict(wl.config)
+    config.update({"l2": "inputs larger than L2 (each step streams > 129 MB)",
+                   "parallelism": f"replicas x{ws}"})
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": ws, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "e4m3 (fp32 accumulate, bf16 out)", "data": "synthetic",
-        "config": {"workload": WORKLOAD["name"] + (f" ({args.only} only)" if args.only else ""),
-                   "M": M, "linears": [list(l) for l in WORKLOAD["linears"]
-                                       if not args.only or l[0] == args.only],
-                   "scales": "fp32 1x128 (X) / 128x128 (W)", "out": "bf16",
-                   "l2": "inputs larger than L2 (each step streams ~1.2 GB)",
-                   "parallelism": f"replicas x{ws}"},
+        "vs_baseline": None, "dtype": "e4m3/e5m2 (fp32 accumulate)", "data": "synthetic",
+        "config": config,
         "pct_of_fp8_peak": 100.0 * value / fp8_peak,
         "roofline": {"bound": "tensor", "kernel": "k_fp8_gemm", "achieved": achieved,
                      "peak": fp8_peak, "unit": "TFLOP/s", "frac": achieved / fp8_peak,
@@ -381,10 +526,10 @@ def run_ours(args):
                      "peak_src": f"{peaks['src']}: 2 x bf16_tflops_sustained "
                                  f"({peaks['bf16_sustained']})"},
         "quant_roofline": {"bound": "hbm", "achieved": quant_gbs, "peak": peaks["hbm_gbs"],
-                           "unit": "GB/s", "frac": quant_gbs / peaks["hbm_gbs"]},
-        "per_linear": per_linear,
+                           "unit": "GB/s", "frac": quant_gbs / peaks["hbm_gbs"] if quant_gbs else None},
+        "per_unit": per,
         "clocks": clk,
-        "gpu_launches": step.launches * args.steps,
+        "gpu_launches": wl.launches * args.steps,
         "e2e": e2e,
         "cpu_baseline": cpu,
     }
@@ -402,10 +547,10 @@ def main():
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", choices=list(WORKLOADS), default="llama3.1-8b-fprop")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--only", choices=[l[0] for l in WORKLOAD["linears"]], default=None,
-                    help="run a single linear of the workload (profiling)")
+    ap.add_argument("--only", default=None, help="run a single linear of the workload (profiling)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

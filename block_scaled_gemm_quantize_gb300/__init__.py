@@ -186,12 +186,19 @@ class DelayedScaling:
         self.scale = torch.ones(1, dtype=torch.float32, device=device)
         self.amax = torch.zeros(1, dtype=torch.float32, device=device)
 
-    def quantize(self, x, q=None, stream=None):
-        """Quantize x with the scale in use, then fold its amax into the state."""
+    def quantize(self, x, q=None, stream=None, update=True):
+        """Quantize x with the scale in use, then (update=True) fold its amax
+        into the state.  With update=False the caller runs update() later --
+        e.g. after the GEMMs that read `scale` as this step's dequant scale."""
         q, _ = fp8_quantize_tensor_delayed(x, self.fmt, self.scale, q=q, amax=self.amax, stream=stream)
+        if update:
+            self.update(stream=stream)
+        return q
+
+    def update(self, stream=None):
+        """Push this step's amax into the history and compute the next scale."""
         fp8_amax_history_update(self.history, self.head, self.amax, self.fmt, self.margin,
                                 self.scale, stream=stream)
-        return q
 
     def state_dict(self):
         return {"history": self.history.cpu(), "head": self.head.cpu(), "scale": self.scale.cpu(),

@@ -69,6 +69,7 @@ def lib() -> ctypes.CDLL:
             "fp8_block_gemm": [i64, i64, i64, op, op, i32, vp, i64, i32, vp],
             "fp8_grouped_block_gemm": [i32, vp, i64, i64, i64, op, op, i32, vp, i64, i32, vp],
             "fp8bs_device_status": [vp],
+            "fp8bs_selftest_wait_timeout": [i32, vp, vp],
             "fp8bs_version": [],
             "fp8bs_last_error": [],
         }
@@ -195,8 +196,12 @@ class DelayedScaling:
             self.update(stream=stream)
         return q
 
-    def update(self, stream=None):
-        """Push this step's amax into the history and compute the next scale."""
+    def update(self, stream=None, group=None):
+        """Push this step's amax into the history and compute the next scale.
+        With a process group, the amax is first reduced (MAX) over its ranks,
+        so every data-parallel replica advances the same history."""
+        if group is not None:
+            reduce_amax(self.amax, group)
         fp8_amax_history_update(self.history, self.head, self.amax, self.fmt, self.margin,
                                 self.scale, stream=stream)
 
@@ -267,6 +272,24 @@ def linear_fprop(x, w, mode=SCALE_FP32, out_dtype=OUT_BF16, stream=None):
 def device_status(stream=None) -> None:
     """Raise if a kernel gave up on a bounded device wait (synchronizes)."""
     _call("fp8bs_device_status", _stream(stream))
+
+
+def selftest_wait_timeout(limit_ms: int = 200, stream=None) -> bool:
+    """Run the bounded-wait self-test; returns True if the wait gave up (and
+    leaves the timeout recorded for device_status())."""
+    torch = _torch()
+    out = torch.full((1,), -1, dtype=torch.int32, device="cuda")
+    _call("fp8bs_selftest_wait_timeout", limit_ms, out.data_ptr(), _stream(stream))
+    torch.cuda.current_stream().synchronize() if stream is None else stream.synchronize()
+    return int(out.item()) == 0
+
+
+def reduce_amax(amax, group=None):
+    """Data-parallel exchange of delayed scaling: element-wise MAX of this
+    step's amax over the ranks of `group` (torch.distributed), in place."""
+    import torch.distributed as dist
+    dist.all_reduce(amax, op=dist.ReduceOp.MAX, group=group)
+    return amax
 
 
 def version() -> int:

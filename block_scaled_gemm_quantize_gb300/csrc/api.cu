@@ -286,6 +286,15 @@ int fp8_grouped_block_gemm(int32_t num_groups, const int32_t* row_offsets, int64
                     mode, Y, ld_y, out_dtype, (cudaStream_t)stream);
 }
 
+int fp8bs_selftest_wait_timeout(int32_t limit_ms, int32_t* waited_ok, fp8bs_stream_t stream) {
+    const char* fn = "fp8bs_selftest_wait_timeout";
+    if (!waited_ok) return fail(FP8BS_ERR_INVALID_ARG, "%s: null output", fn);
+    if (limit_ms < 1 || limit_ms > 10000) return fail(FP8BS_ERR_INVALID_ARG, "%s: limit_ms in [1, 10000]", fn);
+    cudaError_t e = fp8bs::launch_wait_selftest(static_cast<uint64_t>(limit_ms) * 1000000ull, waited_ok,
+                                                (cudaStream_t)stream);
+    return e == cudaSuccess ? FP8BS_OK : cuda_fail(e, fn);
+}
+
 int fp8bs_device_status(fp8bs_stream_t stream) {
     cudaError_t e = cudaStreamSynchronize((cudaStream_t)stream);
     if (e != cudaSuccess) return cuda_fail(e, "fp8bs_device_status");

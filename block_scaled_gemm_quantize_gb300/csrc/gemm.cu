@@ -490,7 +490,27 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     }
 }
 
+// Self-test of the bounded wait: one thread waits on an mbarrier that nothing
+// arrives at, with a limit of `limit_ns`; on expiry it records the timeout in
+// g_status exactly as the GEMM roles do, and the kernel returns normally.
+__global__ void k_wait_selftest(uint64_t limit_ns, int* out) {
+    __shared__ __align__(8) uint64_t bar;
+    if (threadIdx.x == 0) {
+        const uint32_t b = smem_u32(&bar);
+        mbar_init(b, 1);
+        fence_mbar_init();
+        const bool ok = wait_bounded(b, 0, limit_ns);
+        if (!ok) atomicExch(&g_status, kStatusDeviceTimeout);
+        *out = ok ? 1 : 0;
+    }
+}
+
 }  // namespace
+
+cudaError_t launch_wait_selftest(uint64_t limit_ns, int* out, cudaStream_t st) {
+    k_wait_selftest<<<1, 32, 0, st>>>(limit_ns, out);
+    return cudaGetLastError();
+}
 
 uint32_t gemm_smem_bytes() { return SMEM_BYTES; }
 

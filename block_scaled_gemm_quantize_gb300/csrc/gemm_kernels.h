@@ -39,5 +39,6 @@ int gemm_tile_m();
 cudaError_t launch_fp8_gemm(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmY,
                             const GemmParams& p, bool a_mn, bool b_mn, int grid, cudaStream_t st);
 cudaError_t read_and_clear_status(int* status);
+cudaError_t launch_wait_selftest(uint64_t limit_ns, int* out, cudaStream_t st);
 
 }  // namespace fp8bs

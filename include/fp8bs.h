@@ -206,6 +206,15 @@ const char* fp8bs_last_error(void);
  * the record), FP8BS_ERR_CUDA on a CUDA error, else FP8BS_OK. */
 int fp8bs_device_status(fp8bs_stream_t stream);
 
+/* Self-test of the device-side failure detection: launches one thread that
+ * waits, with the same bounded mbarrier wait the GEMM roles use, on a barrier
+ * nothing arrives at, giving up after `limit_ms` (1..10000).  It then records
+ * FP8BS_ERR_DEVICE_TIMEOUT exactly as a stalled GEMM would, writes 0 to the
+ * device int *waited_ok (1 if the wait had completed) and returns; the CUDA
+ * context stays usable.  fp8bs_device_status() afterwards reports the timeout.
+ * Errors: INVALID_ARG (null output, limit out of range). */
+int fp8bs_selftest_wait_timeout(int32_t limit_ms, int32_t* waited_ok, fp8bs_stream_t stream);
+
 /* Library version, for the binding's load check. */
 int fp8bs_version(void);
 

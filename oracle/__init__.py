@@ -57,7 +57,13 @@ def _load():
     global _lib
     with _lock:
         if _lib is None:
-            lib = ctypes.CDLL(build())
+            _lib = _bind(ctypes.CDLL(build()))
+    return _lib
+
+
+def _bind(lib):
+    if True:
+        if True:
             i64, i32, vp, f32 = ctypes.c_int64, ctypes.c_int32, ctypes.c_void_p, ctypes.c_float
             lib.fp8o_decode.argtypes = [ctypes.c_uint32, ctypes.c_int]
             lib.fp8o_decode.restype = ctypes.c_double
@@ -85,8 +91,45 @@ def _load():
             lib.fp8o_grouped_gemm.argtypes = [i32, vp, i64, i64, i64, ctypes.POINTER(Operand),
                                               ctypes.POINTER(Operand), i64, vp, i64, vp, vp, vp]
             lib.fp8o_grouped_gemm.restype = ctypes.c_int
-            _lib = lib
-    return _lib
+    return lib
+
+
+def build_variant(source: str, name: str) -> str:
+    """Compile a modified copy of the oracle source (tests that plant a
+    mistake in the oracle use this to show that the pins catch it)."""
+    os.makedirs(_BUILD, exist_ok=True)
+    src = os.path.join(_BUILD, f"{name}.c")
+    out = os.path.join(_BUILD, f"{name}_{platform.machine()}.so")
+    with open(src, "w") as f:
+        f.write(source)
+    subprocess.run(["gcc", "-std=c11", "-O2", "-ffp-contract=off", "-fno-fast-math", "-fPIC",
+                    "-shared", "-o", out, src, "-lm"], check=True)
+    return out
+
+
+class using_library:
+    """Context manager: route every oracle call through another compiled
+    oracle (a planted-mistake variant) and restore the real one on exit."""
+
+    def __init__(self, path: str):
+        self.path = path
+
+    def __enter__(self):
+        global _lib
+        _load()
+        self._old = _lib
+        _lib = _bind(ctypes.CDLL(self.path))
+        return self
+
+    def __exit__(self, *exc):
+        global _lib
+        _lib = self._old
+        return False
+
+
+def source() -> str:
+    with open(_SRC) as f:
+        return f.read()
 
 
 def _ptr(a: np.ndarray) -> int:

@@ -102,6 +102,20 @@ int make_out_map(CUtensorMap* m, void* base, bool bf16, uint64_t N, uint64_t row
     return FP8BS_OK;
 }
 
+// fp32 scale table [nkb][rows] (rows contiguous); box 128 rows x 1 K block.
+int make_scale_map(CUtensorMap* m, const float* base, uint64_t rows, uint64_t nkb) {
+    cuuint64_t dims[2] = {rows, nkb};
+    cuuint64_t strides[1] = {rows * 4};
+    cuuint32_t box[2] = {128, 1};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float*>(base), dims, strides, box,
+                          estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                          CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS)
+        return fail(FP8BS_ERR_CUDA, "cuTensorMapEncodeTiled (scales) failed (CUresult %d)", (int)r);
+    return FP8BS_OK;
+}
+
 int sm_count() {
     int dev = 0, n = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return 0;
@@ -209,7 +223,22 @@ int run_gemm(const char* fn, int32_t G, const int32_t* offsets, int64_t a_rows, 
     if (sms <= 0) return fail(FP8BS_ERR_CUDA, "%s: cannot query the device", fn);
     const int grid = static_cast<int>(tiles < sms ? tiles : sms);
     if (grid <= 0) return FP8BS_OK;
-    cudaError_t e = fp8bs::launch_fp8_gemm(tmA, tmB, tmY, p, a_mn, b_mn, grid, stream);
+    // Power-of-two scales on K-major operands go to the block-scaled (MX)
+    // kernel: the tensor core applies the UE8M0 scales, no promotion.
+    cudaError_t e;
+#ifndef FP8BS_NO_MX
+    // (1x128 A scales reach the kernel by TMA: a row pitch of 16 bytes needed)
+    const bool sa_tma_ok = A->gran != FP8BS_GRAN_1x128 || (a_rows % 4 == 0 && aligned16(A->scales));
+    if (mode == FP8BS_SCALE_POW2 && !a_mn && !b_mn && !grouped && sa_tma_ok) {
+        CUtensorMap tmSA;
+        memset(&tmSA, 0, sizeof(tmSA));
+        if (A->gran == FP8BS_GRAN_1x128 && (rc = make_scale_map(&tmSA, A->scales, a_rows, K / 128)) != FP8BS_OK)
+            return rc;
+        p.idesc = fp8bs::make_idesc_mx(A->fmt, B->fmt, BN);
+        e = fp8bs::launch_fp8_gemm_mx(tmA, tmB, tmY, tmSA, p, grid, stream);
+    } else
+#endif
+        e = fp8bs::launch_fp8_gemm(tmA, tmB, tmY, p, a_mn, b_mn, grid, stream);
     return e == cudaSuccess ? FP8BS_OK : cuda_fail(e, fn);
 }
 

@@ -111,6 +111,21 @@ __device__ __forceinline__ bool wait_or_flag(uint32_t bar, uint32_t parity) {
     return false;
 }
 
+// Bounded wait for a rare event (once per tile): backs off with nanosleep so
+// the waiting warps leave the issue slots to the producer and MMA warps.
+__device__ __forceinline__ bool wait_or_flag_sleepy(uint32_t bar, uint32_t parity) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = global_timer_ns();
+    while (true) {
+        __nanosleep(256);
+        if (mbar_try_wait(bar, parity)) return true;
+        if (global_timer_ns() - t0 > WAIT_LIMIT_NS) {
+            atomicExch(&g_status, kStatusDeviceTimeout);
+            return false;
+        }
+    }
+}
+
 struct Tile {
     int g, row0, row_end, nt;
 };
@@ -141,6 +156,79 @@ __device__ __forceinline__ Tile decode_tile(int t, int total_slots, int tiles_n,
 }
 
 __device__ __forceinline__ float ld_scale(const float* p) { return __ldg(p); }
+
+// Store one warp's 32 rows x 128 columns of a finished tile (acc = 128 fp32
+// as packed pairs): TMA bulk stores of 32 x 64-byte slabs when the warp's 32
+// rows all belong to the tile's group (TMA clips only at the tensor edge),
+// otherwise masked direct stores.
+__device__ __forceinline__ void store_tile(const GemmParams& p, const CUtensorMap& tmY,
+                                           const uint64_t (&acc)[64], const Tile& tl, int64_t row,
+                                           bool row_ok, int64_t col0, int quarter, int lane,
+                                           uint32_t slab) {
+    const int64_t wrow0 = static_cast<int64_t>(tl.row0) + quarter * 32;
+    if (p.tma_store && (p.offsets == nullptr || wrow0 + 32 <= tl.row_end)) {
+        const uint32_t rbase = slab + lane * 64;
+        const uint32_t sw = (lane >> 1) & 3;          // 64-B swizzle: chunk ^= (row/2)%4
+        const int passes = p.out_bf16 ? 4 : 8;        // 32 bf16 or 16 fp32 columns each
+#pragma unroll
+        for (int ps = 0; ps < 8; ps++) {
+            if (ps >= passes) break;
+            if (lane == 0) bulk_wait_group_read0();   // slab free again
+            __syncwarp();
+#pragma unroll
+            for (int c = 0; c < 4; c++) {
+                uint32_t w[4];
+                if (p.out_bf16) {
+#pragma unroll
+                    for (int i = 0; i < 4; i++) {
+                        const float2 f = unpack_f32x2(acc[ps * 16 + c * 4 + i]);
+                        __nv_bfloat162 h = __floats2bfloat162_rn(f.x, f.y);
+                        w[i] = *reinterpret_cast<uint32_t*>(&h);
+                    }
+                } else {
+                    const float2 a = unpack_f32x2(acc[ps * 8 + c * 2]);
+                    const float2 b = unpack_f32x2(acc[ps * 8 + c * 2 + 1]);
+                    w[0] = __float_as_uint(a.x); w[1] = __float_as_uint(a.y);
+                    w[2] = __float_as_uint(b.x); w[3] = __float_as_uint(b.y);
+                }
+                st_shared_v4(rbase + ((c ^ sw) << 4), w[0], w[1], w[2], w[3]);
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+                tma_store_2d(&tmY, slab, static_cast<int32_t>(col0 + ps * (p.out_bf16 ? 32 : 16)),
+                             static_cast<int32_t>(wrow0));
+                bulk_commit_group();
+            }
+        }
+    } else if (row_ok) {
+        if (p.out_bf16) {
+            uint16_t* y = reinterpret_cast<uint16_t*>(p.y) + row * p.ldy + col0;
+#pragma unroll
+            for (int j = 0; j < 128; j += 8) {
+                if (col0 + j < p.N) {
+                    uint32_t w[4];
+#pragma unroll
+                    for (int i = 0; i < 4; i++) {
+                        const float2 f = unpack_f32x2(acc[j / 2 + i]);
+                        __nv_bfloat162 h = __floats2bfloat162_rn(f.x, f.y);
+                        w[i] = *reinterpret_cast<uint32_t*>(&h);
+                    }
+                    *reinterpret_cast<uint4*>(y + j) = make_uint4(w[0], w[1], w[2], w[3]);
+                }
+            }
+        } else {
+            float* y = reinterpret_cast<float*>(p.y) + row * p.ldy + col0;
+#pragma unroll
+            for (int j = 0; j < 128; j += 4) {
+                if (col0 + j < p.N) {
+                    const float2 a = unpack_f32x2(acc[j / 2]), b = unpack_f32x2(acc[j / 2 + 1]);
+                    *reinterpret_cast<float4*>(y + j) = make_float4(a.x, a.y, b.x, b.y);
+                }
+            }
+        }
+    }
+}
 
 template <bool A_MN, bool B_MN>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
@@ -411,75 +499,262 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 }
             }
             if (!ok) break;
-            // ---- store: TMA bulk stores of 32 x 64-byte slabs when this warp's
-            // 32 rows all belong to the tile's group (TMA clips only at the
-            // tensor edge), otherwise masked direct stores
-            const int64_t wrow0 = static_cast<int64_t>(tl.row0) + quarter * 32;
-            if (p.tma_store && (p.offsets == nullptr || wrow0 + 32 <= tl.row_end)) {
-                const uint32_t slab = sbase + OUT_OFF + (warp - EPI_WARP0) * OUT_SLAB;
-                const uint32_t rbase = slab + lane * 64;
-                const uint32_t sw = (lane >> 1) & 3;          // 64-B swizzle: chunk ^= (row/2)%4
-                const int passes = p.out_bf16 ? 4 : 8;        // 32 bf16 or 16 fp32 columns each
-#pragma unroll
-                for (int ps = 0; ps < 8; ps++) {
-                    if (ps >= passes) break;
-                    if (lane == 0) bulk_wait_group_read0();   // slab free again
-                    __syncwarp();
-#pragma unroll
-                    for (int c = 0; c < 4; c++) {
-                        uint32_t w[4];
-                        if (p.out_bf16) {
-#pragma unroll
-                            for (int i = 0; i < 4; i++) {
-                                const float2 f = unpack_f32x2(acc[ps * 16 + c * 4 + i]);
-                                __nv_bfloat162 h = __floats2bfloat162_rn(f.x, f.y);
-                                w[i] = *reinterpret_cast<uint32_t*>(&h);
-                            }
-                        } else {
-                            const float2 a = unpack_f32x2(acc[ps * 8 + c * 2]);
-                            const float2 b = unpack_f32x2(acc[ps * 8 + c * 2 + 1]);
-                            w[0] = __float_as_uint(a.x); w[1] = __float_as_uint(a.y);
-                            w[2] = __float_as_uint(b.x); w[3] = __float_as_uint(b.y);
-                        }
-                        st_shared_v4(rbase + ((c ^ sw) << 4), w[0], w[1], w[2], w[3]);
-                    }
-                    fence_proxy_async_smem();
-                    __syncwarp();
-                    if (lane == 0) {
-                        tma_store_2d(&tmY, slab, static_cast<int32_t>(col0 + ps * (p.out_bf16 ? 32 : 16)),
-                                     static_cast<int32_t>(wrow0));
-                        bulk_commit_group();
-                    }
+            store_tile(p, tmY, acc, tl, row, row_ok, col0, quarter, lane,
+                       sbase + OUT_OFF + (warp - EPI_WARP0) * OUT_SLAB);
+        }
+        if (lane == 0) bulk_wait_group0();   // every store of this warp has landed
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem_base, TMEM_COLS);
+    }
+}
+
+
+// ====================================================================== MX
+// Power-of-two block scales applied by the tensor core: kind::mxf8f6f4 with
+// UE8M0 scale factors in TMEM, so the whole K accumulates in TMEM with no
+// promotion (the "block scaling accelerated by hardware" of Blackwell).
+// Warp 0 loads each K block's operand tiles and (1x128 A scales) A's 128
+// fp32 row scales by TMA; warp 2 waits for the stage to land and writes its
+// UE8M0 words into the stage's scale area (B's two per-block scales come
+// from a register ring), off the MMA's critical path; warp 1 copies them
+// into a 4-slot TMEM ring with tcgen05.cp (ordered with its MMAs) and issues
+// the block-scaled MMAs.  A's
+// scale of row m sits at TMEM (lane m, column m/32) of its slot (the 128x128b
+// copy fills all four columns of each lane); B's scale of column n sits at
+// (lane 32*quarter + n%32, column 4 + n/32), one copy per lane quarter (the
+// 32x128b.warpx4 copy).  One 256-column accumulator; the epilogue loads it,
+// releases it and stores.
+// per stage: A's raw fp32 scales (512 B, by TMA) at 0, SFA words 128x16 B at
+// 512, SFB words 2 x 32x16 B at 2560 and 3072
+constexpr uint32_t MX_SF_STAGE = 3584;
+constexpr uint32_t MX_SF_OFF = STAGES * STAGE_BYTES;
+constexpr uint32_t MX_BAR_OFF = MX_SF_OFF + STAGES * MX_SF_STAGE;
+constexpr int MX_NUM_BARS = 3 * STAGES + 2 + 1;        // full, empty, sfready, tfull, tempty, done
+constexpr uint32_t MX_TMEMSLOT_OFF = MX_BAR_OFF + MX_NUM_BARS * 8;
+constexpr uint32_t MX_TABLE_OFF = (MX_TMEMSLOT_OFF + 16 + 15) & ~15u;
+constexpr uint32_t MX_OUT_OFF = (MX_TABLE_OFF + 16 + 1023) & ~1023u;
+constexpr uint32_t MX_SMEM_BYTES = 1024 + MX_OUT_OFF + NUM_EPI_WARPS * OUT_SLAB;
+static_assert(MX_SMEM_BYTES <= 232448, "shared memory budget (MX)");
+constexpr uint32_t MX_SF_TMEM = 256;                   // scale-factor ring after the accumulator
+constexpr int MX_SF_SLOTS = 4;                         // 16 columns each: SFA 4 + SFB 8
+#ifndef FP8BS_MPF
+#define FP8BS_MPF 8
+#endif
+constexpr int MPF = FP8BS_MPF;                         // producer scale prefetch (K blocks)
+constexpr int MX_REGS_LOW = 88, MX_REGS_HIGH = 208;   // 128*88 + 256*208 == 384*168
+
+// UE8M0 code of a power-of-two fp32 scale (its exponent field), in all 4 bytes
+__device__ __forceinline__ uint32_t ue8m0_word(float s) {
+    return ((__float_as_uint(s) >> 23) & 0xFFu) * 0x01010101u;
+}
+
+template <int UNUSED>
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+    k_fp8_gemm_mx(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                  const __grid_constant__ CUtensorMap tmY, const __grid_constant__ CUtensorMap tmSA,
+                  const GemmParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    uint8_t* smem = smem_raw + ((1024u - (raw & 1023u)) & 1023u);
+    const uint32_t sbase = smem_u32(smem);
+    const uint32_t sA = sbase, sB = sbase + STAGES * A_STAGE, sSF = sbase + MX_SF_OFF;
+    const uint32_t bars = sbase + MX_BAR_OFF;
+    auto full_bar = [&](int s) { return bars + 8u * s; };
+    auto empty_bar = [&](int s) { return bars + 8u * (STAGES + s); };
+    auto sfready_bar = [&](int s) { return bars + 8u * (2 * STAGES + s); };
+    const uint32_t tfull_bar = bars + 8u * (3 * STAGES);
+    const uint32_t tempty_bar = bars + 8u * (3 * STAGES + 1);
+    const uint32_t done_bar = bars + 8u * (3 * STAGES + 2);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + MX_TMEMSLOT_OFF);
+    int* s_off = reinterpret_cast<int*>(smem + MX_TABLE_OFF);
+    int* s_slot = s_off + 2;
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+
+    if (warp == 0 && lane == 0) {
+        tma_prefetch_desc(&tmA);
+        tma_prefetch_desc(&tmB);
+        for (int s = 0; s < STAGES; s++) {
+            mbar_init(full_bar(s), 1);
+            mbar_init(empty_bar(s), 1);
+            mbar_init(sfready_bar(s), 1);
+        }
+        mbar_init(tfull_bar, 1);
+        mbar_init(tempty_bar, NUM_EPI_WARPS);
+        mbar_init(done_bar, 1);
+        fence_mbar_init();
+        fence_proxy_async_smem();
+        s_off[0] = 0;
+        s_off[1] = static_cast<int>(p.M);
+        s_slot[0] = 0;
+        s_slot[1] = static_cast<int>((p.M + BM - 1) / BM);
+    }
+    if (warp == 1) tmem_alloc(smem_u32(tmem_slot), TMEM_COLS);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+    const int total_slots = s_slot[1];
+    const int total_tiles = total_slots * p.tiles_n;
+    const int nkb = static_cast<int>(p.K / BK);
+    const int64_t nkb64 = nkb;
+    const int64_t nrbB = (p.N + 127) / 128;
+
+    const bool sa_tma = p.a_gran == 0;                 // A's 1x128 scales arrive by TMA
+
+    if (warp < EPI_WARP0) {
+      asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(MX_REGS_LOW));
+      if (warp == 0) {
+        // -------------------------------- producer: operand tiles + A's scale vector
+        if (lane == 0) {
+            if (sa_tma) tma_prefetch_desc(&tmSA);
+            const uint32_t bytes = STAGE_BYTES + (sa_tma ? 512u : 0u);
+            int stage = 0;
+            uint32_t phase = 0;
+            bool ok = true;
+            int issued = 0;
+            for (int t = blockIdx.x; ok && t < total_tiles; t += gridDim.x) {
+                const Tile tl = decode_tile(t, total_slots, p.tiles_n, 1, s_slot, s_off);
+                for (int kb = 0; kb < nkb; kb++) {
+                    if (!wait_or_flag(empty_bar(stage), phase ^ 1u)) { ok = false; break; }
+                    mbar_arrive_expect_tx(full_bar(stage), bytes);
+                    tma_load_2d(sA + stage * A_STAGE, &tmA, kb * BK, tl.row0, full_bar(stage));
+                    tma_load_2d(sB + stage * B_STAGE, &tmB, kb * BK, tl.nt * BN, full_bar(stage));
+                    if (sa_tma)   // 128 fp32 row scales of this K block (rows contiguous)
+                        tma_load_2d(sSF + stage * MX_SF_STAGE, &tmSA, tl.row0, kb, full_bar(stage));
+                    issued++;
+                    if (++stage == STAGES) { stage = 0; phase ^= 1u; }
                 }
-            } else if (row_ok) {
-                if (p.out_bf16) {
-                    uint16_t* y = reinterpret_cast<uint16_t*>(p.y) + row * p.ldy + col0;
-#pragma unroll
-                    for (int j = 0; j < 128; j += 8) {
-                        if (col0 + j < p.N) {
-                            uint32_t w[4];
-#pragma unroll
-                            for (int i = 0; i < 4; i++) {
-                                const float2 f = unpack_f32x2(acc[j / 2 + i]);
-                                __nv_bfloat162 h = __floats2bfloat162_rn(f.x, f.y);
-                                w[i] = *reinterpret_cast<uint32_t*>(&h);
-                            }
-                            *reinterpret_cast<uint4*>(y + j) = make_uint4(w[0], w[1], w[2], w[3]);
-                        }
-                    }
-                } else {
-                    float* y = reinterpret_cast<float*>(p.y) + row * p.ldy + col0;
-#pragma unroll
-                    for (int j = 0; j < 128; j += 4) {
-                        if (col0 + j < p.N) {
-                            const float2 a = unpack_f32x2(acc[j / 2]), b = unpack_f32x2(acc[j / 2 + 1]);
-                            *reinterpret_cast<float4*>(y + j) = make_float4(a.x, a.y, b.x, b.y);
-                        }
-                    }
+            }
+            if (!ok) {
+                for (int i = 0; i < STAGES && i < issued; i++) {
+                    if (--stage < 0) { stage = STAGES - 1; phase ^= 1u; }
+                    wait_bounded(full_bar(stage), phase, DRAIN_LIMIT_NS);
                 }
             }
         }
-        if (lane == 0) bulk_wait_group0();   // every store of this warp has landed
+      } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA
+        if (lane == 0) {
+            int stage = 0;
+            uint32_t phase = 0, tile_i = 0, kbg = 0;
+            bool ok = true, issued_mma = false;
+            for (int t = blockIdx.x; ok && t < total_tiles; t += gridDim.x, tile_i++) {
+                if (!wait_or_flag(tempty_bar, (tile_i & 1u) ^ 1u)) { ok = false; break; }
+                for (int kb = 0; kb < nkb; kb++, kbg++) {
+                    // scale words written (the converter saw the stage's TMA land)
+                    if (!wait_or_flag(sfready_bar(stage), phase)) { ok = false; break; }
+                    tc_fence_after();
+                    const uint32_t sf = sSF + stage * MX_SF_STAGE;
+                    const uint32_t tsfa = tmem_base + MX_SF_TMEM + (kbg % MX_SF_SLOTS) * 16;
+                    const uint32_t tsfb = tsfa + 4;
+                    tmem_cp_128x128b(tsfa, smem_desc_rows16(sf + 512));
+                    tmem_cp_32x128b_warpx4(tsfb, smem_desc_rows16(sf + 2560));
+                    tmem_cp_32x128b_warpx4(tsfb + 4, smem_desc_rows16(sf + 3072));
+                    const uint32_t aS = sA + stage * A_STAGE, bS = sB + stage * B_STAGE;
+#pragma unroll
+                    for (int k4 = 0; k4 < BK / 32; k4++)
+                        mma_mxf8f6f4(tmem_base, smem_desc_sw128(aS + k4 * 32, 16, 1024),
+                                     smem_desc_sw128(bS + k4 * 32, 16, 1024), p.idesc, tsfa, tsfb,
+                                     (kb > 0 || k4 > 0) ? 1u : 0u);
+                    issued_mma = true;
+                    mma_commit(empty_bar(stage));
+                    if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+                }
+                if (!ok) break;
+                mma_commit(tfull_bar);
+            }
+            if (!ok && issued_mma) {
+                mma_commit(done_bar);
+                wait_bounded(done_bar, 0, DRAIN_LIMIT_NS);
+            }
+        }
+      } else if (warp == 2) {
+        // ---------------- scale converter: UE8M0 words of each landed stage
+        int stage = 0;
+        uint32_t phase = 0;
+        bool ok = true;
+        for (int t = blockIdx.x; ok && t < total_tiles; t += gridDim.x) {
+            const Tile tl = decode_tile(t, total_slots, p.tiles_n, 1, s_slot, s_off);
+            const int64_t nb0 = min(static_cast<int64_t>(2 * tl.nt), nrbB - 1);
+            const int64_t nb1 = min(static_cast<int64_t>(2 * tl.nt + 1), nrbB - 1);
+            const int64_t arow = min(static_cast<int64_t>(tl.row0), p.a_rows - 1);
+            // lane-uniform scale values of K block kb in register slot kb % MPF
+            float ru[MPF], rb0[MPF], rb1[MPF];
+            auto load_sf = [&](int kb, float& u, float& b0, float& b1) {
+                u = p.a_gran == 1 ? ld_scale(p.sa + (arow / 128) * nkb64 + kb)
+                                  : (p.a_gran == 2 ? ld_scale(p.sa) : 0.0f);
+                b0 = p.b_gran == 1 ? ld_scale(p.sb + nb0 * nkb64 + kb) : ld_scale(p.sb);
+                b1 = p.b_gran == 1 ? ld_scale(p.sb + nb1 * nkb64 + kb) : ld_scale(p.sb);
+            };
+#pragma unroll
+            for (int i = 0; i < MPF; i++) load_sf(min(i, nkb - 1), ru[i], rb0[i], rb1[i]);
+            for (int kb0 = 0; ok && kb0 < nkb; kb0 += MPF) {
+#pragma unroll
+                for (int i = 0; i < MPF; i++) {
+                    const int kb = kb0 + i;
+                    if (kb >= nkb) break;
+                    ok = __all_sync(0xFFFFFFFFu, wait_or_flag(full_bar(stage), phase));
+                    if (!ok) break;
+                    const uint32_t sf = sSF + stage * MX_SF_STAGE;
+#pragma unroll
+                    for (int r = 0; r < 4; r++) {
+                        const float v = sa_tma ? ld_shared_f32(sf + (32 * r + lane) * 4) : ru[i];
+                        const uint32_t w = ue8m0_word(v);
+                        st_shared_v4(sf + 512 + (32 * r + lane) * 16, w, w, w, w);
+                    }
+                    const uint32_t w0 = ue8m0_word(rb0[i]), w1 = ue8m0_word(rb1[i]);
+                    st_shared_v4(sf + 2560 + lane * 16, w0, w0, w0, w0);
+                    st_shared_v4(sf + 3072 + lane * 16, w1, w1, w1, w1);
+                    if (kb + MPF < nkb) load_sf(kb + MPF, ru[i], rb0[i], rb1[i]);
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(sfready_bar(stage));
+                    if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+                }
+            }
+        }
+      }
+    } else {
+        asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(MX_REGS_HIGH));
+        // ----------------------------------------------------- epilogue
+        const int quarter = warp & 3;
+        const int half = (warp - EPI_WARP0) >> 2;
+        uint32_t tile_i = 0;
+        bool ok = true;
+        for (int t = blockIdx.x; ok && t < total_tiles; t += gridDim.x, tile_i++) {
+            const Tile tl = decode_tile(t, total_slots, p.tiles_n, 1, s_slot, s_off);
+            const int64_t row = static_cast<int64_t>(tl.row0) + quarter * 32 + lane;
+            const bool row_ok = row < tl.row_end;
+            const int64_t col0 = static_cast<int64_t>(tl.nt) * BN + half * 128;
+            ok = __all_sync(0xFFFFFFFFu, wait_or_flag_sleepy(tfull_bar, tile_i & 1u));
+            if (!ok) break;
+            tc_fence_after();
+            const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + half * 128;
+            uint64_t acc[64];
+#pragma unroll
+            for (int j = 0; j < 4; j += 2) {
+                uint32_t r[2][32];
+                tmem_ld_32x32b_x32(taddr + j * 32, r[0]);
+                tmem_ld_32x32b_x32(taddr + (j + 1) * 32, r[1]);
+                tmem_wait_ld();
+#pragma unroll
+                for (int u = 0; u < 2; u++)
+#pragma unroll
+                    for (int i = 0; i < 16; i++) acc[(j + u) * 16 + i] = pack_f32x2(r[u][2 * i], r[u][2 * i + 1]);
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(tempty_bar);       // accumulator free for the next tile
+            store_tile(p, tmY, acc, tl, row, row_ok, col0, quarter, lane,
+                       sbase + MX_OUT_OFF + (warp - EPI_WARP0) * OUT_SLAB);
+        }
+        if (lane == 0) bulk_wait_group0();
     }
 
     tc_fence_before();
@@ -527,6 +802,29 @@ uint32_t make_idesc_f8f6f4(int a_fmt, int b_fmt, bool a_mn, bool b_mn, int n) {
     d |= static_cast<uint32_t>(n >> 3) << 17;
     d |= static_cast<uint32_t>(BM >> 4) << 24;
     return d;
+}
+
+// kind::mxf8f6f4 (block-scaled) instruction descriptor: B / A scale-factor
+// byte ids at bits 4-5 / 29-30 (0: the four bytes of a scale word are equal
+// here), A/B formats at 7-9 / 10-12, N >> 3 at 17-22, scale type UE8M0 at
+// bit 23, M >> 4 at 24-28; the accumulator is always fp32.
+uint32_t make_idesc_mx(int a_fmt, int b_fmt, int n) {
+    uint32_t d = 0;
+    d |= static_cast<uint32_t>(a_fmt & 7) << 7;
+    d |= static_cast<uint32_t>(b_fmt & 7) << 10;
+    d |= static_cast<uint32_t>(n >> 3) << 17;
+    d |= 1u << 23;
+    d |= static_cast<uint32_t>(BM >> 4) << 24;
+    return d;
+}
+
+cudaError_t launch_fp8_gemm_mx(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmY,
+                               const CUtensorMap& tmSA, const GemmParams& p, int grid, cudaStream_t st) {
+    auto k = k_fp8_gemm_mx<0>;
+    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, MX_SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    k<<<grid, NUM_THREADS, MX_SMEM_BYTES, st>>>(tmA, tmB, tmY, tmSA, p);
+    return cudaGetLastError();
 }
 
 int gemm_tile_n() { return BN; }

@@ -38,6 +38,9 @@ int gemm_mma_n();   // N of one tcgen05.mma (a K-major B); an MN-major B always 
 int gemm_tile_m();
 cudaError_t launch_fp8_gemm(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmY,
                             const GemmParams& p, bool a_mn, bool b_mn, int grid, cudaStream_t st);
+uint32_t make_idesc_mx(int a_fmt, int b_fmt, int n);
+cudaError_t launch_fp8_gemm_mx(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmY,
+                               const CUtensorMap& tmSA, const GemmParams& p, int grid, cudaStream_t st);
 cudaError_t read_and_clear_status(int* status);
 cudaError_t launch_wait_selftest(uint64_t limit_ns, int* out, cudaStream_t st);
 

@@ -84,19 +84,23 @@ def test_ragged_shapes(M, N, K, mode):
                                            (orc.GRAN_TENSOR, orc.GRAN_128x128),
                                            (orc.GRAN_1x128, orc.GRAN_TENSOR),
                                            (orc.GRAN_TENSOR, orc.GRAN_TENSOR)])
-def test_granularities(a_gran, b_gran):
+@pytest.mark.parametrize("mode", [orc.SCALE_FP32, orc.SCALE_POW2])
+def test_granularities(a_gran, b_gran, mode):
+    """fp32 scales: promotion kernel; pow2 scales: block-scaled (MX) kernel."""
     M, N, K = 200, 512, 1024
-    A_o, B_o, A_d, B_d = _case(M, N, K, a_gran, b_gran, seed=7)
+    A_o, B_o, A_d, B_d = _case(M, N, K, a_gran, b_gran, mode=mode, seed=7)
     y_ref, yabs = orc.gemm(M, N, K, A_o, B_o)
-    _check(fp8.fp8_block_gemm(A_d, B_d, M, N, K, fp8.OUT_F32), y_ref, yabs, fp8.OUT_F32)
+    _check(fp8.fp8_block_gemm(A_d, B_d, M, N, K, fp8.OUT_F32, mode), y_ref, yabs, fp8.OUT_F32)
 
 
 @pytest.mark.parametrize("fa,fb", [(orc.E5M2, orc.E4M3), (orc.E4M3, orc.E5M2), (orc.E5M2, orc.E5M2)])
-def test_mixed_formats(fa, fb):
+@pytest.mark.parametrize("mode", [orc.SCALE_FP32, orc.SCALE_POW2])
+def test_mixed_formats(fa, fb, mode):
     M, N, K = 256, 256, 768
-    A_o, B_o, A_d, B_d = _case(M, N, K, orc.GRAN_1x128, orc.GRAN_128x128, fa=fa, fb=fb, seed=11)
+    A_o, B_o, A_d, B_d = _case(M, N, K, orc.GRAN_1x128, orc.GRAN_128x128, fa=fa, fb=fb, mode=mode,
+                               seed=11)
     y_ref, yabs = orc.gemm(M, N, K, A_o, B_o)
-    _check(fp8.fp8_block_gemm(A_d, B_d, M, N, K, fp8.OUT_F32), y_ref, yabs, fp8.OUT_F32)
+    _check(fp8.fp8_block_gemm(A_d, B_d, M, N, K, fp8.OUT_F32, mode), y_ref, yabs, fp8.OUT_F32)
 
 
 @pytest.mark.parametrize("a_t,b_t,a_gran,b_gran", [
@@ -166,8 +170,48 @@ def test_back_to_back_calls_and_side_stream():
     fp8.device_status()
 
 
+def test_pow2_scale_extremes_mx():
+    """Block-scaled (MX) path with scales spread over a wide exponent range,
+    per-row and per-block (tiny and huge blocks side by side)."""
+    M, N, K = 256, 512, 512
+    rng = np.random.default_rng(21)
+    a = inputs.bits_to_f32(inputs.activations(M, K, seed=21))
+    a *= (2.0 ** rng.integers(-40, 40, size=(M, 1))).astype(np.float32)
+    b = inputs.bits_to_f32(inputs.gaussian((N, K), 0.02, seed=22))
+    b *= (2.0 ** rng.integers(-30, 30, size=(N // 128, 1))).repeat(128, axis=0).astype(np.float32)
+    qa, sa = orc.quantize_1x128(inputs.bf16_bits(a), orc.E4M3, orc.SCALE_POW2)
+    qb, sb = orc.quantize_128x128(inputs.bf16_bits(b), orc.E4M3, orc.SCALE_POW2)
+    y_ref, yabs = orc.gemm(M, N, K, orc.operand(qa, orc.E4M3, orc.GRAN_1x128, sa),
+                           orc.operand(qb, orc.E4M3, orc.GRAN_128x128, sb))
+    y = fp8.fp8_block_gemm(fp8.operand(dev(qa), dev(sa)), fp8.operand(dev(qb), dev(sb), gran=fp8.GRAN_128x128),
+                           M, N, K, fp8.OUT_F32, fp8.SCALE_POW2)
+    _check(y, y_ref, yabs, fp8.OUT_F32)
+
+
 # ------------------------------------------------------------ full sizes
 LLAMA8B = [("qkv", 6144, 4096), ("o", 4096, 4096), ("gate_up", 28672, 4096), ("down", 4096, 14336)]
+
+
+LLAMA2 = [("qkv", 12288, 4096), ("down", 4096, 11008)]
+
+
+@pytest.mark.parametrize("name,N,K", LLAMA2)
+def test_llama2_7b_pow2_linears_sampled(name, N, K):
+    """Llama-2-7B-shaped linears (M=4096) with power-of-two scales: the
+    block-scaled (MX) kernel at full size, sampled outputs."""
+    M = 4096
+    x = inputs.activations(M, K, seed=3000 + K)
+    w = inputs.gaussian((N, K), 0.02, seed=4000 + N)
+    qa, sa = orc.quantize_1x128(x, orc.E4M3, orc.SCALE_POW2)
+    qb, sb = orc.quantize_128x128(w, orc.E4M3, orc.SCALE_POW2)
+    rng = np.random.default_rng(N)
+    rows, cols = stratified(M, 128, rng), stratified(N, 256, rng, extra=(N - 8,))
+    y_ref, yabs = orc.gemm(M, N, K, orc.operand(qa, orc.E4M3, orc.GRAN_1x128, sa),
+                           orc.operand(qb, orc.E4M3, orc.GRAN_128x128, sb), rows=rows, cols=cols)
+    A_d = fp8.operand(dev(qa), dev(sa))
+    B_d = fp8.operand(dev(qb), dev(sb), gran=fp8.GRAN_128x128)
+    for out in (fp8.OUT_BF16, fp8.OUT_F32):
+        _check(fp8.fp8_block_gemm(A_d, B_d, M, N, K, out, fp8.SCALE_POW2), y_ref, yabs, out, rows, cols)
 
 
 @pytest.mark.parametrize("name,N,K", LLAMA8B)

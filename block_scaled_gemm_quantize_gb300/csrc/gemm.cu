@@ -111,21 +111,6 @@ __device__ __forceinline__ bool wait_or_flag(uint32_t bar, uint32_t parity) {
     return false;
 }
 
-// Bounded wait for a rare event (once per tile): backs off with nanosleep so
-// the waiting warps leave the issue slots to the producer and MMA warps.
-__device__ __forceinline__ bool wait_or_flag_sleepy(uint32_t bar, uint32_t parity) {
-    if (mbar_try_wait(bar, parity)) return true;
-    const uint64_t t0 = global_timer_ns();
-    while (true) {
-        __nanosleep(256);
-        if (mbar_try_wait(bar, parity)) return true;
-        if (global_timer_ns() - t0 > WAIT_LIMIT_NS) {
-            atomicExch(&g_status, kStatusDeviceTimeout);
-            return false;
-        }
-    }
-}
-
 struct Tile {
     int g, row0, row_end, nt;
 };
@@ -732,7 +717,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             const int64_t row = static_cast<int64_t>(tl.row0) + quarter * 32 + lane;
             const bool row_ok = row < tl.row_end;
             const int64_t col0 = static_cast<int64_t>(tl.nt) * BN + half * 128;
-            ok = __all_sync(0xFFFFFFFFu, wait_or_flag_sleepy(tfull_bar, tile_i & 1u));
+            ok = __all_sync(0xFFFFFFFFu, wait_or_flag(tfull_bar, tile_i & 1u));
             if (!ok) break;
             tc_fence_after();
             const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + half * 128;

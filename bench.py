@@ -38,6 +38,10 @@ sys.path.insert(0, ROOT)
 from block_scaled_gemm_quantize_gb300 import inputs as W_  # noqa: E402
 
 METRIC = "block-scaled FP8 linear TFLOPS (quant+GEMM) and % of GB300 dense FP8 peak"
+# DRAM read+write bytes per GEMM launch of the default workload, from one ncu capture of the
+# current kernel (profiles/k_fp8_gemm_llama31_8b_gate_up.md); None for other workloads.
+GEMM_TRAFFIC_BYTES = {"llama3.1-8b-fprop": {"qkv": 134.3e6, "o": 81.0e6, "gate_up": 936.8e6,
+                                            "down": 516.8e6}}
 FP8_OVER_BF16 = 2.0      # nominal dense fp8 / bf16 tensor ratio (4.5 / 2.25 PFLOP/s)
 
 
@@ -473,6 +477,9 @@ def run_ours(args):
     quant_ms = sum(v for k, v in tot.items() if k.startswith("quant:"))
     qbytes = getattr(wl, "quant_bytes", None) or sum(u[2] for u in wl.units)
     achieved = gemm_flops / gemm_ms / 1e9
+    tr = GEMM_TRAFFIC_BYTES.get(args.workload)
+    traffic = (sum(tr[u[0]] for u in wl.units) / len(wl.units)
+               if tr and all(u[0] in tr for u in wl.units) else None)
     fp8_peak = FP8_OVER_BF16 * peaks["bf16_sustained"]
     quant_gbs = qbytes / quant_ms / 1e6 if quant_ms else None
 
@@ -529,7 +536,7 @@ def run_ours(args):
         "pct_of_fp8_peak": 100.0 * value / fp8_peak,
         "roofline": {"bound": "tensor", "kernel": "k_fp8_gemm", "achieved": achieved,
                      "peak": fp8_peak, "unit": "TFLOP/s", "frac": achieved / fp8_peak,
-                     "traffic": None,
+                     "traffic": traffic, "traffic_unit": "bytes per launch (mean, ncu)",
                      "peak_src": f"{peaks['src']}: 2 x bf16_tflops_sustained "
                                  f"({peaks['bf16_sustained']})"},
         "quant_roofline": {"bound": "hbm", "achieved": quant_gbs, "peak": peaks["hbm_gbs"],

@@ -9,8 +9,13 @@ bf16 out).  One step = for each linear: quantize X (1x128), re-quantize W
 (128x128, the weights change every optimizer step), GEMM -> Y.
 
 Other workloads (--workload): llama2-7b-fprop (pow2 scales, M=4096),
+llama3.1-8b-fprop-mxfp8 (the same linears in MXFP8: 1x32 blocks, E8M0 scales),
 llama3.1-8b-mlp-bwd (per-tensor delayed E5M2 dY, dgrad + wgrad on transposed
-operands), qwen3-30b-a3b-moe (grouped expert GEMMs).
+operands), llama3.1-8b-mlp-bwd-blockwise (the same backward under the block
+recipe: row-wise and column-wise transposed 1x128 copies of dY and X),
+qwen3-30b-a3b-moe (grouped expert GEMMs), llama3.1-8b-mlp-fused and
+qwen3-30b-a3b-moe-fused (gate/up product with a SwiGLU + FP8-quantizing
+epilogue feeding the down product directly).
 
 Inputs are synthetic (seeded), resident in HBM; every step streams more than
 the 129 MB L2.
@@ -174,7 +179,8 @@ class Fprop:
     def __init__(self, cfg, fp8, device, seed=0, only=None):
         import torch
         self.cfg, self.fp8 = cfg, fp8
-        self.mode = fp8.SCALE_POW2 if cfg["scale_mode"] == "pow2" else fp8.SCALE_FP32
+        self.mx = cfg["scale_mode"] == "mx"
+        self.mode = fp8.SCALE_POW2 if cfg["scale_mode"] in ("pow2", "mx") else fp8.SCALE_FP32
         M = self.M = cfg["M"]
         g = torch.Generator(device=device)
         self.items = []
@@ -186,28 +192,45 @@ class Fprop:
             w = (_randn(g, (N, K), device, 0.02)).to(torch.bfloat16)
             it = dict(name=name, N=N, K=K, x=x, w=w,
                       qx=torch.empty((M, K), dtype=torch.uint8, device=device),
-                      sx=torch.empty((K // 128, M), dtype=torch.float32, device=device),
                       qw=torch.empty((N, K), dtype=torch.uint8, device=device),
-                      sw=torch.empty(((N + 127) // 128, K // 128), dtype=torch.float32, device=device),
                       y=torch.empty((M, N), dtype=torch.bfloat16, device=device))
-            it["A"] = fp8.operand(it["qx"], it["sx"], fp8.E4M3, fp8.GRAN_1x128)
-            it["B"] = fp8.operand(it["qw"], it["sw"], fp8.E4M3, fp8.GRAN_128x128)
+            if self.mx:   # MXFP8: E8M0 codes, one per 32 elements along K, both operands
+                it["sx"] = torch.empty((K // 128, M, 4), dtype=torch.uint8, device=device)
+                it["sw"] = torch.empty((K // 128, N, 4), dtype=torch.uint8, device=device)
+                it["A"] = fp8.operand(it["qx"], it["sx"], fp8.E4M3, fp8.GRAN_1x32)
+                it["B"] = fp8.operand(it["qw"], it["sw"], fp8.E4M3, fp8.GRAN_1x32)
+            else:
+                it["sx"] = torch.empty((K // 128, M), dtype=torch.float32, device=device)
+                it["sw"] = torch.empty(((N + 127) // 128, K // 128), dtype=torch.float32, device=device)
+                it["A"] = fp8.operand(it["qx"], it["sx"], fp8.E4M3, fp8.GRAN_1x128)
+                it["B"] = fp8.operand(it["qw"], it["sw"], fp8.E4M3, fp8.GRAN_128x128)
             self.items.append(it)
-        self.units = [(it["name"], 2.0 * M * it["N"] * it["K"],
-                       M * it["K"] * 3 + 4 * M * (it["K"] // 128) + it["N"] * it["K"] * 3
-                       + 4 * ((it["N"] + 127) // 128) * (it["K"] // 128)) for it in self.items]
+        if self.mx:
+            self.units = [(it["name"], 2.0 * M * it["N"] * it["K"],
+                           (M + it["N"]) * it["K"] * 3 + (M + it["N"]) * (it["K"] // 32))
+                          for it in self.items]
+        else:
+            self.units = [(it["name"], 2.0 * M * it["N"] * it["K"],
+                           M * it["K"] * 3 + 4 * M * (it["K"] // 128) + it["N"] * it["K"] * 3
+                           + 4 * ((it["N"] + 127) // 128) * (it["K"] // 128)) for it in self.items]
         self.flops = sum(u[1] for u in self.units)
         self.launches = 3 * len(self.items)
         self.config = {"workload": cfg["name"] + (f" ({only} only)" if only else ""), "M": M,
                        "linears": [[it["name"], it["N"], it["K"]] for it in self.items],
-                       "scales": f"{cfg['scale_mode']} 1x128 (X) / 128x128 (W)", "out": "bf16"}
+                       "scales": ("MXFP8: E8M0 per 1x32 (X and W)" if self.mx
+                                  else f"{cfg['scale_mode']} 1x128 (X) / 128x128 (W)"), "out": "bf16"}
 
     def step(self, rec=None):
         fp8, M, mode = self.fp8, self.M, self.mode
         for it in self.items:
-            _run(rec, "quant:" + it["name"], lambda it=it: (
-                fp8.fp8_quantize_1x128(it["x"], fp8.E4M3, mode, q=it["qx"], scales=it["sx"]),
-                fp8.fp8_quantize_128x128(it["w"], fp8.E4M3, mode, q=it["qw"], scales=it["sw"])))
+            if self.mx:
+                _run(rec, "quant:" + it["name"], lambda it=it: (
+                    fp8.fp8_quantize_mx(it["x"], fp8.E4M3, q=it["qx"], scales=it["sx"]),
+                    fp8.fp8_quantize_mx(it["w"], fp8.E4M3, q=it["qw"], scales=it["sw"])))
+            else:
+                _run(rec, "quant:" + it["name"], lambda it=it: (
+                    fp8.fp8_quantize_1x128(it["x"], fp8.E4M3, mode, q=it["qx"], scales=it["sx"]),
+                    fp8.fp8_quantize_128x128(it["w"], fp8.E4M3, mode, q=it["qw"], scales=it["sw"])))
             _run(rec, "gemm:" + it["name"], lambda it=it: fp8.fp8_block_gemm(
                 it["A"], it["B"], M, it["N"], it["K"], fp8.OUT_BF16, mode, y=it["y"]))
 
@@ -285,6 +308,79 @@ class MlpBwd:
         return [it["dy"] for it in self.items], [it["dx"] for it in self.items] + [it["dw"] for it in self.items]
 
 
+class MlpBwdBlock:
+    """Backward of the Llama-3.1-8B MLP under the block recipe: per linear,
+    dY is quantized once into its row-wise 1x128 copy (dgrad operand) and its
+    column-wise transposed copy (wgrad operand) from a single read, X into
+    its column-wise transposed copy; dgrad dX = dY W (W 128x128, stored
+    transposed for the product, bf16 out) and wgrad dW = dY^T X (both 1x128
+    along the tokens, fp32 out).  E4M3 throughout."""
+
+    def __init__(self, cfg, fp8, device, seed=0, only=None):
+        import torch
+        self.fp8, self.M = fp8, cfg["M"]
+        self.mode = fp8.SCALE_POW2 if cfg["scale_mode"] == "pow2" else fp8.SCALE_FP32
+        M = self.M
+        g = torch.Generator(device=device)
+        self.items = []
+        u8, f32 = torch.uint8, torch.float32
+        for i, (name, n_out, k_in) in enumerate(cfg["linears"]):
+            if only and name != only:
+                continue
+            g.manual_seed(seed * 1000 + 300 + i)
+            z = _randn(g, (M, n_out), device)
+            chi = sum(_randn(g, (M, n_out), device) ** 2 for _ in range(int(cfg["dy_nu"])))
+            dy = (z / torch.sqrt(chi / cfg["dy_nu"]) * cfg["dy_scale"]).to(torch.bfloat16)
+            del z, chi
+            x = _activations(g, M, k_in, device)
+            w = _randn(g, (n_out, k_in), device, 0.02).to(torch.bfloat16)
+            qw, sw = fp8.fp8_quantize_128x128(w, fp8.E4M3, self.mode)   # as the forward leaves it
+            it = dict(name=name, n_out=n_out, k_in=k_in, dy=dy, x=x, qw=qw, sw=sw,
+                      qdy=torch.empty((M, n_out), dtype=u8, device=device),
+                      sdy=torch.empty((n_out // 128, M), dtype=f32, device=device),
+                      qdyt=torch.empty((n_out, M), dtype=u8, device=device),
+                      sdyt=torch.empty((M // 128, n_out), dtype=f32, device=device),
+                      qxt=torch.empty((k_in, M), dtype=u8, device=device),
+                      sxt=torch.empty((M // 128, k_in), dtype=f32, device=device),
+                      dx=torch.empty((M, k_in), dtype=torch.bfloat16, device=device),
+                      dw=torch.empty((n_out, k_in), dtype=f32, device=device))
+            E4 = fp8.E4M3
+            it["A_dg"] = fp8.operand(it["qdy"], it["sdy"], E4, fp8.GRAN_1x128)                 # [M][n_out]
+            it["B_dg"] = fp8.operand(qw, sw, E4, fp8.GRAN_128x128, transposed=True)            # W^T
+            it["A_wg"] = fp8.operand(it["qdyt"], it["sdyt"], E4, fp8.GRAN_1x128)               # dY^T
+            it["B_wg"] = fp8.operand(it["qxt"], it["sxt"], E4, fp8.GRAN_1x128)                 # X^T
+            self.items.append(it)
+        self.units = []
+        for it in self.items:
+            f = 2.0 * M * it["n_out"] * it["k_in"]
+            qb = (4 * M * it["n_out"] + 8 * M * it["n_out"] // 128) + (3 * M * it["k_in"] + 4 * M * it["k_in"] // 128)
+            self.units += [(it["name"] + ".dgrad", f, qb), (it["name"] + ".wgrad", f, 0)]
+        self.flops = sum(u[1] for u in self.units)
+        self.launches = 4 * len(self.items)     # dY row+col quant, X col quant, dgrad, wgrad
+        self.config = {"workload": cfg["name"] + (f" ({only} only)" if only else ""), "M": M,
+                       "linears": [[it["name"], it["n_out"], it["k_in"]] for it in self.items],
+                       "scales": f"{cfg['scale_mode']} 1x128 (dY row-wise and column-wise, X column-wise) "
+                                 "/ 128x128 (W), E4M3",
+                       "out": "dX bf16, dW fp32"}
+
+    def step(self, rec=None):
+        fp8, M, mode = self.fp8, self.M, self.mode
+        for it in self.items:
+            n = it["name"] + ".dgrad"
+            _run(rec, "quant:" + n, lambda it=it: (
+                fp8.fp8_quantize_1x128_colwise(it["dy"], fp8.E4M3, mode, qt=it["qdyt"], scales_t=it["sdyt"],
+                                               q=it["qdy"], scales=it["sdy"]),
+                fp8.fp8_quantize_1x128_colwise(it["x"], fp8.E4M3, mode, qt=it["qxt"], scales_t=it["sxt"])))
+            _run(rec, "gemm:" + n, lambda it=it: fp8.fp8_block_gemm(
+                it["A_dg"], it["B_dg"], M, it["k_in"], it["n_out"], fp8.OUT_BF16, mode, y=it["dx"]))
+            _run(rec, "gemm:" + it["name"] + ".wgrad", lambda it=it: fp8.fp8_block_gemm(
+                it["A_wg"], it["B_wg"], it["n_out"], it["k_in"], M, fp8.OUT_F32, mode, y=it["dw"]))
+
+    def host_io(self):
+        return ([it["dy"] for it in self.items] + [it["x"] for it in self.items],
+                [it["dx"] for it in self.items] + [it["dw"] for it in self.items])
+
+
 class MoE:
     """Qwen3-30B-A3B-style expert GEMMs: 8192 tokens x top-8 of 128 experts
     (Zipf(1.1) loads), gate+up 2048->1536 and down 768->2048 per expert as two
@@ -337,14 +433,113 @@ class MoE:
         return [it["x"] for it in self.items] + [it["w"] for it in self.items], [it["y"] for it in self.items]
 
 
+class FusedMlp:
+    """An MLP block as two chained FP8 linears whose intermediate stays FP8:
+    quant X (1x128) and re-quant W_gate_up, W_down (128x128); the gate/up
+    product's epilogue applies SwiGLU and quantizes to the down product's
+    1x128 operand (no bf16 intermediate, no separate quantization pass);
+    the down product writes bf16.  Dense (Llama-3.1-8B MLP) or grouped
+    (Qwen3-30B-A3B experts, Zipf(1.1) loads)."""
+
+    def __init__(self, cfg, fp8, device, seed=0, only=None):
+        import torch
+        self.fp8 = fp8
+        self.mode = fp8.SCALE_POW2 if cfg["scale_mode"] == "pow2" else fp8.SCALE_FP32
+        D, I = cfg["hidden"], cfg["intermediate"]
+        g = torch.Generator(device=device)
+        g.manual_seed(seed * 1000 + 700)
+        if "experts" in cfg:
+            loads, off = W_.moe_routing(cfg["tokens"], cfg["experts"], cfg["topk"], cfg["zipf_a"],
+                                        seed=seed)
+            self.off = torch.from_numpy(off).to(device)
+            rows, G = int(off[-1]), cfg["experts"]
+            self.x = _randn(g, (rows, D), device).to(torch.bfloat16)
+            extra = {"rows": rows, "experts": G, "max_rows": int(loads.max()), "min_rows": int(loads.min())}
+        else:
+            self.off = None
+            rows, G = cfg["M"], 1
+            self.x = _activations(g, rows, D, device)
+            extra = {"M": rows}
+        self.rows, self.D, self.I, self.G = rows, D, I, G
+        # per expert: W_gate_up [2I][D] (I gate rows, then I up rows), W_down [D][I]
+        self.w_gu = _randn(g, (G * 2 * I, D), device, 0.02).to(torch.bfloat16)
+        self.w_dn = _randn(g, (G * D, I), device, 0.02).to(torch.bfloat16)
+        u8, f32 = torch.uint8, torch.float32
+        self.qx = torch.empty((rows, D), dtype=u8, device=device)
+        self.sx = torch.empty((D // 128, rows), dtype=f32, device=device)
+        self.qgu = torch.empty((G * 2 * I, D), dtype=u8, device=device)
+        self.sgu = torch.empty((G * 2 * I // 128, D // 128), dtype=f32, device=device)
+        self.qdn = torch.empty((G * D, I), dtype=u8, device=device)
+        self.sdn = torch.empty((G * D // 128, I // 128), dtype=f32, device=device)
+        self.qh = torch.empty((rows, I), dtype=u8, device=device)
+        self.sh = torch.empty((I // 128, rows), dtype=f32, device=device)
+        self.y = torch.empty((rows, D), dtype=torch.bfloat16, device=device)
+        E4 = fp8.E4M3
+        self.A_gu = fp8.operand(self.qx, self.sx, E4, fp8.GRAN_1x128)
+        self.B_gu = fp8.operand(self.qgu, self.sgu, E4, fp8.GRAN_128x128)
+        self.A_dn = fp8.operand(self.qh, self.sh, E4, fp8.GRAN_1x128)
+        self.B_dn = fp8.operand(self.qdn, self.sdn, E4, fp8.GRAN_128x128)
+        self.units = [("gate_up", 2.0 * rows * 2 * I * D,
+                       3 * rows * D + 4 * rows * (D // 128) + 3 * G * 2 * I * D + 4 * G * 2 * I * D // 16384),
+                      ("down", 2.0 * rows * D * I, 3 * G * D * I + 4 * G * D * I // 16384)]
+        self.flops = sum(u[1] for u in self.units)
+        self.launches = 5
+        self.config = {"workload": cfg["name"], **extra, "hidden": D, "intermediate": I,
+                       "linears": [["gate_up+swiglu", 2 * I, D], ["down", D, I]],
+                       "scales": f"{cfg['scale_mode']} 1x128 (X, h) / 128x128 (W)",
+                       "out": "h: e4m3 + 1x128 scales from the gate/up epilogue; y: bf16"}
+
+    def step(self, rec=None):
+        fp8, mode, rows, D, I = self.fp8, self.mode, self.rows, self.D, self.I
+        _run(rec, "quant:gate_up", lambda: (
+            fp8.fp8_quantize_1x128(self.x, fp8.E4M3, mode, q=self.qx, scales=self.sx),
+            fp8.fp8_quantize_128x128(self.w_gu, fp8.E4M3, mode, q=self.qgu, scales=self.sgu)))
+        if self.off is None:
+            _run(rec, "gemm:gate_up", lambda: fp8.fp8_block_gemm_quant(
+                self.A_gu, self.B_gu, rows, 2 * I, D, fp8.EPI_SWIGLU, fp8.E4M3, mode, mode,
+                q=self.qh, q_scales=self.sh))
+        else:
+            _run(rec, "gemm:gate_up", lambda: fp8.fp8_grouped_block_gemm_quant(
+                self.off, self.A_gu, self.B_gu, rows, 2 * I, D, fp8.EPI_SWIGLU, fp8.E4M3, mode, mode,
+                q=self.qh, q_scales=self.sh))
+        _run(rec, "quant:down", lambda: fp8.fp8_quantize_128x128(self.w_dn, fp8.E4M3, mode, q=self.qdn,
+                                                                 scales=self.sdn))
+        if self.off is None:
+            _run(rec, "gemm:down", lambda: fp8.fp8_block_gemm(
+                self.A_dn, self.B_dn, rows, D, I, fp8.OUT_BF16, mode, y=self.y))
+        else:
+            _run(rec, "gemm:down", lambda: fp8.fp8_grouped_block_gemm(
+                self.off, self.A_dn, self.B_dn, rows, D, I, fp8.OUT_BF16, mode, y=self.y))
+
+    def host_io(self):
+        return [self.x, self.w_gu, self.w_dn], [self.y]
+
+
 WORKLOADS = {"llama3.1-8b-fprop": (Fprop, W_.LLAMA31_8B_FPROP),
+             "llama3.1-8b-fprop-mxfp8": (Fprop, W_.LLAMA31_8B_FPROP_MX),
              "llama2-7b-fprop": (Fprop, W_.LLAMA2_7B_FPROP),
              "tiny-fprop": (Fprop, W_.TINY_FPROP),
              "llama3.1-8b-mlp-bwd": (MlpBwd, W_.LLAMA31_8B_MLP_BWD),
-             "qwen3-30b-a3b-moe": (MoE, W_.QWEN3_30B_MOE)}
+             "llama3.1-8b-mlp-bwd-blockwise": (MlpBwdBlock, W_.LLAMA31_8B_MLP_BWD_BLOCK),
+             "qwen3-30b-a3b-moe": (MoE, W_.QWEN3_30B_MOE),
+             "llama3.1-8b-mlp-fused": (FusedMlp, W_.LLAMA31_8B_MLP_FUSED),
+             "qwen3-30b-a3b-moe-fused": (FusedMlp, W_.QWEN3_30B_MOE_FUSED)}
 
 
 # ------------------------------------------------------------ CPU oracle
+def _oracle_linear(orc, x, w, rows, N, K, mode, mx):
+    """Oracle quantization of x and w and the fp64 product of the x rows."""
+    if mx:
+        qw, sw = orc.quantize_mx(w)
+        qx, sx = orc.quantize_mx(x)
+        return orc.gemm(rows, N, K, orc.operand(qx, orc.E4M3, orc.GRAN_1x32, sx),
+                        orc.operand(qw, orc.E4M3, orc.GRAN_1x32, sw))
+    qw, sw = orc.quantize_128x128(w, orc.E4M3, mode)
+    qx, sx = orc.quantize_1x128(x, orc.E4M3, mode)
+    return orc.gemm(rows, N, K, orc.operand(qx, orc.E4M3, orc.GRAN_1x128, sx),
+                    orc.operand(qw, orc.E4M3, orc.GRAN_128x128, sw))
+
+
 def cpu_oracle_sample(wl, rows=8):
     """Time the oracle on a bounded sample of an fprop workload: per linear,
     quantize the full W (128x128) and `rows` rows of X (1x128), and compute
@@ -358,10 +553,7 @@ def cpu_oracle_sample(wl, rows=8):
     flops = 0.0
     for x, w in zip(xs, ws):
         N, K = w.shape
-        qw, sw = orc.quantize_128x128(w, orc.E4M3, mode)
-        qx, sx = orc.quantize_1x128(x, orc.E4M3, mode)
-        orc.gemm(rows, N, K, orc.operand(qx, orc.E4M3, orc.GRAN_1x128, sx),
-                 orc.operand(qw, orc.E4M3, orc.GRAN_128x128, sw))
+        _oracle_linear(orc, x, w, rows, N, K, mode, wl.mx)
         flops += 2.0 * rows * N * K
     return time.perf_counter() - t0, flops
 
@@ -380,17 +572,15 @@ def run_reference(args):
         print(json.dumps({"impl": "reference", "unavailable":
                           "the reference arm samples the fprop workloads only"}), flush=True)
         return 0
-    mode = orc.SCALE_POW2 if cfg["scale_mode"] == "pow2" else orc.SCALE_FP32
+    mode = orc.SCALE_POW2 if cfg["scale_mode"] in ("pow2", "mx") else orc.SCALE_FP32
+    mx = cfg["scale_mode"] == "mx"
     lin = [(W_.activations(4, K, seed=1), W_.gaussian((128, K), 0.02, seed=2), K)
            for _, N, K in cfg["linears"]]
 
     def step():
         f = 0.0
         for x, w, K in lin:
-            qw, sw = orc.quantize_128x128(w, orc.E4M3, mode)
-            qx, sx = orc.quantize_1x128(x, orc.E4M3, mode)
-            orc.gemm(4, 128, K, orc.operand(qx, orc.E4M3, orc.GRAN_1x128, sx),
-                     orc.operand(qw, orc.E4M3, orc.GRAN_128x128, sw))
+            _oracle_linear(orc, x, w, 4, 128, K, mode, mx)
             f += 2.0 * 4 * 128 * K
         return f
 
@@ -402,7 +592,8 @@ def run_reference(args):
         fl += step()
     dt = time.perf_counter() - t0
     val = fl / dt / 1e12
-    sample = "per linear: 128 W rows (128x128), 4 X rows (1x128), 4x128 outputs in fp64"
+    sample = ("per linear: 128 W rows and 4 X rows (MXFP8 1x32), 4x128 outputs in fp64" if mx else
+              "per linear: 128 W rows (128x128), 4 X rows (1x128), 4x128 outputs in fp64")
     line = {"metric": METRIC, "value": val, "unit": "TFLOP/s", "n_gpus": ws, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",

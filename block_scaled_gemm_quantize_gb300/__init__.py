@@ -24,7 +24,8 @@ from .build import LIB as _LIB_PATH
 E4M3, E5M2 = 0, 1
 SCALE_FP32, SCALE_POW2 = 0, 1
 OUT_F32, OUT_BF16 = 0, 1
-GRAN_1x128, GRAN_128x128, GRAN_TENSOR = 0, 1, 2
+GRAN_1x128, GRAN_128x128, GRAN_TENSOR, GRAN_1x32 = 0, 1, 2, 3
+EPI_NONE, EPI_SWIGLU = 0, 1
 
 STATUS = {0: "OK", -1: "INVALID_ARG", -2: "UNSUPPORTED", -3: "MISALIGNED", -4: "CUDA",
           -5: "DEVICE_TIMEOUT"}
@@ -65,9 +66,14 @@ def lib() -> ctypes.CDLL:
             "fp8_quantize_1x128": [vp, i64, i64, i64, i32, i32, vp, i64, vp, vp],
             "fp8_quantize_128x128": [vp, i64, i64, i64, i32, i32, vp, i64, vp, vp],
             "fp8_quantize_tensor_delayed": [vp, i64, i32, vp, vp, vp, vp],
+            "fp8_quantize_mx": [vp, i64, i64, i64, i32, vp, i64, vp, vp],
+            "fp8_quantize_1x128_colwise": [vp, i64, i64, i64, i32, i32, vp, i64, vp, vp, i64, vp, vp],
             "fp8_amax_history_update": [vp, vp, i32, vp, i32, i32, vp, vp],
             "fp8_block_gemm": [i64, i64, i64, op, op, i32, vp, i64, i32, vp],
             "fp8_grouped_block_gemm": [i32, vp, i64, i64, i64, op, op, i32, vp, i64, i32, vp],
+            "fp8_block_gemm_quant": [i64, i64, i64, op, op, i32, i32, i32, i32, vp, i64, vp, vp],
+            "fp8_grouped_block_gemm_quant": [i32, vp, i64, i64, i64, op, op, i32, i32, i32, i32, vp, i64,
+                                             vp, vp],
             "fp8bs_device_status": [vp],
             "fp8bs_selftest_wait_timeout": [i32, vp, vp],
             "fp8bs_version": [],
@@ -149,6 +155,54 @@ def fp8_quantize_128x128(w, fmt=E4M3, mode=SCALE_FP32, q=None, scales=None, stre
     return q, scales
 
 
+def fp8_quantize_mx(x, fmt=E4M3, q=None, scales=None, stream=None):
+    """MXFP8: one E8M0 scale per 32 elements of a row.  Returns (q [rows, cols]
+    uint8, scales [cols/128, rows, 4] uint8)."""
+    torch = _torch()
+    _rowmajor(_dev(x, "x", torch.bfloat16), "x")
+    rows, cols = x.shape
+    if q is None:
+        q = torch.empty((rows, cols), dtype=torch.uint8, device=x.device)
+    if scales is None:
+        scales = torch.empty((cols // 128, rows, 4), dtype=torch.uint8, device=x.device)
+    _rowmajor(_dev(q, "q", torch.uint8), "q")
+    _dev(scales, "scales", torch.uint8)
+    _call("fp8_quantize_mx", x.data_ptr(), rows, cols, x.stride(0), fmt, q.data_ptr(), q.stride(0),
+          scales.data_ptr(), _stream(stream))
+    return q, scales
+
+
+def fp8_quantize_1x128_colwise(x, fmt=E4M3, mode=SCALE_FP32, rowwise=False, qt=None, scales_t=None,
+                               q=None, scales=None, stream=None):
+    """Column-wise 1x128 tiles (128 rows of one column), written transposed:
+    returns (qt [cols, rows] uint8, scales_t [rows/128, cols] fp32) and, with
+    rowwise=True (or q/scales given), also the row-wise (q, scales) from the
+    same read of x."""
+    torch = _torch()
+    _rowmajor(_dev(x, "x", torch.bfloat16), "x")
+    rows, cols = x.shape
+    if qt is None:
+        qt = torch.empty((cols, rows), dtype=torch.uint8, device=x.device)
+    if scales_t is None:
+        scales_t = torch.empty((rows // 128, cols), dtype=torch.float32, device=x.device)
+    _rowmajor(_dev(qt, "qt", torch.uint8), "qt")
+    _dev(scales_t, "scales_t", torch.float32)
+    if rowwise or q is not None:
+        if q is None:
+            q = torch.empty((rows, cols), dtype=torch.uint8, device=x.device)
+        if scales is None:
+            scales = torch.empty((cols // 128, rows), dtype=torch.float32, device=x.device)
+        _rowmajor(_dev(q, "q", torch.uint8), "q")
+        _dev(scales, "scales", torch.float32)
+    _call("fp8_quantize_1x128_colwise", x.data_ptr(), rows, cols, x.stride(0), fmt, mode, qt.data_ptr(),
+          qt.stride(0), scales_t.data_ptr(), q.data_ptr() if q is not None else None,
+          q.stride(0) if q is not None else 0, scales.data_ptr() if scales is not None else None,
+          _stream(stream))
+    if q is not None:
+        return qt, scales_t, q, scales
+    return qt, scales_t
+
+
 def fp8_quantize_tensor_delayed(x, fmt, scale, q=None, amax=None, stream=None):
     """Per-tensor quantization with the scale in use (device scalar); returns (q, amax)."""
     torch = _torch()
@@ -222,7 +276,7 @@ def operand(q, scales, fmt=E4M3, gran=GRAN_1x128, transposed=False) -> Operand:
     transposed, [K, rows]; scales follow the table layouts of fp8bs.h."""
     torch = _torch()
     _rowmajor(_dev(q, "q", torch.uint8), "q")
-    _dev(scales, "scales", torch.float32)
+    _dev(scales, "scales", torch.uint8 if gran == GRAN_1x32 else torch.float32)
     op = Operand(data=q.data_ptr(), ld=q.stride(0), transposed=int(bool(transposed)), fmt=fmt,
                  gran=gran, reserved=0, scales=scales.data_ptr())
     op._keep = (q, scales)
@@ -257,6 +311,44 @@ def fp8_grouped_block_gemm(offsets, A: Operand, B: Operand, a_rows: int, N: int,
           ctypes.byref(A), ctypes.byref(B), mode, y.data_ptr(), y.stride(0), out_dtype,
           _stream(stream))
     return y
+
+
+def _quant_out(rows, n_out, q, q_scales, device):
+    torch = _torch()
+    if q is None:
+        q = torch.empty((rows, n_out), dtype=torch.uint8, device=device)
+    if q_scales is None:
+        q_scales = torch.empty((n_out // 128, rows), dtype=torch.float32, device=device)
+    _rowmajor(_dev(q, "q", torch.uint8), "q")
+    _dev(q_scales, "q_scales", torch.float32)
+    return q, q_scales
+
+
+def fp8_block_gemm_quant(A: Operand, B: Operand, M: int, N: int, K: int, epilogue=EPI_NONE,
+                         q_fmt=E4M3, q_mode=SCALE_FP32, mode=SCALE_FP32, q=None, q_scales=None,
+                         stream=None):
+    """Product whose epilogue emits the next linear's FP8 operand: Z = Y or
+    (SwiGLU) silu(Y[:, :N/2]) * Y[:, N/2:], quantized per 1x128 tile.
+    Returns (q [M, cols(Z)] uint8, q_scales [cols(Z)/128, M] fp32)."""
+    n_out = N // 2 if epilogue == EPI_SWIGLU else N
+    q, q_scales = _quant_out(M, n_out, q, q_scales, A._keep[0].device)
+    _call("fp8_block_gemm_quant", M, N, K, ctypes.byref(A), ctypes.byref(B), mode, epilogue, q_fmt,
+          q_mode, q.data_ptr(), q.stride(0), q_scales.data_ptr(), _stream(stream))
+    return q, q_scales
+
+
+def fp8_grouped_block_gemm_quant(offsets, A: Operand, B: Operand, a_rows: int, N: int, K: int,
+                                 epilogue=EPI_NONE, q_fmt=E4M3, q_mode=SCALE_FP32, mode=SCALE_FP32,
+                                 q=None, q_scales=None, stream=None):
+    """Grouped form of fp8_block_gemm_quant (expert layers)."""
+    torch = _torch()
+    _dev(offsets, "offsets", torch.int32)
+    n_out = N // 2 if epilogue == EPI_SWIGLU else N
+    q, q_scales = _quant_out(a_rows, n_out, q, q_scales, offsets.device)
+    _call("fp8_grouped_block_gemm_quant", offsets.numel() - 1, offsets.data_ptr(), a_rows, N, K,
+          ctypes.byref(A), ctypes.byref(B), mode, epilogue, q_fmt, q_mode, q.data_ptr(), q.stride(0),
+          q_scales.data_ptr(), _stream(stream))
+    return q, q_scales
 
 
 def linear_fprop(x, w, mode=SCALE_FP32, out_dtype=OUT_BF16, stream=None):

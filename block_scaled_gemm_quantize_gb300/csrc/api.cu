@@ -86,15 +86,17 @@ int make_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer, u
     return FP8BS_OK;
 }
 
-// Output tensor [rows][N] of bf16 or fp32 with row pitch `pitch` bytes; box
-// 32 rows x 64 bytes, 64-byte swizzle (matches the epilogue's staging slabs).
-int make_out_map(CUtensorMap* m, void* base, bool bf16, uint64_t N, uint64_t rows, uint64_t pitch) {
+// Output tensor [rows][N] of fp32, bf16 or 8-bit codes (esz 4, 2, 1) with
+// row pitch `pitch` bytes; box 32 rows x 64 bytes, 64-byte swizzle (matches
+// the epilogue's staging slabs).
+int make_out_map(CUtensorMap* m, void* base, int esz, uint64_t N, uint64_t rows, uint64_t pitch) {
     cuuint64_t dims[2] = {N, rows};
     cuuint64_t strides[1] = {pitch};
-    cuuint32_t box[2] = {bf16 ? 32u : 16u, 32u};
+    cuuint32_t box[2] = {64u / static_cast<cuuint32_t>(esz), 32u};
     cuuint32_t estr[2] = {1, 1};
-    CUresult r = g_encode(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2,
-                          base, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+    const CUtensorMapDataType dt = esz == 4 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
+                                 : esz == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8;
+    CUresult r = g_encode(m, dt, 2, base, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                           CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
                           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS)
@@ -128,12 +130,17 @@ int check_operand(const char* fn, const char* name, const fp8bs_operand* o, int6
     if (!o) return fail(FP8BS_ERR_INVALID_ARG, "%s: %s is null", fn, name);
     if (!o->data || !o->scales) return fail(FP8BS_ERR_INVALID_ARG, "%s: %s data/scales null", fn, name);
     if (!valid_fmt(o->fmt)) return fail(FP8BS_ERR_INVALID_ARG, "%s: %s bad format", fn, name);
-    if (o->gran < 0 || o->gran > 2 || o->reserved != 0)
+    if (o->gran < 0 || o->gran > 3 || o->reserved != 0)
         return fail(FP8BS_ERR_INVALID_ARG, "%s: %s bad granularity", fn, name);
+    if (o->gran == FP8BS_GRAN_1x32 && (o->transposed || grouped))
+        return fail(FP8BS_ERR_UNSUPPORTED, "%s: %s MXFP8 (1x32) operands must be non-transposed, not grouped",
+                    fn, name);
     if (o->transposed != 0 && o->transposed != 1)
         return fail(FP8BS_ERR_INVALID_ARG, "%s: %s bad transposed flag", fn, name);
-    if (o->gran == FP8BS_GRAN_1x128 && (is_b || o->transposed))
-        return fail(FP8BS_ERR_UNSUPPORTED, "%s: %s 1x128 scales only on a non-transposed A", fn, name);
+    if (o->gran == FP8BS_GRAN_1x128 && o->transposed)
+        return fail(FP8BS_ERR_UNSUPPORTED, "%s: %s 1x128 scales only on a non-transposed operand", fn, name);
+    if (o->gran == FP8BS_GRAN_1x128 && is_b && grouped)
+        return fail(FP8BS_ERR_UNSUPPORTED, "%s: 1x128 B scales not supported in a grouped product", fn);
     if (grouped && o->transposed)
         return fail(FP8BS_ERR_UNSUPPORTED, "%s: %s must be non-transposed in a grouped product", fn, name);
     if (grouped && !is_b && o->gran == FP8BS_GRAN_128x128)
@@ -146,24 +153,45 @@ int check_operand(const char* fn, const char* name, const fp8bs_operand* o, int6
     return FP8BS_OK;
 }
 
+// Where and how a product writes its result.
+struct OutSpec {
+    void* y;              // Y (float output) or Q (8-bit codes)
+    int64_t ld;           // elements between rows
+    int32_t dtype;        // FP8BS_OUT_F32 / FP8BS_OUT_BF16 (float output)
+    bool quant;           // quantized output: codes + 1x128 scales
+    int32_t epilogue;     // FP8BS_EPI_NONE / FP8BS_EPI_SWIGLU (quantized output)
+    int32_t q_fmt, q_mode;
+    float* q_scales;      // [n_out/128][a_rows]
+};
+
 int run_gemm(const char* fn, int32_t G, const int32_t* offsets, int64_t a_rows, int64_t M,
              int64_t N, int64_t K, const fp8bs_operand* A, const fp8bs_operand* B, int32_t mode,
-             void* Y, int64_t ld_y, int32_t out_dtype, cudaStream_t stream) {
+             const OutSpec& o, cudaStream_t stream) {
     const bool grouped = offsets != nullptr;
     if (M < 0 || N < 0 || K < 0 || a_rows < 0) return fail(FP8BS_ERR_INVALID_ARG, "%s: negative size", fn);
     if (!valid_mode(mode)) return fail(FP8BS_ERR_INVALID_ARG, "%s: bad scale mode", fn);
-    if (out_dtype != FP8BS_OUT_F32 && out_dtype != FP8BS_OUT_BF16)
+    if (!o.quant && o.dtype != FP8BS_OUT_F32 && o.dtype != FP8BS_OUT_BF16)
         return fail(FP8BS_ERR_INVALID_ARG, "%s: bad output dtype", fn);
+    if (o.quant && (o.epilogue != FP8BS_EPI_NONE && o.epilogue != FP8BS_EPI_SWIGLU))
+        return fail(FP8BS_ERR_INVALID_ARG, "%s: bad epilogue", fn);
+    if (o.quant && (!valid_fmt(o.q_fmt) || !valid_mode(o.q_mode)))
+        return fail(FP8BS_ERR_INVALID_ARG, "%s: bad output format or scale mode", fn);
     if (grouped && (G < 1 || G > fp8bs::kMaxGroups))
         return fail(FP8BS_ERR_INVALID_ARG, "%s: num_groups must be in [1, %d]", fn, fp8bs::kMaxGroups);
+    const bool swiglu = o.quant && o.epilogue == FP8BS_EPI_SWIGLU;
+    if (swiglu && N % 256) return fail(FP8BS_ERR_UNSUPPORTED, "%s: SwiGLU needs N %% 256 == 0", fn);
+    if (o.quant && N % 128) return fail(FP8BS_ERR_UNSUPPORTED, "%s: quantized output needs N %% 128 == 0", fn);
     if (M == 0 || N == 0) return FP8BS_OK;
-    if (!Y) return fail(FP8BS_ERR_INVALID_ARG, "%s: Y is null", fn);
-    if (ld_y < N) return fail(FP8BS_ERR_INVALID_ARG, "%s: ld_y < N", fn);
-    const int64_t esz = out_dtype == FP8BS_OUT_BF16 ? 2 : 4;
-    if (!aligned16(Y) || (ld_y * esz) % 16)
-        return fail(FP8BS_ERR_MISALIGNED, "%s: Y must be 16-byte aligned with 16-byte row pitch", fn);
-    if (K == 0) {  // empty contraction: Y = 0
-        cudaError_t e = cudaMemset2DAsync(Y, ld_y * esz, 0, N * esz, M, stream);
+    const int64_t n_out = swiglu ? N / 2 : N;
+    const int64_t esz = o.quant ? 1 : (o.dtype == FP8BS_OUT_BF16 ? 2 : 4);
+    if (!o.y) return fail(FP8BS_ERR_INVALID_ARG, "%s: output is null", fn);
+    if (o.quant && !o.q_scales) return fail(FP8BS_ERR_INVALID_ARG, "%s: output scales are null", fn);
+    if (o.ld < n_out) return fail(FP8BS_ERR_INVALID_ARG, "%s: output leading dimension too small", fn);
+    if (!aligned16(o.y) || (o.ld * esz) % 16 || (o.quant && !aligned4(o.q_scales)))
+        return fail(FP8BS_ERR_MISALIGNED, "%s: output must be 16-byte aligned with 16-byte row pitch", fn);
+    if (K == 0) {  // empty contraction: Y = 0 (quantized: codes 0, scales 1)
+        cudaError_t e = cudaMemset2DAsync(o.y, o.ld * esz, 0, n_out * esz, M, stream);
+        if (e == cudaSuccess && o.quant) e = fp8bs::launch_fill_f32(o.q_scales, (n_out / 128) * M, 1.0f, stream);
         return e == cudaSuccess ? FP8BS_OK : cuda_fail(e, fn);
     }
     if (K % 128) return fail(FP8BS_ERR_UNSUPPORTED, "%s: K %% 128 != 0 (K=%lld)", fn, (long long)K);
@@ -171,6 +199,16 @@ int run_gemm(const char* fn, int32_t G, const int32_t* offsets, int64_t a_rows, 
     int rc;
     if ((rc = check_operand(fn, "A", A, M, K, false, grouped)) != FP8BS_OK) return rc;
     if ((rc = check_operand(fn, "B", B, N, K, true, grouped)) != FP8BS_OK) return rc;
+    if (swiglu && (A->transposed || B->transposed))
+        return fail(FP8BS_ERR_UNSUPPORTED, "%s: SwiGLU needs non-transposed operands", fn);
+    if (B->gran == FP8BS_GRAN_1x128 && (swiglu || A->transposed))
+        return fail(FP8BS_ERR_UNSUPPORTED, "%s: 1x128 B scales need a non-transposed A and no SwiGLU", fn);
+    const bool mx32 = A->gran == FP8BS_GRAN_1x32 || B->gran == FP8BS_GRAN_1x32;
+    if (mx32 && (A->gran != B->gran || swiglu))
+        return fail(FP8BS_ERR_UNSUPPORTED, "%s: MXFP8 (1x32) needs both operands 1x32 and no SwiGLU", fn);
+    if (mx32 && (a_rows % 4 || !aligned16(A->scales)))
+        return fail(a_rows % 4 ? FP8BS_ERR_UNSUPPORTED : FP8BS_ERR_MISALIGNED,
+                    "%s: MXFP8 A scales need rows %% 4 == 0 and a 16-byte aligned table", fn);
     if (a_rows > (int64_t)INT32_MAX - 256 || N * (grouped ? G : 1) > (int64_t)INT32_MAX - 256 ||
         K > (int64_t)INT32_MAX)
         return fail(FP8BS_ERR_UNSUPPORTED, "%s: dimension beyond 2^31", fn);
@@ -184,11 +222,11 @@ int run_gemm(const char* fn, int32_t G, const int32_t* offsets, int64_t a_rows, 
     if (rc) return rc;
     const int64_t b_rows_total = grouped ? (int64_t)G * N : N;
     if (b_mn) rc = make_map(&tmB, B->data, N, K, B->ld, 128);
-    else rc = make_map(&tmB, B->data, K, b_rows_total, B->ld, BN);
+    else rc = make_map(&tmB, B->data, K, b_rows_total, B->ld, swiglu ? 64 : BN);
     if (rc) return rc;
 
     CUtensorMap tmY;
-    if ((rc = make_out_map(&tmY, Y, out_dtype == FP8BS_OUT_BF16, N, a_rows, ld_y * esz)) != FP8BS_OK)
+    if ((rc = make_out_map(&tmY, o.y, static_cast<int>(esz), n_out, a_rows, o.ld * esz)) != FP8BS_OK)
         return rc;
 
     fp8bs::GemmParams p;
@@ -204,15 +242,23 @@ int run_gemm(const char* fn, int32_t G, const int32_t* offsets, int64_t a_rows, 
     p.sa = A->scales;
     p.sb = B->scales;
     p.offsets = offsets;
-    p.y = Y;
-    p.ldy = ld_y;
+    p.y = o.y;
+    p.ldy = o.ld;
     p.num_groups = grouped ? G : 1;
     p.b_rows_per_group = grouped ? static_cast<int32_t>(N) : 0;
     p.a_gran = A->gran;
     p.b_gran = B->gran;
-    p.tiles_n = static_cast<int32_t>((N + BN - 1) / BN);
+    p.tiles_n = static_cast<int32_t>(swiglu ? n_out / 128 : (N + BN - 1) / BN);
     p.promote = (A->gran == FP8BS_GRAN_TENSOR && B->gran == FP8BS_GRAN_TENSOR) ? 0 : 1;
-    p.out_bf16 = out_dtype == FP8BS_OUT_BF16;
+    p.out_bf16 = !o.quant && o.dtype == FP8BS_OUT_BF16;
+    p.out_q = o.quant;
+    p.q_fmt = o.q_fmt;
+    p.q_mode = o.q_mode;
+    p.sq = o.q_scales;
+    p.n_out = n_out;
+    p.swiglu = swiglu;
+    p.swiglu_i = swiglu ? N / 2 : 0;
+    p.mx32 = mx32;
     p.idesc = fp8bs::make_idesc_f8f6f4(A->fmt, B->fmt, a_mn, b_mn, b_mn ? 128 : fp8bs::gemm_mma_n());
 
     // upper bound on tiles (the grouped count is only known on the device)
@@ -226,10 +272,18 @@ int run_gemm(const char* fn, int32_t G, const int32_t* offsets, int64_t a_rows, 
     // Power-of-two scales on K-major operands go to the block-scaled (MX)
     // kernel: the tensor core applies the UE8M0 scales, no promotion.
     cudaError_t e;
+    if (mx32) {   // MXFP8: the block-scaled kernel reads the E8M0 words directly
+        CUtensorMap tmSA;
+        if ((rc = make_scale_map(&tmSA, A->scales, a_rows, K / 128)) != FP8BS_OK) return rc;
+        p.idesc = fp8bs::make_idesc_mx(A->fmt, B->fmt, BN);
+        e = fp8bs::launch_fp8_gemm_mx(tmA, tmB, tmY, tmSA, p, grid, stream);
+        return e == cudaSuccess ? FP8BS_OK : cuda_fail(e, fn);
+    }
 #ifndef FP8BS_NO_MX
     // (1x128 A scales reach the kernel by TMA: a row pitch of 16 bytes needed)
     const bool sa_tma_ok = A->gran != FP8BS_GRAN_1x128 || (a_rows % 4 == 0 && aligned16(A->scales));
-    if (mode == FP8BS_SCALE_POW2 && !a_mn && !b_mn && !grouped && sa_tma_ok) {
+    if (mode == FP8BS_SCALE_POW2 && !a_mn && !b_mn && !grouped && sa_tma_ok &&
+        B->gran != FP8BS_GRAN_1x128) {
         CUtensorMap tmSA;
         memset(&tmSA, 0, sizeof(tmSA));
         if (A->gran == FP8BS_GRAN_1x128 && (rc = make_scale_map(&tmSA, A->scales, a_rows, K / 128)) != FP8BS_OK)
@@ -240,6 +294,28 @@ int run_gemm(const char* fn, int32_t G, const int32_t* offsets, int64_t a_rows, 
 #endif
         e = fp8bs::launch_fp8_gemm(tmA, tmB, tmY, p, a_mn, b_mn, grid, stream);
     return e == cudaSuccess ? FP8BS_OK : cuda_fail(e, fn);
+}
+
+OutSpec float_out(void* Y, int64_t ld_y, int32_t out_dtype) {
+    OutSpec o;
+    memset(&o, 0, sizeof(o));
+    o.y = Y;
+    o.ld = ld_y;
+    o.dtype = out_dtype;
+    return o;
+}
+
+OutSpec quant_out(uint8_t* Q, int64_t ld_q, int32_t epilogue, int32_t q_fmt, int32_t q_mode, float* q_scales) {
+    OutSpec o;
+    memset(&o, 0, sizeof(o));
+    o.y = Q;
+    o.ld = ld_q;
+    o.quant = true;
+    o.epilogue = epilogue;
+    o.q_fmt = q_fmt;
+    o.q_mode = q_mode;
+    o.q_scales = q_scales;
+    return o;
 }
 
 }  // namespace
@@ -268,6 +344,40 @@ int fp8_quantize_128x128(const void* w, int64_t rows, int64_t cols, int64_t ld_w
     cudaError_t e = fp8bs::launch_quant_128x128(static_cast<const uint16_t*>(w), rows, cols, ld_w,
                                                 fmt, mode, q, ld_q, scales, (cudaStream_t)stream);
     return e == cudaSuccess ? FP8BS_OK : cuda_fail(e, "fp8_quantize_128x128");
+}
+
+int fp8_quantize_mx(const void* x, int64_t rows, int64_t cols, int64_t ld_x, int32_t fmt, uint8_t* q,
+                    int64_t ld_q, uint8_t* scales, fp8bs_stream_t stream) {
+    const char* fn = "fp8_quantize_mx";
+    int rc = check_block_quant(fn, x, rows, cols, ld_x, fmt, FP8BS_SCALE_POW2, q, ld_q,
+                               reinterpret_cast<const float*>(scales));
+    if (rc <= 0) return rc;
+    cudaError_t e = fp8bs::launch_quant_mx(static_cast<const uint16_t*>(x), rows, cols, ld_x, fmt, q, ld_q,
+                                           reinterpret_cast<uint32_t*>(scales), (cudaStream_t)stream);
+    return e == cudaSuccess ? FP8BS_OK : cuda_fail(e, fn);
+}
+
+int fp8_quantize_1x128_colwise(const void* x, int64_t rows, int64_t cols, int64_t ld_x, int32_t fmt,
+                               int32_t mode, uint8_t* qt, int64_t ld_qt, float* scales_t, uint8_t* q,
+                               int64_t ld_q, float* scales, fp8bs_stream_t stream) {
+    const char* fn = "fp8_quantize_1x128_colwise";
+    if (rows < 0 || cols < 0) return fail(FP8BS_ERR_INVALID_ARG, "%s: negative size", fn);
+    if (!valid_fmt(fmt) || !valid_mode(mode))
+        return fail(FP8BS_ERR_INVALID_ARG, "%s: bad format %d or scale mode %d", fn, fmt, mode);
+    if ((q == nullptr) != (scales == nullptr))
+        return fail(FP8BS_ERR_INVALID_ARG, "%s: row-wise q and scales must both be given or both be null", fn);
+    if (rows == 0 || cols == 0) return FP8BS_OK;
+    if (!x || !qt || !scales_t) return fail(FP8BS_ERR_INVALID_ARG, "%s: null pointer", fn);
+    if (ld_x < cols || ld_qt < rows || (q && ld_q < cols))
+        return fail(FP8BS_ERR_INVALID_ARG, "%s: leading dimension too small", fn);
+    if (rows % 128 || cols % 128)
+        return fail(FP8BS_ERR_UNSUPPORTED, "%s: rows and cols must be multiples of 128", fn);
+    if (!aligned16(x) || (ld_x * 2) % 16 || !aligned16(qt) || ld_qt % 16 || !aligned4(scales_t) ||
+        (q && (!aligned16(q) || ld_q % 16 || !aligned4(scales))))
+        return fail(FP8BS_ERR_MISALIGNED, "%s: x/q/qt must be 16-byte aligned with 16-byte row pitch", fn);
+    cudaError_t e = fp8bs::launch_quant_colwise(static_cast<const uint16_t*>(x), rows, cols, ld_x, fmt, mode,
+                                                qt, ld_qt, scales_t, q, ld_q, scales, (cudaStream_t)stream);
+    return e == cudaSuccess ? FP8BS_OK : cuda_fail(e, fn);
 }
 
 int fp8_quantize_tensor_delayed(const void* x, int64_t numel, int32_t fmt, const float* scale,
@@ -301,8 +411,16 @@ int fp8_amax_history_update(float* history, int32_t* head, int32_t history_len, 
 int fp8_block_gemm(int64_t M, int64_t N, int64_t K, const fp8bs_operand* A,
                    const fp8bs_operand* B, int32_t mode, void* Y, int64_t ld_y, int32_t out_dtype,
                    fp8bs_stream_t stream) {
-    return run_gemm("fp8_block_gemm", 1, nullptr, M, M, N, K, A, B, mode, Y, ld_y, out_dtype,
+    return run_gemm("fp8_block_gemm", 1, nullptr, M, M, N, K, A, B, mode, float_out(Y, ld_y, out_dtype),
                     (cudaStream_t)stream);
+}
+
+int fp8_block_gemm_quant(int64_t M, int64_t N, int64_t K, const fp8bs_operand* A,
+                         const fp8bs_operand* B, int32_t mode, int32_t epilogue, int32_t q_fmt,
+                         int32_t q_mode, uint8_t* Q, int64_t ld_q, float* q_scales,
+                         fp8bs_stream_t stream) {
+    return run_gemm("fp8_block_gemm_quant", 1, nullptr, M, M, N, K, A, B, mode,
+                    quant_out(Q, ld_q, epilogue, q_fmt, q_mode, q_scales), (cudaStream_t)stream);
 }
 
 int fp8_grouped_block_gemm(int32_t num_groups, const int32_t* row_offsets, int64_t a_rows,
@@ -312,7 +430,17 @@ int fp8_grouped_block_gemm(int32_t num_groups, const int32_t* row_offsets, int64
     if (!row_offsets) return fail(FP8BS_ERR_INVALID_ARG, "fp8_grouped_block_gemm: null row_offsets");
     if (!aligned4(row_offsets)) return fail(FP8BS_ERR_MISALIGNED, "fp8_grouped_block_gemm: offsets");
     return run_gemm("fp8_grouped_block_gemm", num_groups, row_offsets, a_rows, a_rows, N, K, A, B,
-                    mode, Y, ld_y, out_dtype, (cudaStream_t)stream);
+                    mode, float_out(Y, ld_y, out_dtype), (cudaStream_t)stream);
+}
+
+int fp8_grouped_block_gemm_quant(int32_t num_groups, const int32_t* row_offsets, int64_t a_rows,
+                                 int64_t N, int64_t K, const fp8bs_operand* A, const fp8bs_operand* B,
+                                 int32_t mode, int32_t epilogue, int32_t q_fmt, int32_t q_mode,
+                                 uint8_t* Q, int64_t ld_q, float* q_scales, fp8bs_stream_t stream) {
+    if (!row_offsets) return fail(FP8BS_ERR_INVALID_ARG, "fp8_grouped_block_gemm_quant: null row_offsets");
+    if (!aligned4(row_offsets)) return fail(FP8BS_ERR_MISALIGNED, "fp8_grouped_block_gemm_quant: offsets");
+    return run_gemm("fp8_grouped_block_gemm_quant", num_groups, row_offsets, a_rows, a_rows, N, K, A, B,
+                    mode, quant_out(Q, ld_q, epilogue, q_fmt, q_mode, q_scales), (cudaStream_t)stream);
 }
 
 int fp8bs_selftest_wait_timeout(int32_t limit_ms, int32_t* waited_ok, fp8bs_stream_t stream) {

@@ -39,6 +39,7 @@
 #include <cuda_runtime.h>
 #include <cstdint>
 
+#include "fp8_math.cuh"
 #include "gemm_kernels.h"
 #include "ptx_sm100.cuh"
 
@@ -86,13 +87,21 @@ constexpr uint32_t BAR_OFF = STAGES * STAGE_BYTES;
 constexpr int HALVES = FP8BS_HALVES;
 constexpr int MMA_N = BN / HALVES;
 constexpr int TBUFS = 512 / MMA_N;
-constexpr int NUM_BARS = 2 * STAGES + 2 * TBUFS + 1;   // full, empty, tfull, tempty, done
+// per-column B scales (1x128 B): a ring of BSF_SLOTS K blocks x 256 fp32
+constexpr int BSF_SLOTS = 4;
+constexpr int BSF_LPF = 4;                            // loader prefetch distance (K blocks)
+// full, empty, tfull, tempty, done, xchg[4], bsf_full, bsf_empty
+constexpr int NUM_BARS = 2 * STAGES + 2 * TBUFS + 1 + 4 + 2 * BSF_SLOTS;
 constexpr uint32_t TMEMSLOT_OFF = BAR_OFF + NUM_BARS * 8;
 constexpr uint32_t TABLE_OFF = (TMEMSLOT_OFF + 16 + 15) & ~15u;
 // output staging: one 2 KiB slab per epilogue warp (32 rows x 64 B, 64-B swizzle)
 constexpr uint32_t OUT_SLAB = 2048;
 constexpr uint32_t OUT_OFF = (TABLE_OFF + 2 * (kMaxGroups + 1) * 4 + 1023) & ~1023u;
-constexpr uint32_t SMEM_BYTES = 1024 + OUT_OFF + NUM_EPI_WARPS * OUT_SLAB;
+// amax exchange of the SwiGLU epilogue: [tile parity][column half][row] fp32
+constexpr uint32_t XCHG_BYTES = 2 * 2 * 128 * 4;
+constexpr uint32_t XCHG_OFF = OUT_OFF + NUM_EPI_WARPS * OUT_SLAB;
+constexpr uint32_t BSF_OFF = XCHG_OFF + XCHG_BYTES;
+constexpr uint32_t SMEM_BYTES = 1024 + BSF_OFF + BSF_SLOTS * 1024;
 static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 
 __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
@@ -215,7 +224,123 @@ __device__ __forceinline__ void store_tile(const GemmParams& p, const CUtensorMa
     }
 }
 
-template <bool A_MN, bool B_MN>
+// SwiGLU on one thread's 128 accumulator columns: columns 0-63 hold gate
+// values and 64-127 the up values of the same 64 output columns; the
+// results h = silu(gate) * up, silu(g) = g / (1 + e^-g), replace acc[0..31].
+// The exponential and the division are the fast hardware forms (__expf,
+// __fdividef: relative error about 5e-7 + 4e-8 |g|), since this runs on
+// the critical path between tiles; the result is quantized to 8 bits.
+// (g < -88: e^-g = inf and g / inf = -0.)
+__device__ __forceinline__ void swiglu_inplace(uint64_t (&acc)[64]) {
+#pragma unroll
+    for (int i = 0; i < 32; i++) {
+        const float2 g = unpack_f32x2(acc[i]);
+        const float2 u = unpack_f32x2(acc[32 + i]);
+        const float hx = __fdividef(g.x, 1.0f + __expf(-g.x)) * u.x;
+        const float hy = __fdividef(g.y, 1.0f + __expf(-g.y)) * u.y;
+        acc[i] = pack_f32x2(__float_as_uint(hx), __float_as_uint(hy));
+    }
+}
+
+// Quantize one thread's first `nv` (128 or 64) output values of its row with
+// the reciprocal block scale r and store the codes: TMA bulk stores of
+// 32-row x 64-byte slabs as for the float output, else masked direct stores.
+__device__ __forceinline__ void store_tile_q(const GemmParams& p, const CUtensorMap& tmY,
+                                             const uint64_t (&acc)[64], int nv, float r,
+                                             const Tile& tl, int64_t row, bool row_ok,
+                                             int64_t qcol0, int quarter, int lane, uint32_t slab) {
+    const int64_t wrow0 = static_cast<int64_t>(tl.row0) + quarter * 32;
+    const int fmt = p.q_fmt;
+    if (p.tma_store && (p.offsets == nullptr || wrow0 + 32 <= tl.row_end)) {
+        const uint32_t rbase = slab + lane * 64;
+        const uint32_t sw = (lane >> 1) & 3;          // 64-B swizzle: chunk ^= (row/2)%4
+#pragma unroll
+        for (int ps = 0; ps < 2; ps++) {
+            if (ps * 64 >= nv) break;
+            if (lane == 0) bulk_wait_group_read0();   // slab free again
+            __syncwarp();
+#pragma unroll
+            for (int c = 0; c < 4; c++) {            // 16 columns per 16-byte chunk
+                uint32_t w[4];
+#pragma unroll
+                for (int i = 0; i < 4; i++) {
+                    const float2 a = unpack_f32x2(acc[ps * 32 + c * 8 + 2 * i]);
+                    const float2 b = unpack_f32x2(acc[ps * 32 + c * 8 + 2 * i + 1]);
+                    w[i] = quant4_rt(a.x, a.y, b.x, b.y, r, fmt);
+                }
+                st_shared_v4(rbase + ((c ^ sw) << 4), w[0], w[1], w[2], w[3]);
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+                tma_store_2d(&tmY, slab, static_cast<int32_t>(qcol0 + ps * 64), static_cast<int32_t>(wrow0));
+                bulk_commit_group();
+            }
+        }
+    } else if (row_ok) {
+        uint8_t* y = reinterpret_cast<uint8_t*>(p.y) + row * p.ldy + qcol0;
+#pragma unroll
+        for (int j = 0; j < 128; j += 16) {
+            if (j >= nv) break;
+            uint32_t w[4];
+#pragma unroll
+            for (int i = 0; i < 4; i++) {
+                const float2 a = unpack_f32x2(acc[j / 2 + 2 * i]);
+                const float2 b = unpack_f32x2(acc[j / 2 + 2 * i + 1]);
+                w[i] = quant4_rt(a.x, a.y, b.x, b.y, r, fmt);
+            }
+            *reinterpret_cast<uint4*>(y + j) = make_uint4(w[0], w[1], w[2], w[3]);
+        }
+    }
+}
+
+// End of a tile in the epilogue: the float store, or (quantized output)
+// optional SwiGLU, the block amax, the 1x128 scale and the codes.  With
+// SwiGLU a 1x128 output block spans the two threads of a row (warps w and
+// w + 4): each publishes its half's amax in shared memory and both wait,
+// bounded, on their lane quarter's exchange barrier (64 arrivals per tile;
+// two buffers by tile parity).  Returns false if that wait timed out.
+template <bool SWIGLU>
+__device__ __forceinline__ bool finish_tile(const GemmParams& p, const CUtensorMap& tmY,
+                                            uint64_t (&acc)[64], const Tile& tl, int64_t row,
+                                            bool row_ok, int64_t col0, int quarter, int half,
+                                            int lane, uint32_t slab, uint32_t xbuf, uint32_t xbar,
+                                            uint32_t tile_par) {
+    if (!p.out_q) {
+        store_tile(p, tmY, acc, tl, row, row_ok, col0, quarter, lane, slab);
+        return true;
+    }
+    int nv = 128;
+    int64_t qcol0 = col0, blk_col = col0;
+    if (SWIGLU) {
+        swiglu_inplace(acc);
+        nv = 64;
+        blk_col = static_cast<int64_t>(tl.nt) * 128;
+        qcol0 = blk_col + half * 64;
+    }
+    float am = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 64; i++) {
+        if (2 * i >= nv) break;
+        const float2 f = unpack_f32x2(acc[i]);
+        am = fmaxf(am, fmaxf(fabsf(f.x), fabsf(f.y)));
+    }
+    if (SWIGLU) {
+        const int lrow = quarter * 32 + lane;
+        st_shared_f32(xbuf + ((tile_par * 2 + half) * 128 + lrow) * 4, am);
+        mbar_arrive(xbar);
+        if (!__all_sync(0xFFFFFFFFu, wait_or_flag(xbar, tile_par))) return false;
+        am = fmaxf(am, ld_shared_f32(xbuf + ((tile_par * 2 + (half ^ 1)) * 128 + lrow) * 4));
+    }
+    if (blk_col < p.n_out) {
+        const float s = block_scale_rt(am, p.q_fmt, p.q_mode);
+        store_tile_q(p, tmY, acc, nv, __frcp_rn(s), tl, row, row_ok, qcol0, quarter, lane, slab);
+        if (row_ok && (!SWIGLU || half == 0)) p.sq[(blk_col / 128) * p.a_rows + row] = s;
+    }
+    return true;
+}
+
+template <bool A_MN, bool B_MN, bool SWIGLU, bool B_COL>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     k_fp8_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                const __grid_constant__ CUtensorMap tmY, const GemmParams p) {
@@ -231,6 +356,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     auto tfull_bar = [&](int b) { return bars + 8u * (2 * STAGES + b); };
     auto tempty_bar = [&](int b) { return bars + 8u * (2 * STAGES + TBUFS + b); };
     const uint32_t done_bar = bars + 8u * (2 * STAGES + 2 * TBUFS);
+    auto xchg_bar = [&](int q) { return bars + 8u * (2 * STAGES + 2 * TBUFS + 1 + q); };
+    auto bsf_full = [&](int q) { return bars + 8u * (2 * STAGES + 2 * TBUFS + 5 + q); };
+    auto bsf_empty = [&](int q) { return bars + 8u * (2 * STAGES + 2 * TBUFS + 5 + BSF_SLOTS + q); };
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + TMEMSLOT_OFF);
     int* s_off = reinterpret_cast<int*>(smem + TABLE_OFF);
     int* s_slot = s_off + (kMaxGroups + 1);
@@ -251,6 +379,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             mbar_init(tempty_bar(b), NUM_EPI_WARPS / HALVES);   // the warps reading it
         }
         mbar_init(done_bar, 1);
+        for (int q = 0; q < 4; q++) mbar_init(xchg_bar(q), 64);
+        for (int q = 0; q < BSF_SLOTS; q++) {
+            mbar_init(bsf_full(q), 32);                   // the loader warp's lanes
+            mbar_init(bsf_empty(q), 32 * NUM_EPI_WARPS);  // every epilogue thread
+        }
         fence_mbar_init();
         fence_proxy_async_smem();
     }
@@ -314,6 +447,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     if (B_MN) {
                         tma_load_2d(dB, &tmB, b_row, kc, full_bar(stage));
                         tma_load_2d(dB + B_STAGE / 2, &tmB, b_row + 128, kc, full_bar(stage));
+                    } else if (SWIGLU) {
+                        // 64-row boxes: gate, up, gate + 64, up + 64 of this 128-column tile
+                        const int gb = tl.g * p.b_rows_per_group + tl.nt * 128;
+                        const int ub = gb + static_cast<int>(p.swiglu_i);
+                        tma_load_2d(dB, &tmB, kc, gb, full_bar(stage));
+                        tma_load_2d(dB + B_STAGE / 4, &tmB, kc, ub, full_bar(stage));
+                        tma_load_2d(dB + B_STAGE / 2, &tmB, kc, gb + 64, full_bar(stage));
+                        tma_load_2d(dB + 3 * (B_STAGE / 4), &tmB, kc, ub + 64, full_bar(stage));
                     } else {
                         tma_load_2d(dB, &tmB, kc, b_row, full_bar(stage));
                     }
@@ -389,6 +530,43 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 wait_bounded(done_bar, 0, DRAIN_LIMIT_NS);
             }
         }
+      } else if (B_COL && warp == 3) {
+        // ------------- per-column B scale loader (1x128 B: table [K/128][N])
+        // Each K block's 256 column scales of the tile go to a ring slot; the
+        // epilogue threads release a slot once they have read it.  Loads run
+        // BSF_LPF K blocks ahead in registers.
+        int slot = 0;
+        uint32_t ph = 0;
+        bool ok = true;
+        for (int t = blockIdx.x; ok && t < total_tiles; t += gridDim.x) {
+            const Tile tl = decode_tile(t, total_slots, p.tiles_n, G, s_slot, s_off);
+            const int64_t n0 = static_cast<int64_t>(tl.nt) * BN;
+            float pre[BSF_LPF][8];
+            auto load = [&](int kbi, float (&d)[8]) {
+#pragma unroll
+                for (int c = 0; c < 8; c++) {
+                    const int64_t n = n0 + 32 * c + lane;
+                    d[c] = (kbi < nkb && n < p.N) ? ld_scale(p.sb + static_cast<int64_t>(kbi) * p.N + n) : 0.0f;
+                }
+            };
+#pragma unroll
+            for (int i = 0; i < BSF_LPF; i++) load(i, pre[i]);
+            for (int kb0 = 0; ok && kb0 < nkb; kb0 += BSF_LPF) {
+#pragma unroll
+                for (int i = 0; i < BSF_LPF; i++) {
+                    const int kb = kb0 + i;
+                    if (kb >= nkb) break;
+                    ok = __all_sync(0xFFFFFFFFu, wait_or_flag(bsf_empty(slot), ph ^ 1u));
+                    if (!ok) break;
+                    const uint32_t dst = sbase + BSF_OFF + slot * 1024;
+#pragma unroll
+                    for (int c = 0; c < 8; c++) st_shared_f32(dst + (32 * c + lane) * 4, pre[i][c]);
+                    mbar_arrive(bsf_full(slot));
+                    load(kb + BSF_LPF, pre[i]);
+                    if (++slot == BSF_SLOTS) { slot = 0; ph ^= 1u; }
+                }
+            }
+        }
       }
     } else {
         asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(REGS_HIGH));
@@ -396,16 +574,21 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const int quarter = warp & 3;           // TMEM lanes 32*quarter ..
         const int half = (warp - EPI_WARP0) >> 2;  // columns 128*half ..
         const int lrow = quarter * 32 + lane;
-        uint32_t chunk = 0;
+        uint32_t chunk = 0, tile_i = 0;
+        int bslot = 0;
+        uint32_t bph = 0;
         bool ok = true;
         const int64_t nkb64 = nkb;
-        for (int t = blockIdx.x; ok && t < total_tiles; t += gridDim.x) {
+        for (int t = blockIdx.x; ok && t < total_tiles; t += gridDim.x, tile_i++) {
             const Tile tl = decode_tile(t, total_slots, p.tiles_n, G, s_slot, s_off);
             const int64_t row = static_cast<int64_t>(tl.row0) + lrow;
             const bool row_ok = row < tl.row_end;
             const int64_t srow = row < p.a_rows ? row : p.a_rows - 1;   // clamp for scale reads
             const int64_t col0 = static_cast<int64_t>(tl.nt) * BN + half * 128;
-            const int64_t nb = min(col0, p.N - 1) / 128;                // weight row-block
+            // weight row-blocks of this thread's columns 0-63 (nb) and 64-127
+            // (nbu); they differ only with SwiGLU (gate and up rows)
+            const int64_t nb = SWIGLU ? tl.nt : min(col0, p.N - 1) / 128;
+            const int64_t nbu = SWIGLU ? p.swiglu_i / 128 + tl.nt : nb;
             // scale pointers for this (row, column block); advanced per K block
             const float* pa;
             int64_t sa_step;
@@ -415,11 +598,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 else { pa = p.sa + (srow / 128) * nkb64; sa_step = 1; }
             } else { pa = p.sa; sa_step = 0; }
             const float* pb;
+            const float* pbu;
             int64_t sb_step;
             if (p.b_gran == 1) {
-                if (B_MN) { pb = p.sb + nb; sb_step = p.b_rblocks; }
-                else { pb = p.sb + tl.g * p.b_scale_group_stride + nb * nkb64; sb_step = 1; }
-            } else { pb = p.sb; sb_step = 0; }
+                if (B_MN) { pb = p.sb + nb; pbu = pb; sb_step = p.b_rblocks; }
+                else {
+                    pb = p.sb + tl.g * p.b_scale_group_stride + nb * nkb64;
+                    pbu = p.sb + tl.g * p.b_scale_group_stride + nbu * nkb64;
+                    sb_step = 1;
+                }
+            } else { pb = p.sb; pbu = pb; sb_step = 0; }
 
             uint64_t acc[64];   // 128 fp32 accumulators as packed pairs
 #pragma unroll
@@ -428,12 +616,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             // (kb0 + i); the K-block loop is unrolled by SPF so each slot is
             // refilled (SPF chunks ahead) right after use, with no register
             // copies that would wait on the load early.
-            float sa_r[SPF], sb_r[SPF];
+            float sa_r[SPF], sb_r[SPF], sbu_r[SPF];
 #pragma unroll
             for (int i = 0; i < SPF; i++) {
                 const int kbi = min(i * P, nkb - 1);
                 sa_r[i] = ld_scale(pa + kbi * sa_step);
                 sb_r[i] = ld_scale(pb + kbi * sb_step);
+                sbu_r[i] = SWIGLU ? ld_scale(pbu + kbi * sb_step) : sb_r[i];
             }
             for (int kb0 = 0; ok && kb0 < nkb; kb0 += SPF * P) {
 #pragma unroll
@@ -442,13 +631,24 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     if (kb >= nkb) break;
                     const float s = sa_r[i] * sb_r[i];
                     const uint64_t s2 = pack_f32x2(__float_as_uint(s), __float_as_uint(s));
+                    const float su = sa_r[i] * sbu_r[i];
+                    const uint64_t s2u = pack_f32x2(__float_as_uint(su), __float_as_uint(su));
+                    // A's scale alone, for per-column B scales (taken before the refill)
+                    const uint64_t sa2 = pack_f32x2(__float_as_uint(sa_r[i]), __float_as_uint(sa_r[i]));
                     if (kb + SPF * P < nkb) {
                         sa_r[i] = ld_scale(pa + (kb + SPF * P) * sa_step);
                         sb_r[i] = ld_scale(pb + (kb + SPF * P) * sb_step);
+                        sbu_r[i] = SWIGLU ? ld_scale(pbu + (kb + SPF * P) * sb_step) : sb_r[i];
                     }
                     const uint32_t c = HALVES * chunk + (HALVES == 2 ? half : 0), buf = c % TBUFS;
                     ok = __all_sync(0xFFFFFFFFu, wait_or_flag(tfull_bar(buf), (c / TBUFS) & 1u));
                     if (!ok) break;
+                    // per-column B scales of this K block (1x128 B): sa * sb[n] per pair
+                    const uint32_t sbb = sbase + BSF_OFF + bslot * 1024 + half * 512;
+                    if (B_COL) {
+                        ok = __all_sync(0xFFFFFFFFu, wait_or_flag(bsf_full(bslot), bph));
+                        if (!ok) break;
+                    }
                     tc_fence_after();
                     const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
                                            buf * MMA_N + (HALVES == 1 ? half * 128 : 0);
@@ -465,27 +665,50 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                             __syncwarp();
                             if (lane == 0) mbar_arrive(tempty_bar(buf));
                         }
+                        if (B_COL) {
+#pragma unroll
+                            for (int u = 0; u < EPI_LOADS; u++) {
+#pragma unroll
+                                for (int q4 = 0; q4 < 8; q4++) {
+                                    const uint4 b4 = ld_shared_v4(sbb + ((j + u) * 32 + 4 * q4) * 4);
+                                    const uint64_t s01 = mul_f32x2(pack_f32x2(b4.x, b4.y), sa2);
+                                    const uint64_t s23 = mul_f32x2(pack_f32x2(b4.z, b4.w), sa2);
+                                    fma_f32x2(acc[(j + u) * 16 + 2 * q4], pack_f32x2(r[u][4 * q4], r[u][4 * q4 + 1]),
+                                              s01);
+                                    fma_f32x2(acc[(j + u) * 16 + 2 * q4 + 1],
+                                              pack_f32x2(r[u][4 * q4 + 2], r[u][4 * q4 + 3]), s23);
+                                }
+                            }
+                            continue;
+                        }
 #pragma unroll
                         for (int u = 0; u < EPI_LOADS; u++) {
 #pragma unroll
                             for (int q = 0; q < 16; q++) {
 #if FP8BS_FFMA2
-                                fma_f32x2(acc[(j + u) * 16 + q], pack_f32x2(r[u][2 * q], r[u][2 * q + 1]), s2);
+                                fma_f32x2(acc[(j + u) * 16 + q], pack_f32x2(r[u][2 * q], r[u][2 * q + 1]),
+                                          j + u < 2 ? s2 : s2u);
 #else
+                                const float sc = j + u < 2 ? s : su;
                                 float2 a = unpack_f32x2(acc[(j + u) * 16 + q]);
-                                a.x = __fmaf_rn(__uint_as_float(r[u][2 * q]), s, a.x);
-                                a.y = __fmaf_rn(__uint_as_float(r[u][2 * q + 1]), s, a.y);
+                                a.x = __fmaf_rn(__uint_as_float(r[u][2 * q]), sc, a.x);
+                                a.y = __fmaf_rn(__uint_as_float(r[u][2 * q + 1]), sc, a.y);
                                 acc[(j + u) * 16 + q] = pack_f32x2(__float_as_uint(a.x), __float_as_uint(a.y));
 #endif
                             }
                         }
                     }
+                    if (B_COL) {
+                        mbar_arrive(bsf_empty(bslot));             // this thread read its scales
+                        if (++bslot == BSF_SLOTS) { bslot = 0; bph ^= 1u; }
+                    }
                     chunk++;
                 }
             }
             if (!ok) break;
-            store_tile(p, tmY, acc, tl, row, row_ok, col0, quarter, lane,
-                       sbase + OUT_OFF + (warp - EPI_WARP0) * OUT_SLAB);
+            ok = finish_tile<SWIGLU>(p, tmY, acc, tl, row, row_ok, col0, quarter, half, lane,
+                             sbase + OUT_OFF + (warp - EPI_WARP0) * OUT_SLAB, sbase + XCHG_OFF,
+                             xchg_bar(quarter), tile_i & 1u);
         }
         if (lane == 0) bulk_wait_group0();   // every store of this warp has landed
     }
@@ -519,11 +742,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 constexpr uint32_t MX_SF_STAGE = 3584;
 constexpr uint32_t MX_SF_OFF = STAGES * STAGE_BYTES;
 constexpr uint32_t MX_BAR_OFF = MX_SF_OFF + STAGES * MX_SF_STAGE;
-constexpr int MX_NUM_BARS = 3 * STAGES + 2 + 1;        // full, empty, sfready, tfull, tempty, done
+constexpr int MX_NUM_BARS = 3 * STAGES + 2 + 1 + 4;    // full, empty, sfready, tfull, tempty, done, xchg[4]
 constexpr uint32_t MX_TMEMSLOT_OFF = MX_BAR_OFF + MX_NUM_BARS * 8;
 constexpr uint32_t MX_TABLE_OFF = (MX_TMEMSLOT_OFF + 16 + 15) & ~15u;
 constexpr uint32_t MX_OUT_OFF = (MX_TABLE_OFF + 16 + 1023) & ~1023u;
-constexpr uint32_t MX_SMEM_BYTES = 1024 + MX_OUT_OFF + NUM_EPI_WARPS * OUT_SLAB;
+constexpr uint32_t MX_XCHG_OFF = MX_OUT_OFF + NUM_EPI_WARPS * OUT_SLAB;
+constexpr uint32_t MX_SMEM_BYTES = 1024 + MX_XCHG_OFF + XCHG_BYTES;
 static_assert(MX_SMEM_BYTES <= 232448, "shared memory budget (MX)");
 constexpr uint32_t MX_SF_TMEM = 256;                   // scale-factor ring after the accumulator
 constexpr int MX_SF_SLOTS = 4;                         // 16 columns each: SFA 4 + SFB 8
@@ -538,7 +762,7 @@ __device__ __forceinline__ uint32_t ue8m0_word(float s) {
     return ((__float_as_uint(s) >> 23) & 0xFFu) * 0x01010101u;
 }
 
-template <int UNUSED>
+template <bool SWIGLU, bool MX32>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     k_fp8_gemm_mx(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                   const __grid_constant__ CUtensorMap tmY, const __grid_constant__ CUtensorMap tmSA,
@@ -555,6 +779,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const uint32_t tfull_bar = bars + 8u * (3 * STAGES);
     const uint32_t tempty_bar = bars + 8u * (3 * STAGES + 1);
     const uint32_t done_bar = bars + 8u * (3 * STAGES + 2);
+    auto xchg_bar = [&](int q) { return bars + 8u * (3 * STAGES + 3 + q); };
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + MX_TMEMSLOT_OFF);
     int* s_off = reinterpret_cast<int*>(smem + MX_TABLE_OFF);
     int* s_slot = s_off + 2;
@@ -572,6 +797,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         mbar_init(tfull_bar, 1);
         mbar_init(tempty_bar, NUM_EPI_WARPS);
         mbar_init(done_bar, 1);
+        for (int q = 0; q < 4; q++) mbar_init(xchg_bar(q), 64);
         fence_mbar_init();
         fence_proxy_async_smem();
         s_off[0] = 0;
@@ -590,7 +816,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const int64_t nkb64 = nkb;
     const int64_t nrbB = (p.N + 127) / 128;
 
-    const bool sa_tma = p.a_gran == 0;                 // A's 1x128 scales arrive by TMA
+    // A's 1x128 fp32 scales, or (MXFP8) A's E8M0 words, arrive by TMA
+    const bool sa_tma = MX32 || p.a_gran == 0;
 
     if (warp < EPI_WARP0) {
       asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(MX_REGS_LOW));
@@ -609,7 +836,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     if (!wait_or_flag(empty_bar(stage), phase ^ 1u)) { ok = false; break; }
                     mbar_arrive_expect_tx(full_bar(stage), bytes);
                     tma_load_2d(sA + stage * A_STAGE, &tmA, kb * BK, tl.row0, full_bar(stage));
-                    tma_load_2d(sB + stage * B_STAGE, &tmB, kb * BK, tl.nt * BN, full_bar(stage));
+                    const uint32_t dB = sB + stage * B_STAGE;
+                    if (SWIGLU) {   // 64-row boxes: gate, up, gate + 64, up + 64
+                        const int gb = tl.nt * 128, ub = gb + static_cast<int>(p.swiglu_i);
+                        tma_load_2d(dB, &tmB, kb * BK, gb, full_bar(stage));
+                        tma_load_2d(dB + B_STAGE / 4, &tmB, kb * BK, ub, full_bar(stage));
+                        tma_load_2d(dB + B_STAGE / 2, &tmB, kb * BK, gb + 64, full_bar(stage));
+                        tma_load_2d(dB + 3 * (B_STAGE / 4), &tmB, kb * BK, ub + 64, full_bar(stage));
+                    } else {
+                        tma_load_2d(dB, &tmB, kb * BK, tl.nt * BN, full_bar(stage));
+                    }
                     if (sa_tma)   // 128 fp32 row scales of this K block (rows contiguous)
                         tma_load_2d(sSF + stage * MX_SF_STAGE, &tmSA, tl.row0, kb, full_bar(stage));
                     issued++;
@@ -642,11 +878,17 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     tmem_cp_32x128b_warpx4(tsfb, smem_desc_rows16(sf + 2560));
                     tmem_cp_32x128b_warpx4(tsfb + 4, smem_desc_rows16(sf + 3072));
                     const uint32_t aS = sA + stage * A_STAGE, bS = sB + stage * B_STAGE;
+                    // MXFP8: each K = 32 slice reads its own scale byte of the
+                    // words (A and B scale-factor ids = k4); otherwise the four
+                    // bytes are equal and id 0 serves every slice
 #pragma unroll
                     for (int k4 = 0; k4 < BK / 32; k4++)
                         mma_mxf8f6f4(tmem_base, smem_desc_sw128(aS + k4 * 32, 16, 1024),
-                                     smem_desc_sw128(bS + k4 * 32, 16, 1024), p.idesc, tsfa, tsfb,
-                                     (kb > 0 || k4 > 0) ? 1u : 0u);
+                                     smem_desc_sw128(bS + k4 * 32, 16, 1024),
+                                     MX32 ? (p.idesc | (static_cast<uint32_t>(k4) << 29) |
+                                             (static_cast<uint32_t>(k4) << 4))
+                                          : p.idesc,
+                                     tsfa, tsfb, (kb > 0 || k4 > 0) ? 1u : 0u);
                     issued_mma = true;
                     mma_commit(empty_bar(stage));
                     if (++stage == STAGES) { stage = 0; phase ^= 1u; }
@@ -659,15 +901,62 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 wait_bounded(done_bar, 0, DRAIN_LIMIT_NS);
             }
         }
-      } else if (warp == 2) {
+      } else if (MX32 && warp == 2) {
+        // ------ MXFP8 scale staging: A's words (by TMA) and B's words (from a
+        // register ring, 4 K blocks ahead) into the tcgen05.cp layouts
+        int stage = 0;
+        uint32_t phase = 0;
+        bool ok = true;
+        const uint32_t* sbw = reinterpret_cast<const uint32_t*>(p.sb);   // [K/128][N] words
+        for (int t = blockIdx.x; ok && t < total_tiles; t += gridDim.x) {
+            const Tile tl = decode_tile(t, total_slots, p.tiles_n, 1, s_slot, s_off);
+            const int64_t n0 = static_cast<int64_t>(tl.nt) * BN;
+            uint32_t bw[4][8];
+            auto load_bw = [&](int kbi, uint32_t (&d)[8]) {
+#pragma unroll
+                for (int c = 0; c < 8; c++) {
+                    const int64_t n = n0 + 32 * c + lane;
+                    d[c] = (kbi < nkb && n < p.N) ? __ldg(sbw + static_cast<int64_t>(kbi) * p.N + n) : 0u;
+                }
+            };
+#pragma unroll
+            for (int i = 0; i < 4; i++) load_bw(i, bw[i]);
+            for (int kb0 = 0; ok && kb0 < nkb; kb0 += 4) {
+#pragma unroll
+                for (int i = 0; i < 4; i++) {
+                    const int kb = kb0 + i;
+                    if (kb >= nkb) break;
+                    ok = __all_sync(0xFFFFFFFFu, wait_or_flag(full_bar(stage), phase));
+                    if (!ok) break;
+                    const uint32_t sf = sSF + stage * MX_SF_STAGE;
+#pragma unroll
+                    for (int r = 0; r < 4; r++) {
+                        const uint32_t w = __float_as_uint(ld_shared_f32(sf + (32 * r + lane) * 4));
+                        st_shared_v4(sf + 512 + (32 * r + lane) * 16, w, w, w, w);
+                    }
+                    // word c of row `lane` feeds column 32 c + lane (+128 for the second copy)
+                    st_shared_v4(sf + 2560 + lane * 16, bw[i][0], bw[i][1], bw[i][2], bw[i][3]);
+                    st_shared_v4(sf + 3072 + lane * 16, bw[i][4], bw[i][5], bw[i][6], bw[i][7]);
+                    load_bw(kb + 4, bw[i]);
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(sfready_bar(stage));
+                    if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+                }
+            }
+        }
+      } else if (!MX32 && warp == 2) {
         // ---------------- scale converter: UE8M0 words of each landed stage
         int stage = 0;
         uint32_t phase = 0;
         bool ok = true;
         for (int t = blockIdx.x; ok && t < total_tiles; t += gridDim.x) {
             const Tile tl = decode_tile(t, total_slots, p.tiles_n, 1, s_slot, s_off);
-            const int64_t nb0 = min(static_cast<int64_t>(2 * tl.nt), nrbB - 1);
-            const int64_t nb1 = min(static_cast<int64_t>(2 * tl.nt + 1), nrbB - 1);
+            // weight row-blocks: columns 0-127 / 128-255 of the tile; with
+            // SwiGLU the gate (nb0) and up (nb1) blocks of 64-column runs
+            const int64_t nb0 = SWIGLU ? tl.nt : min(static_cast<int64_t>(2 * tl.nt), nrbB - 1);
+            const int64_t nb1 = SWIGLU ? p.swiglu_i / 128 + tl.nt
+                                         : min(static_cast<int64_t>(2 * tl.nt + 1), nrbB - 1);
             const int64_t arow = min(static_cast<int64_t>(tl.row0), p.a_rows - 1);
             // lane-uniform scale values of K block kb in register slot kb % MPF
             float ru[MPF], rb0[MPF], rb1[MPF];
@@ -693,9 +982,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         const uint32_t w = ue8m0_word(v);
                         st_shared_v4(sf + 512 + (32 * r + lane) * 16, w, w, w, w);
                     }
+                    // word c of row `lane` feeds column 32 c + lane (+128 for the second copy)
                     const uint32_t w0 = ue8m0_word(rb0[i]), w1 = ue8m0_word(rb1[i]);
-                    st_shared_v4(sf + 2560 + lane * 16, w0, w0, w0, w0);
-                    st_shared_v4(sf + 3072 + lane * 16, w1, w1, w1, w1);
+                    if (SWIGLU) {
+                        st_shared_v4(sf + 2560 + lane * 16, w0, w0, w1, w1);
+                        st_shared_v4(sf + 3072 + lane * 16, w0, w0, w1, w1);
+                    } else {
+                        st_shared_v4(sf + 2560 + lane * 16, w0, w0, w0, w0);
+                        st_shared_v4(sf + 3072 + lane * 16, w1, w1, w1, w1);
+                    }
                     if (kb + MPF < nkb) load_sf(kb + MPF, ru[i], rb0[i], rb1[i]);
                     fence_proxy_async_smem();
                     __syncwarp();
@@ -736,8 +1031,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(tempty_bar);       // accumulator free for the next tile
-            store_tile(p, tmY, acc, tl, row, row_ok, col0, quarter, lane,
-                       sbase + MX_OUT_OFF + (warp - EPI_WARP0) * OUT_SLAB);
+            ok = finish_tile<SWIGLU>(p, tmY, acc, tl, row, row_ok, col0, quarter, half, lane,
+                             sbase + MX_OUT_OFF + (warp - EPI_WARP0) * OUT_SLAB, sbase + MX_XCHG_OFF,
+                             xchg_bar(quarter), tile_i & 1u);
         }
         if (lane == 0) bulk_wait_group0();
     }
@@ -765,7 +1061,20 @@ __global__ void k_wait_selftest(uint64_t limit_ns, int* out) {
     }
 }
 
+__global__ void k_fill_f32(float* p, int64_t n, float v) {
+    for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n;
+         i += static_cast<int64_t>(gridDim.x) * blockDim.x)
+        p[i] = v;
+}
+
 }  // namespace
+
+cudaError_t launch_fill_f32(float* p, int64_t n, float v, cudaStream_t st) {
+    if (n <= 0) return cudaSuccess;
+    const int64_t blocks = (n + 255) / 256;
+    k_fill_f32<<<static_cast<unsigned>(blocks < 1024 ? blocks : 1024), 256, 0, st>>>(p, n, v);
+    return cudaGetLastError();
+}
 
 cudaError_t launch_wait_selftest(uint64_t limit_ns, int* out, cudaStream_t st) {
     k_wait_selftest<<<1, 32, 0, st>>>(limit_ns, out);
@@ -805,7 +1114,7 @@ uint32_t make_idesc_mx(int a_fmt, int b_fmt, int n) {
 
 cudaError_t launch_fp8_gemm_mx(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmY,
                                const CUtensorMap& tmSA, const GemmParams& p, int grid, cudaStream_t st) {
-    auto k = k_fp8_gemm_mx<0>;
+    auto k = p.mx32 ? k_fp8_gemm_mx<false, true> : p.swiglu ? k_fp8_gemm_mx<true, false> : k_fp8_gemm_mx<false, false>;
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, MX_SMEM_BYTES);
     if (e != cudaSuccess) return e;
     k<<<grid, NUM_THREADS, MX_SMEM_BYTES, st>>>(tmA, tmB, tmY, tmSA, p);
@@ -818,8 +1127,12 @@ int gemm_tile_m() { return BM; }
 
 cudaError_t launch_fp8_gemm(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmY,
                             const GemmParams& p, bool a_mn, bool b_mn, int grid, cudaStream_t st) {
-    auto k = a_mn ? (b_mn ? k_fp8_gemm<true, true> : k_fp8_gemm<true, false>)
-                  : (b_mn ? k_fp8_gemm<false, true> : k_fp8_gemm<false, false>);
+    // SwiGLU runs only on K-major operands (the host checks it)
+    // (per-column B scales: K-major operands only; the host checks it)
+    auto k = p.swiglu ? k_fp8_gemm<false, false, true, false>
+             : p.b_gran == 0 ? k_fp8_gemm<false, false, false, true>
+             : a_mn ? (b_mn ? k_fp8_gemm<true, true, false, false> : k_fp8_gemm<true, false, false, false>)
+                    : (b_mn ? k_fp8_gemm<false, true, false, false> : k_fp8_gemm<false, false, false, false>);
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
     if (e != cudaSuccess) return e;
     k<<<grid, NUM_THREADS, SMEM_BYTES, st>>>(tmA, tmB, tmY, p);

@@ -29,6 +29,18 @@ struct GemmParams {
     int32_t out_bf16;
     int32_t tma_store;        // 1: tmY describes Y (box 32 rows x 64 B, 64-B swizzle)
     uint32_t idesc;
+    // Quantized output: Y holds 8-bit codes [rows][n_out] and sq its 1x128
+    // scales [n_out/128][a_rows] (the next linear's activation operand).
+    int32_t out_q, q_fmt, q_mode;
+    float* sq;
+    int64_t n_out;            // columns of Y (N, or N/2 with SwiGLU)
+    // SwiGLU: B's rows [0, swiglu_i) are gate rows and [swiglu_i, 2 swiglu_i)
+    // the matching up rows (per group); Y = silu(gate) * up.
+    int32_t swiglu;
+    int64_t swiglu_i;
+    // MXFP8 operands (both): scale tables of 32-bit E8M0 words [K/128][rows],
+    // byte j = scale of the K elements 32 j .. 32 j + 31 of the block
+    int32_t mx32;
 };
 
 uint32_t gemm_smem_bytes();
@@ -43,5 +55,6 @@ cudaError_t launch_fp8_gemm_mx(const CUtensorMap& tmA, const CUtensorMap& tmB, c
                                const CUtensorMap& tmSA, const GemmParams& p, int grid, cudaStream_t st);
 cudaError_t read_and_clear_status(int* status);
 cudaError_t launch_wait_selftest(uint64_t limit_ns, int* out, cudaStream_t st);
+cudaError_t launch_fill_f32(float* p, int64_t n, float v, cudaStream_t st);
 
 }  // namespace fp8bs

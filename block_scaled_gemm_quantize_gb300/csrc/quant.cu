@@ -2,6 +2,8 @@
 //
 //   k_quant_1x128     activations, one scale per 1x128 row tile
 //   k_quant_128x128   weights, one scale per 128x128 tile
+//   k_quant_colwise   1x128 tiles along rows, as a transposed copy (+ row-wise)
+//   k_quant_mx        MXFP8: 1x32 blocks, E8M0 power-of-two scales (floor rule)
 //   k_quant_tensor    per-tensor delayed scaling (scale in use + amax)
 //   k_amax_history    delayed-scaling state update
 //
@@ -19,59 +21,10 @@
 #include <cstdint>
 #include <cstring>
 
+#include "fp8_math.cuh"
 #include "quant_kernels.h"
 
 namespace fp8bs {
-
-template <int FMT>
-struct Fmt;
-template <>
-struct Fmt<0> {  // E4M3 (FN)
-    static constexpr float kMax = 448.0f;
-    static constexpr int kEmax = 8;  // 448 = 1.75 * 2^8
-};
-template <>
-struct Fmt<1> {  // E5M2
-    static constexpr float kMax = 57344.0f;
-    static constexpr int kEmax = 15;  // 57344 = 1.75 * 2^15
-};
-
-// Dequantization scale of a block (mode 0: fp32 amax/fmax, mode 1: power of
-// two rounded up so the block maximum never saturates).
-template <int FMT, int MODE>
-__device__ __forceinline__ float block_scale(float amax) {
-    if (!(amax > 0.0f)) return 1.0f;
-    if (MODE == 0) {
-        float s = __fdiv_rn(amax, Fmt<FMT>::kMax);
-        return fmaxf(s, 0x1p-126f);
-    }
-    // amax = (1 + f) 2^E.  With fmax = 1.75 * 2^Emax the smallest e with
-    // amax <= fmax 2^e is E - Emax, plus one when 1 + f > 1.75 (fraction
-    // field above 0x600000).  Subnormal amax -> -126; infinity -> 127.
-    const uint32_t b = __float_as_uint(amax);
-    const int ef = static_cast<int>(b >> 23);
-    int e;
-    if (ef == 0) {
-        e = -126;
-    } else if (ef == 255) {
-        e = 127;
-    } else {
-        e = (ef - 127) - Fmt<FMT>::kEmax + ((b & 0x7FFFFFu) > 0x600000u ? 1 : 0);
-        e = max(-126, min(127, e));
-    }
-    return __uint_as_float(static_cast<uint32_t>(e + 127) << 23);
-}
-
-// Two fp32 values -> two 8-bit codes (lo in bits 0-7, hi in bits 8-15).
-template <int FMT>
-__device__ __forceinline__ uint32_t cvt2(float lo, float hi) {
-    uint16_t r;
-    if (FMT == 0)
-        asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
-    else
-        asm("cvt.rn.satfinite.e5m2x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
-    return r;
-}
 
 __device__ __forceinline__ uint4 ld_stream_v4(const void* p) {
     uint4 v;
@@ -207,6 +160,139 @@ __global__ void __launch_bounds__(256, FP8BS_Q128_MINB) k_quant_128x128(const ui
     if (threadIdx.x == 0) scales[rb * nkb + kb] = s;
 }
 
+// ---------------------------------------------------------------- MXFP8
+// Microscaling FP8: one E8M0 scale per 32 consecutive elements of a row.
+// Same layout of work as k_quant_1x128 (a half-warp per 128 elements); each
+// group of 4 lanes holds one 32-element block, so the block amax takes two
+// shuffle steps.  Scales: one 32-bit word per (K block of 128, row), byte j =
+// code of sub-block j -- the word the block-scaled MMA selects bytes from.
+template <int FMT, int U>
+__global__ void __launch_bounds__(256) k_quant_mx(const uint16_t* __restrict__ x, int64_t rows,
+                                                 int64_t ldx, uint8_t* __restrict__ q, int64_t ldq,
+                                                 uint32_t* __restrict__ scales) {
+    const int l16 = threadIdx.x & 15;
+    const int hw = threadIdx.x >> 4;
+    const int base = threadIdx.x & 16;      // first lane of this half-warp
+    const int64_t kb = blockIdx.y;
+    const int64_t r0 = static_cast<int64_t>(blockIdx.x) * (16 * U) + hw;
+    const uint16_t* xk = x + kb * 128 + l16 * 8;
+    uint4 v[U];
+#pragma unroll
+    for (int i = 0; i < U; i++) {
+        const int64_t r = r0 + 16 * i;
+        v[i] = make_uint4(0, 0, 0, 0);
+        if (r < rows) v[i] = ld_stream_v4(xk + r * ldx);
+    }
+#pragma unroll
+    for (int i = 0; i < U; i++) {
+        const int64_t r = r0 + 16 * i;
+        float f[8];
+        unpack8(v[i], f);
+        float m = amax8(f);
+        m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, 1));
+        m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, 2));
+        uint32_t code;
+        float mult;
+        mx_scale<FMT>(m, code, mult);
+        const uint32_t c0 = __shfl_sync(0xFFFFFFFFu, code, base);
+        const uint32_t c1 = __shfl_sync(0xFFFFFFFFu, code, base + 4);
+        const uint32_t c2 = __shfl_sync(0xFFFFFFFFu, code, base + 8);
+        const uint32_t c3 = __shfl_sync(0xFFFFFFFFu, code, base + 12);
+        if (r < rows) {
+            uint32_t lo, hi;
+            quant8<FMT>(f, mult, lo, hi);
+            st_v2(q + r * ldq + kb * 128 + l16 * 8, lo, hi);
+            if (l16 == 0) scales[kb * rows + r] = c0 | (c1 << 8) | (c2 << 16) | (c3 << 24);
+        }
+    }
+}
+
+// ------------------------------------------------------ column-wise 1x128
+// The backward products that contract over tokens (wgrad: dW = dY^T X) need
+// 1x128 blocks along the ROWS of dY and X: one scale per 128 consecutive rows
+// of a column, kept as a transposed copy qt [cols][rows] (K-major for the
+// product) with scales [rows/128][cols].  One CTA per 128x128 tile reads x
+// once: the row-wise copy (optional: the forward operand, or dY's dgrad
+// operand) comes from registers as in k_quant_1x128; the column-wise copy
+// from the tile staged in shared memory (thread = one column, one half of
+// the rows; two passes, amax then codes); its codes are staged again in
+// 16-byte chunks XOR-swizzled by column so that both copies leave in full
+// 128-byte rows.
+#ifndef FP8BS_QCOL_MINB
+#define FP8BS_QCOL_MINB 4
+#endif
+template <int FMT, int MODE, bool ROWWISE>
+__global__ void __launch_bounds__(256, FP8BS_QCOL_MINB)
+    k_quant_colwise(const uint16_t* __restrict__ x, int64_t rows, int64_t cols, int64_t ldx,
+                    uint8_t* __restrict__ qt, int64_t ldqt, float* __restrict__ sqt,
+                    uint8_t* __restrict__ q, int64_t ldq, float* __restrict__ sq) {
+    __shared__ __align__(16) uint16_t tile[128 * 128];    // bf16 tile, 256-byte rows
+    __shared__ __align__(16) uint8_t tq[128 * 128];       // transposed codes, swizzled chunks
+    float (*cmax)[128] = reinterpret_cast<float (*)[128]>(tq);   // column amax halves, used before tq
+    const int64_t cb = blockIdx.x, rb = blockIdx.y;
+    const int t = threadIdx.x;
+    const int chunk = t & 15, r0 = t >> 4;
+    const uint16_t* xt = x + (rb * 128) * ldx + cb * 128 + chunk * 8;
+    uint4 v[8];
+#pragma unroll
+    for (int i = 0; i < 8; i++) v[i] = ld_stream_v4(xt + static_cast<int64_t>(r0 + 16 * i) * ldx);
+#pragma unroll
+    for (int i = 0; i < 8; i++) {
+        const int r = r0 + 16 * i;
+        *reinterpret_cast<uint4*>(&tile[r * 128 + chunk * 8]) = v[i];
+        if (ROWWISE) {
+            float f[8];
+            unpack8(v[i], f);
+            float m = amax8(f);
+#pragma unroll
+            for (int o = 8; o >= 1; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
+            const float s = block_scale<FMT, MODE>(m);
+            uint32_t lo, hi;
+            quant8<FMT>(f, __frcp_rn(s), lo, hi);
+            const int64_t row = rb * 128 + r;
+            st_v2(q + row * ldq + cb * 128 + chunk * 8, lo, hi);
+            if (chunk == 0) sq[cb * rows + row] = s;
+        }
+    }
+    __syncthreads();
+    // column pass: thread = column c, rows 64 h .. 64 h + 63
+    const int c = t & 127, h = t >> 7;
+    const uint16_t* col = tile + (64 * h) * 128 + c;
+    float m = 0.0f;
+#pragma unroll 16
+    for (int j = 0; j < 64; j++) m = fmaxf(m, fabsf(__uint_as_float(static_cast<uint32_t>(col[j * 128]) << 16)));
+    cmax[h][c] = m;
+    __syncthreads();
+    m = fmaxf(cmax[0][c], cmax[1][c]);
+    __syncthreads();                              // cmax shares its bytes with tq
+    const float s = block_scale<FMT, MODE>(m);
+    const float rc = __frcp_rn(s);
+    if (h == 0) sqt[rb * cols + cb * 128 + c] = s;
+#pragma unroll
+    for (int k = 0; k < 4; k++) {                 // 16 codes (rows 64 h + 16 k ..) per chunk
+        uint32_t w[4];
+#pragma unroll
+        for (int i = 0; i < 4; i++) {
+            float f[4];
+#pragma unroll
+            for (int e = 0; e < 4; e++)
+                f[e] = __fmul_rn(__uint_as_float(static_cast<uint32_t>(col[(16 * k + 4 * i + e) * 128]) << 16), rc);
+            w[i] = cvt2<FMT>(f[0], f[1]) | (cvt2<FMT>(f[2], f[3]) << 16);
+        }
+        const int ch = (4 * h + k) ^ (c & 7);
+        *reinterpret_cast<uint4*>(&tq[c * 128 + ch * 16]) = make_uint4(w[0], w[1], w[2], w[3]);
+    }
+    __syncthreads();
+    // write-out: 128 rows of qt x 8 chunks, 8 consecutive threads per 128-byte row
+#pragma unroll
+    for (int j = 0; j < 4; j++) {
+        const int kk = t + 256 * j;
+        const int c2 = kk >> 3, ch2 = kk & 7;
+        const uint4 val = *reinterpret_cast<const uint4*>(&tq[c2 * 128 + ((ch2 ^ (c2 & 7)) * 16)]);
+        *reinterpret_cast<uint4*>(qt + (cb * 128 + c2) * ldqt + rb * 128 + ch2 * 16) = val;
+    }
+}
+
 // ------------------------------------------------------- per-tensor delayed
 // Quantize with the scale in use and reduce this tensor's amax: each thread
 // handles U 16-byte vectors (grid-contiguous per iteration), CTA reduction,
@@ -324,6 +410,33 @@ cudaError_t launch_quant_128x128(const uint16_t* w, int64_t rows, int64_t cols, 
     auto k = fmt == 0 ? (mode == 0 ? k_quant_128x128<0, 0> : k_quant_128x128<0, 1>)
                       : (mode == 0 ? k_quant_128x128<1, 0> : k_quant_128x128<1, 1>);
     k<<<static_cast<unsigned>(grid), 256, 0, st>>>(w, rows, ldw, nkb, q, ldq, scales);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_quant_mx(const uint16_t* x, int64_t rows, int64_t cols, int64_t ldx, int fmt,
+                            uint8_t* q, int64_t ldq, uint32_t* scales, cudaStream_t st) {
+    const int64_t gx = (rows + 16 * kU1 - 1) / (16 * kU1), gy = cols / 128;
+    if (gx > 0x7FFFFFFF || gy > 65535) return cudaErrorInvalidValue;
+    auto k = fmt == 0 ? k_quant_mx<0, kU1> : k_quant_mx<1, kU1>;
+    k<<<dim3(static_cast<unsigned>(gx), static_cast<unsigned>(gy)), 256, 0, st>>>(x, rows, ldx, q, ldq, scales);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_quant_colwise(const uint16_t* x, int64_t rows, int64_t cols, int64_t ldx,
+                                int fmt, int mode, uint8_t* qt, int64_t ldqt, float* sqt,
+                                uint8_t* q, int64_t ldq, float* sq, cudaStream_t st) {
+    const int64_t gx = cols / 128, gy = rows / 128;
+    if (gx > 0x7FFFFFFF || gy > 65535) return cudaErrorInvalidValue;
+    const bool rw = q != nullptr;
+    using K = void (*)(const uint16_t*, int64_t, int64_t, int64_t, uint8_t*, int64_t, float*, uint8_t*,
+                       int64_t, float*);
+    K k;
+    if (fmt == 0) k = mode == 0 ? (rw ? k_quant_colwise<0, 0, true> : k_quant_colwise<0, 0, false>)
+                                : (rw ? k_quant_colwise<0, 1, true> : k_quant_colwise<0, 1, false>);
+    else k = mode == 0 ? (rw ? k_quant_colwise<1, 0, true> : k_quant_colwise<1, 0, false>)
+                       : (rw ? k_quant_colwise<1, 1, true> : k_quant_colwise<1, 1, false>);
+    k<<<dim3(static_cast<unsigned>(gx), static_cast<unsigned>(gy)), 256, 0, st>>>(x, rows, cols, ldx, qt, ldqt,
+                                                                                 sqt, q, ldq, sq);
     return cudaGetLastError();
 }
 

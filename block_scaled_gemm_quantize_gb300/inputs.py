@@ -84,3 +84,25 @@ LLAMA31_8B_MLP_BWD = dict(
 QWEN3_30B_MOE = dict(
     name="qwen3-30b-a3b-moe", tokens=8192, hidden=2048, experts=128, topk=8, zipf_a=1.1,
     gate_up_n=1536, down_k=768)
+
+# An MLP block as a chain of two FP8 linears whose intermediate never leaves
+# FP8: gate/up product with a SwiGLU + 1x128-quantizing epilogue, then the
+# down product on those codes (dense Llama-3.1-8B MLP; Qwen3-30B-A3B experts).
+LLAMA31_8B_MLP_FUSED = dict(name="llama3.1-8b-mlp-fused", M=8192, hidden=4096,
+                            intermediate=14336, scale_mode="fp32")
+QWEN3_30B_MOE_FUSED = dict(name="qwen3-30b-a3b-moe-fused", tokens=8192, hidden=2048, experts=128,
+                           topk=8, zipf_a=1.1, intermediate=768, scale_mode="fp32")
+
+# The same MLP backward under the block recipe: dY and X quantized per 1x128
+# tile along the contraction of each product (row-wise for dgrad, column-wise
+# transposed copies for wgrad), W per 128x128 tile, E4M3 throughout.
+LLAMA31_8B_MLP_BWD_BLOCK = dict(
+    name="llama3.1-8b-mlp-bwd-blockwise", M=8192, scale_mode="fp32",
+    linears=[("up", 14336, 4096), ("down", 4096, 14336)], dy_scale=1e-3, dy_nu=3.0)
+
+# The Llama-3.1-8B fprop linears in MXFP8 (1x32 blocks, E8M0 scales) on
+# both operands, the block-scaling format Blackwell's tensor cores apply.
+LLAMA31_8B_FPROP_MX = dict(
+    name="llama3.1-8b-fprop-mxfp8", M=8192, scale_mode="mx",
+    linears=[("qkv", 6144, 4096), ("o", 4096, 4096), ("gate_up", 28672, 4096),
+             ("down", 4096, 14336)])

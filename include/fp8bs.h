@@ -57,7 +57,9 @@ enum fp8bs_status {
 enum fp8bs_format { FP8BS_E4M3 = 0, FP8BS_E5M2 = 1 };
 enum fp8bs_scale_mode { FP8BS_SCALE_FP32 = 0, FP8BS_SCALE_POW2 = 1 };
 enum fp8bs_out_dtype { FP8BS_OUT_F32 = 0, FP8BS_OUT_BF16 = 1 };
-enum fp8bs_granularity { FP8BS_GRAN_1x128 = 0, FP8BS_GRAN_128x128 = 1, FP8BS_GRAN_TENSOR = 2 };
+enum fp8bs_granularity { FP8BS_GRAN_1x128 = 0, FP8BS_GRAN_128x128 = 1, FP8BS_GRAN_TENSOR = 2,
+                         FP8BS_GRAN_1x32 = 3 /* MXFP8 */ };
+enum fp8bs_epilogue { FP8BS_EPI_NONE = 0, FP8BS_EPI_SWIGLU = 1 };
 
 /* ------------------------------------------------------------ quantizers */
 
@@ -93,6 +95,54 @@ int fp8_quantize_1x128(const void* x, int64_t rows, int64_t cols, int64_t ld_x,
 int fp8_quantize_128x128(const void* w, int64_t rows, int64_t cols, int64_t ld_w,
                          int32_t fmt, int32_t mode,
                          uint8_t* q, int64_t ld_q, float* scales, fp8bs_stream_t stream);
+
+/*
+ * MXFP8 (microscaling FP8) quantizer: one power-of-two scale per 32
+ * consecutive elements of a row.  The introl page names MXFP8 as Blackwell's
+ * hardware block scaling ("Requisitos de hardware para entrenamiento FP8";
+ * "Escalado por bloque (MXFP8)" in "Estrategias de escalado y estabilidad";
+ * "Blackwell MXFP8 y NVFP4") without the block size or the scale rule; this
+ * follows the open microscaling format the name refers to:
+ *   per 32-element block: e = floor(log2(amax)) - Emax (Emax = 8 for E4M3,
+ *   15 for E5M2), clamped to [-127, 127] (amax == 0 or subnormal: -127);
+ *   code = e + 127 (E8M0); elements q = enc(x * 2^-e), rounded to nearest
+ *   even and saturated (the block maximum lies in [2^Emax, 2^(Emax+1)) and
+ *   may saturate); a non-finite amax gives code 255 (NaN) and NaN elements.
+ *   x      [rows][ld_x] bf16;  q [rows][ld_q] codes (output);
+ *   scales [cols/128][rows][4] uint8 codes (output): byte j of entry
+ *          (kb, r) is the scale of columns 128 kb + 32 j .. 128 kb + 32 j + 31
+ *          -- one 32-bit word per (128-column block, row), the rows of a
+ *          block contiguous, as the block-scaled product reads them.
+ * Errors as fp8_quantize_1x128 (scales 4-byte aligned).
+ */
+int fp8_quantize_mx(const void* x, int64_t rows, int64_t cols, int64_t ld_x, int32_t fmt,
+                    uint8_t* q, int64_t ld_q, uint8_t* scales, fp8bs_stream_t stream);
+
+/*
+ * Column-wise 1x128 quantizer for the backward products.  The block recipe
+ * ("El avance tecnico": 1x128 activation tiles) applied to products that
+ * contract over the token dimension (wgrad dW = dY^T X) needs tiles of 128
+ * consecutive ROWS of one column of dY and of X.  This call quantizes x with
+ * such 128x1 tiles and writes the result transposed, so the product reads a
+ * K-major operand with the ordinary 1x128 layout; from the same read of x it
+ * can also write the row-wise 1x128 copy (dY's dgrad operand, or X's
+ * forward operand).
+ *   x        [rows][ld_x] bf16.
+ *   qt       [cols][ld_qt] codes: qt[c][r] = enc(x[r][c] * (1/st)), st the
+ *            scale of tile (r/128, c) -- the fp8_quantize_1x128 rules
+ *            applied to x^T.
+ *   scales_t [rows/128][cols] fp32 (the 1x128 table of the [cols][rows]
+ *            operand qt).
+ *   q, scales: the row-wise copy exactly as fp8_quantize_1x128 writes it
+ *            (ld_q), or both NULL to skip it.
+ * Errors: INVALID_ARG (nulls, one of q/scales null, ld too small, bad enum),
+ * UNSUPPORTED (rows % 128 or cols % 128), MISALIGNED (x, qt, q 16-byte
+ * aligned with 16-byte row pitches, scale tables 4-byte aligned).
+ */
+int fp8_quantize_1x128_colwise(const void* x, int64_t rows, int64_t cols, int64_t ld_x,
+                               int32_t fmt, int32_t mode,
+                               uint8_t* qt, int64_t ld_qt, float* scales_t,
+                               uint8_t* q, int64_t ld_q, float* scales, fp8bs_stream_t stream);
 
 /*
  * Per-tensor delayed-scaling quantizer ("Escalado diferido", introl.com
@@ -137,11 +187,19 @@ int fp8_amax_history_update(float* history, int32_t* head, int32_t history_len,
  *                   backward products (dgrad reads W and wgrad reads dY and X
  *                   across their stored rows).
  * Scale tables (fp32), in the orientation of the stored matrix:
- *   GRAN_1x128   (transposed = 0 only, A only): [K/128][rows]
+ *   GRAN_1x128   (transposed = 0 only): [K/128][rows].  On B (one scale per
+ *                128 K-elements of each column of the product) it is the
+ *                wgrad operand of the block recipe's backward pass (see
+ *                fp8_quantize_1x128_colwise); not in grouped products.
  *   GRAN_128x128, transposed = 0: [ceil(rows/128)][K/128]
  *   GRAN_128x128, transposed = 1: [K/128][ceil(rows/128)]
  *   GRAN_TENSOR: one value.
  */
+/*   GRAN_1x32 (MXFP8; transposed = 0, both operands, not grouped): the
+ *                uint8 table of fp8_quantize_mx, [K/128][rows][4] codes,
+ *                passed through the `scales` pointer (cast); the tensor core
+ *                applies each 32-element block's scale.  A's table needs
+ *                rows % 4 == 0 and 16-byte alignment. */
 typedef struct {
     const uint8_t* data;
     int64_t ld;            /* elements (= bytes) between stored rows */
@@ -165,8 +223,8 @@ typedef struct {
  *   [2^-126, 2^127] (from the POW2 quantizers); the result is the same sum.
  *   Y [M][ld_y], fp32 or bf16 (round to nearest even), written, not
  *   accumulated.
- * Errors: INVALID_ARG, UNSUPPORTED (K % 128, N % 8, GRAN_1x128 on B or on a
- * transposed operand), MISALIGNED (data 16-byte aligned, ld % 16, Y 16-byte
+ * Errors: INVALID_ARG, UNSUPPORTED (K % 128, N % 8, GRAN_1x128 on a
+ * transposed operand, GRAN_1x128 B with a transposed A), MISALIGNED (data 16-byte aligned, ld % 16, Y 16-byte
  * aligned with ld_y * element size a multiple of 16).
  */
 int fp8_block_gemm(int64_t M, int64_t N, int64_t K,
@@ -187,7 +245,8 @@ int fp8_block_gemm(int64_t M, int64_t N, int64_t K,
  *   B               [G][N][K] stored as one [G*N][ld] matrix, transposed = 0,
  *                   GRAN_128x128 (scales [G][ceil(N/128)][K/128]) or
  *                   GRAN_TENSOR (one value for all groups).
- *   Y               [a_rows][ld_y]; rows outside every group are not written.
+ *   Y               [a_rows][ld_y]; rows outside every group are not written
+ *                   (K == 0: every row of Y is zeroed).
  * Errors as fp8_block_gemm; num_groups in [1, 1024].
  */
 int fp8_grouped_block_gemm(int32_t num_groups, const int32_t* row_offsets, int64_t a_rows,
@@ -195,6 +254,53 @@ int fp8_grouped_block_gemm(int32_t num_groups, const int32_t* row_offsets, int64
                            const fp8bs_operand* A, const fp8bs_operand* B,
                            int32_t mode, void* Y, int64_t ld_y, int32_t out_dtype,
                            fp8bs_stream_t stream);
+
+/*
+ * Product with a quantized output: the GEMM epilogue emits the next linear
+ * layer's FP8 activation operand directly, with no float round trip through
+ * memory and no separate quantization pass (the quantization-kernel overhead
+ * that hotbookzone.com "Ganancias de rendimiento en el mundo real" names as
+ * part of the gap between the theoretical 2x and the 15-25 % measured on
+ * linear layers).
+ *   epilogue = FP8BS_EPI_NONE:   Z = Y (as fp8_block_gemm computes it, fp32).
+ *   epilogue = FP8BS_EPI_SWIGLU: B's rows [0, N/2) are gate rows and
+ *     [N/2, N) the matching up rows; Z[m][j] = silu(Y[m][j]) * Y[m][N/2 + j]
+ *     with silu(g) = g / (1 + e^-g), evaluated in fp32 (the non-linear
+ *     function stays out of FP8 math, as "El avance tecnico" keeps
+ *     non-linear layers in higher precision); Z has N/2 columns.
+ * Z is then quantized exactly as fp8_quantize_1x128 quantizes its input,
+ * with the fp32 values of Z in place of bf16 ones:
+ *   Q        [M][ld_q] codes of Z (format q_fmt), Z's columns;
+ *   q_scales [cols(Z)/128][M] fp32 (scale mode q_mode): the 1x128 operand
+ *            layout, ready to be the A operand of the next product.
+ * The fp32 values of Z are those of the float-output product (same
+ * accumulation), so they match the exact sum within fp8_block_gemm's
+ * tolerance; codes and scales follow from those values.
+ * K == 0: Q = 0 and every scale 1.
+ * Errors as fp8_block_gemm, plus UNSUPPORTED (N % 128, or N % 256 with
+ * SwiGLU; SwiGLU with a transposed operand), INVALID_ARG (bad epilogue,
+ * q_fmt or q_mode, null Q or q_scales), MISALIGNED (Q 16-byte aligned,
+ * ld_q % 16, q_scales 4-byte aligned).
+ */
+int fp8_block_gemm_quant(int64_t M, int64_t N, int64_t K,
+                         const fp8bs_operand* A, const fp8bs_operand* B, int32_t mode,
+                         int32_t epilogue, int32_t q_fmt, int32_t q_mode,
+                         uint8_t* Q, int64_t ld_q, float* q_scales, fp8bs_stream_t stream);
+
+/*
+ * Grouped form of fp8_block_gemm_quant (mixture-of-experts expert layers:
+ * the gate/up product with SwiGLU feeds the down product's FP8 operand).
+ * Operands, groups and offsets as fp8_grouped_block_gemm; with SwiGLU each
+ * expert's B block [N][K] holds its N/2 gate rows then its N/2 up rows.
+ *   Q [a_rows][ld_q], q_scales [cols(Z)/128][a_rows]; rows outside every
+ *   group are not written (K == 0: every row is written, Q = 0, scales 1).
+ * Errors as fp8_block_gemm_quant and fp8_grouped_block_gemm.
+ */
+int fp8_grouped_block_gemm_quant(int32_t num_groups, const int32_t* row_offsets, int64_t a_rows,
+                                 int64_t N, int64_t K,
+                                 const fp8bs_operand* A, const fp8bs_operand* B, int32_t mode,
+                                 int32_t epilogue, int32_t q_fmt, int32_t q_mode,
+                                 uint8_t* Q, int64_t ld_q, float* q_scales, fp8bs_stream_t stream);
 
 /* ------------------------------------------------------------ diagnostics */
 

@@ -24,7 +24,7 @@ import numpy as np
 
 E4M3, E5M2 = 0, 1
 SCALE_FP32, SCALE_POW2 = 0, 1
-GRAN_1x128, GRAN_128x128, GRAN_TENSOR = 0, 1, 2
+GRAN_1x128, GRAN_128x128, GRAN_TENSOR, GRAN_1x32 = 0, 1, 2, 3
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "fp8_oracle.c")
@@ -79,6 +79,13 @@ def _bind(lib):
             lib.fp8o_block_scale.restype = f32
             lib.fp8o_quantize_1x128.argtypes = [vp, i64, i64, i64, ctypes.c_int, ctypes.c_int, vp, i64, vp]
             lib.fp8o_quantize_1x128.restype = None
+            lib.fp8o_quantize_1x128_f32.argtypes = [vp, i64, i64, i64, ctypes.c_int, ctypes.c_int, vp, i64,
+                                                    vp]
+            lib.fp8o_quantize_1x128_f32.restype = None
+            lib.fp8o_mx_scale_code.argtypes = [f32, ctypes.c_int]
+            lib.fp8o_mx_scale_code.restype = ctypes.c_uint8
+            lib.fp8o_quantize_mx.argtypes = [vp, i64, i64, i64, ctypes.c_int, vp, i64, vp]
+            lib.fp8o_quantize_mx.restype = None
             lib.fp8o_quantize_128x128.argtypes = [vp, i64, i64, i64, ctypes.c_int, ctypes.c_int, vp, i64, vp]
             lib.fp8o_quantize_128x128.restype = None
             lib.fp8o_quantize_tensor.argtypes = [vp, i64, ctypes.c_int, f32, vp, vp]
@@ -189,6 +196,40 @@ def quantize_1x128(x: np.ndarray, fmt: int = E4M3, mode: int = SCALE_FP32):
     return q, s
 
 
+def quantize_1x128_f32(y: np.ndarray, fmt: int = E4M3, mode: int = SCALE_FP32):
+    """The 1x128 rule on an fp32 matrix (a product's own result, quantized for
+    the next linear layer) -> (q [rows, cols] u8, scales [ceil(cols/128), rows])."""
+    y = np.ascontiguousarray(y, dtype=np.float32)
+    rows, cols = y.shape
+    q = np.empty((rows, cols), dtype=np.uint8)
+    s = np.empty(((cols + 127) // 128, rows), dtype=np.float32)
+    _load().fp8o_quantize_1x128_f32(_ptr(y), rows, cols, cols, fmt, mode, _ptr(q), cols, _ptr(s))
+    return q, s
+
+
+def quantize_1x128_colwise(x: np.ndarray, fmt: int = E4M3, mode: int = SCALE_FP32):
+    """Column-wise 1x128 tiles (128 consecutive rows of one column), kept as
+    the transposed copy: by definition the 1x128 rule applied to x^T.
+    x: [rows, cols] bf16 bits -> (qt [cols, rows] u8, scales_t [ceil(rows/128), cols])."""
+    return quantize_1x128(np.ascontiguousarray(_bf16(x).T), fmt, mode)
+
+
+def mx_scale_code(amax: float, fmt: int) -> int:
+    """MXFP8 scale code (E8M0) of a 32-element block with this amax."""
+    return int(_load().fp8o_mx_scale_code(ctypes.c_float(amax), fmt))
+
+
+def quantize_mx(x: np.ndarray, fmt: int = E4M3):
+    """MXFP8: 32-element blocks along rows, E8M0 scale codes.
+    x: [rows, cols] bf16 bits -> (q [rows, cols] u8, scales [ceil(cols/128), rows, 4] u8)."""
+    x = _bf16(x)
+    rows, cols = x.shape
+    q = np.empty((rows, cols), dtype=np.uint8)
+    s = np.empty(((cols + 127) // 128, rows, 4), dtype=np.uint8)
+    _load().fp8o_quantize_mx(_ptr(x), rows, cols, cols, fmt, _ptr(q), cols, _ptr(s))
+    return q, s
+
+
 def quantize_128x128(w: np.ndarray, fmt: int = E4M3, mode: int = SCALE_FP32):
     """w: [rows, cols] bf16 bits -> (q, scales [ceil(rows/128), ceil(cols/128)] f32)."""
     w = _bf16(w)
@@ -232,7 +273,7 @@ class DelayedState:
 # ------------------------------------------------------------------- GEMM
 def operand(data: np.ndarray, fmt: int, gran: int, scales: np.ndarray, transposed: bool = False):
     data = np.ascontiguousarray(data, dtype=np.uint8)
-    scales = np.ascontiguousarray(scales, dtype=np.float32)
+    scales = np.ascontiguousarray(scales, dtype=np.uint8 if gran == GRAN_1x32 else np.float32)
     op = Operand(data=_ptr(data), ld=data.shape[-1], transposed=int(transposed), fmt=fmt,
                  gran=gran, pad_=0, scales=_ptr(scales))
     op._keep = (data, scales)
@@ -306,3 +347,118 @@ def check_bf16(y_bits: np.ndarray, y_ref: np.ndarray, yabs: np.ndarray, rel: flo
     hi = _ordinal(_bf16_round(y_ref + tol)) + 1
     o = _ordinal(np.asarray(y_bits, dtype=np.uint16))
     return ~((o >= lo) & (o <= hi))
+
+
+# ------------------------------------------------------------ SwiGLU
+def swiglu(g: np.ndarray, u: np.ndarray) -> np.ndarray:
+    """silu(g) * u in fp64 with silu(g) = g / (1 + e^-g): the gated activation
+    between an MLP's gate/up product and its down product.  It is one of the
+    non-linear functions the NeMo RL page keeps out of FP8 math ("El avance
+    tecnico"); here it sits between two FP8 products."""
+    g = np.asarray(g, dtype=np.float64)
+    u = np.asarray(u, dtype=np.float64)
+    with np.errstate(over="ignore"):
+        return g / (1.0 + np.exp(-g)) * u
+
+
+def _silu_argmin() -> float:
+    """Where silu has its minimum: the root of silu'(x) = s(x) (1 + x (1 - s(x)))
+    with s the logistic function, i.e. of 1 + x (1 - s(x)), found by bisection
+    on [-2, -1] (the root is near -1.2785)."""
+    lo, hi = -2.0, -1.0
+    for _ in range(200):
+        mid = 0.5 * (lo + hi)
+        f = 1.0 + mid * (1.0 - 1.0 / (1.0 + np.exp(-mid)))
+        if f > 0:
+            hi = mid
+        else:
+            lo = mid
+    return 0.5 * (lo + hi)
+
+
+SILU_ARGMIN = _silu_argmin()
+
+
+def silu_range(lo: np.ndarray, hi: np.ndarray):
+    """Element-wise (min, max) of silu over the intervals [lo, hi]: silu falls
+    on (-inf, SILU_ARGMIN] and rises after it."""
+    lo = np.asarray(lo, dtype=np.float64)
+    hi = np.asarray(hi, dtype=np.float64)
+    one = np.ones_like(lo)
+    a, b = swiglu(lo, one), swiglu(hi, one)
+    inside = (lo <= SILU_ARGMIN) & (hi >= SILU_ARGMIN)
+    mn = np.where(inside, swiglu(np.float64(SILU_ARGMIN), 1.0), np.minimum(a, b))
+    return mn, np.maximum(a, b)
+
+
+def swiglu_bounds(g, g_tol, u, u_tol, rel: float = 1e-6, rel_g: float = 1e-7):
+    """Interval [lo, hi] holding silu(g') * u' for every g' within g_tol of g
+    and u' within u_tol of u, widened by (rel + rel_g |g'|) of its magnitude
+    for an fp32 evaluation of silu and of the product.  The default slack is
+    twice the error of the fast exponential / division forms: the argument
+    -g log2(e) is rounded to fp32 (relative error of e^-g up to
+    |g| log2(e) 2^-24 ln 2, about 4e-8 |g|) and the base-2 exponential,
+    the reciprocal and three roundings add about 5e-7."""
+    g = np.asarray(g, dtype=np.float64)
+    s_lo, s_hi = silu_range(g - g_tol, g + g_tol)
+    u_lo, u_hi = np.asarray(u) - u_tol, np.asarray(u) + u_tol
+    prods = np.stack([s_lo * u_lo, s_lo * u_hi, s_hi * u_lo, s_hi * u_hi])
+    lo, hi = prods.min(axis=0), prods.max(axis=0)
+    slack = (rel + rel_g * (np.abs(g) + g_tol)) * np.maximum(np.abs(lo), np.abs(hi)) + 1e-37
+    return lo - slack, hi + slack
+
+
+# ---------------------------------------------- quantized-output acceptance
+def _code_ordinal(c: np.ndarray) -> np.ndarray:
+    """8-bit code -> integer monotone in the encoded value (+0 and -0 both 0)."""
+    c = np.asarray(c).astype(np.int64)
+    return np.where(c & 0x80, -(c & 0x7F), c & 0x7F)
+
+
+def _block_scale_vec(amax: np.ndarray, fmt: int, mode: int) -> np.ndarray:
+    flat = np.asarray(amax, dtype=np.float32).ravel()
+    out = np.array([block_scale(float(a), fmt, mode) for a in flat], dtype=np.float32)
+    return out.reshape(np.shape(amax))
+
+
+def check_quantized_1x128(q: np.ndarray, s: np.ndarray, lo: np.ndarray, hi: np.ndarray,
+                          fmt: int, mode: int):
+    """Accept a 1x128 quantization (codes q [rows, cols], scales s [cols/128,
+    rows]) of fp32 values that are only known to lie in [lo, hi] (fp64,
+    element-wise): a product's result inside its tolerance.
+      scale: between the scale rule applied to the smallest and to the largest
+             block amax the intervals allow (1 also allowed when the amax can
+             be 0: the zero-block rule);
+      code:  between enc(fl32(lo32 * r)) and enc(fl32(hi32 * r)) in value
+             order, r = fl32(1 / s) the reciprocal of the scale the kernel
+             chose, lo32/hi32 the intervals rounded outward to fp32 (the
+             encoder and fl32(x * r) are both monotone).
+    With lo == hi == an fp32 matrix this is exactly quantize_1x128_f32.
+    Returns (bad_scale [cols/128, rows], bad_code [rows, cols]) masks."""
+    lo = np.asarray(lo, dtype=np.float64)
+    hi = np.asarray(hi, dtype=np.float64)
+    rows, cols = lo.shape
+    nb = cols // 128
+    lo32 = lo.astype(np.float32)
+    lo32 = np.where(lo32.astype(np.float64) > lo, np.nextafter(lo32, np.float32(-np.inf)), lo32)
+    hi32 = hi.astype(np.float32)
+    hi32 = np.where(hi32.astype(np.float64) < hi, np.nextafter(hi32, np.float32(np.inf)), hi32)
+    amin = np.where((lo32 <= 0) & (hi32 >= 0), np.float32(0),
+                    np.minimum(np.abs(lo32), np.abs(hi32)))
+    amaxe = np.maximum(np.abs(lo32), np.abs(hi32))
+    blk_lo = amin.reshape(rows, nb, 128).max(axis=2)
+    blk_hi = amaxe.reshape(rows, nb, 128).max(axis=2)
+    tiny = np.float32(np.finfo(np.float32).smallest_subnormal)
+    s_lo = _block_scale_vec(np.maximum(blk_lo, tiny), fmt, mode)
+    s_hi = _block_scale_vec(np.maximum(blk_hi, tiny), fmt, mode)
+    sg = np.asarray(s, dtype=np.float32).T                       # [rows, nb]
+    ok_s = ((sg >= s_lo) & (sg <= s_hi)) | ((blk_lo == 0) & (sg == np.float32(1.0)))
+    r = (np.float32(1.0) / sg).astype(np.float32)
+    r_e = np.repeat(r, 128, axis=1)
+    v_lo = (lo32 * r_e).astype(np.float32)
+    v_hi = (hi32 * r_e).astype(np.float32)
+    o_lo = _code_ordinal(encode_array(v_lo, fmt))
+    o_hi = _code_ordinal(encode_array(v_hi, fmt))
+    o = _code_ordinal(q)
+    ok_c = (o >= o_lo) & (o <= o_hi)
+    return ~ok_s.T, ~ok_c

@@ -40,6 +40,7 @@
 #define ORC_GRAN_1x128 0
 #define ORC_GRAN_128x128 1
 #define ORC_GRAN_TENSOR 2
+#define ORC_GRAN_1x32 3
 
 /* ---------------------------------------------------------------- formats */
 
@@ -187,6 +188,85 @@ void fp8o_quantize_1x128(const uint16_t* x, int64_t rows, int64_t cols, int64_t 
     }
 }
 
+/* The same 1x128 rule on fp32 input: the quantization a product's epilogue
+ * applies to its own fp32 result so that it can feed the next FP8 linear
+ * layer directly (the quantization step the NeMo RL page counts among the
+ * overheads of "Ganancias de rendimiento en el mundo real", done on the
+ * product's output).  Reading: the same scale and element rules as for a
+ * bf16 input, with the fp32 value in place of the widened bf16 one.
+ * y: [rows][ldy] fp32; q, scales as fp8o_quantize_1x128. */
+void fp8o_quantize_1x128_f32(const float* y, int64_t rows, int64_t cols, int64_t ldy,
+                             int fmt, int mode, uint8_t* q, int64_t ldq, float* scales) {
+    int64_t nkb = (cols + 127) / 128;
+    for (int64_t r = 0; r < rows; r++) {
+        for (int64_t kb = 0; kb < nkb; kb++) {
+            int64_t c0 = kb * 128, c1 = c0 + 128 < cols ? c0 + 128 : cols;
+            float amax = 0.0f;
+            for (int64_t c = c0; c < c1; c++) {
+                float a = fabsf(y[r * ldy + c]);
+                if (a > amax) amax = a;
+            }
+            float s = fp8o_block_scale(amax, fmt, mode);
+            scales[kb * rows + r] = s;
+            for (int64_t c = c0; c < c1; c++)
+                q[r * ldq + c] = quant_elem(y[r * ldy + c], s, fmt);
+        }
+    }
+}
+
+/* MXFP8 (microscaling FP8): one shared power-of-two scale per 32 consecutive
+ * elements of a row.  The introl page names MXFP8 as Blackwell's block
+ * scaling -- a separate scale factor for each block of a tensor, applied by
+ * the hardware ("Requisitos de hardware para entrenamiento FP8",
+ * "Estrategias de escalado y estabilidad", "Blackwell MXFP8 y NVFP4") --
+ * without giving the block size or the scale rule.  Reading: the open
+ * microscaling format the name refers to --
+ *   32-element blocks; an 8-bit power-of-two scale X = 2^e stored as the
+ *   code e + 127 (E8M0, 255 = NaN);
+ *   e = floor(log2(amax)) - emax, emax the exponent of the element format's
+ *   largest binade (8 for E4M3, 15 for E5M2), clamped to [-127, 127];
+ *   elements enc(x * 2^-e) with the usual rounding and saturation (the
+ *   block maximum lies in [2^emax, 2^(emax+1)) and may saturate);
+ *   amax == 0 -> e = -127 (code 0); a non-finite amax -> code 255 and NaN
+ *   elements.
+ * floor(log2(amax)) is exact from frexp (amax = m 2^ex, m in [0.5, 1)). */
+uint8_t fp8o_mx_scale_code(float amax, int fmt) {
+    if (!isfinite(amax)) return 255;
+    if (amax == 0.0f) return 0;
+    int ex;
+    frexp((double)amax, &ex);
+    int e = (ex - 1) - (fmt == ORC_E4M3 ? 8 : 15);
+    if (e < -127) e = -127;
+    if (e > 127) e = 127;
+    return (uint8_t)(e + 127);
+}
+
+/* x: [rows][ldx] bf16 bits; q: [rows][ldq] codes;
+ * scales: [ceil(cols/128)][rows][4] codes -- byte j of entry (kb, r) is
+ * the scale of columns 128 kb + 32 j .. 128 kb + 32 j + 31 of row r. */
+void fp8o_quantize_mx(const uint16_t* x, int64_t rows, int64_t cols, int64_t ldx, int fmt,
+                      uint8_t* q, int64_t ldq, uint8_t* scales) {
+    int64_t nkb = (cols + 127) / 128;
+    for (int64_t r = 0; r < rows; r++) {
+        for (int64_t b = 0; b < nkb * 4; b++) {
+            int64_t c0 = b * 32, c1 = c0 + 32 < cols ? c0 + 32 : cols;
+            uint8_t code = 0;
+            if (c0 < cols) {
+                float amax = 0.0f;
+                for (int64_t c = c0; c < c1; c++) {
+                    float a = fabsf(fp8o_bf16_to_f32(x[r * ldx + c]));
+                    if (a > amax) amax = a;   /* as in the other quantizers: NaN does not enter */
+                }
+                code = fp8o_mx_scale_code(amax, fmt);
+                float mult = code == 255 ? NAN : (float)ldexp(1.0, 127 - (int)code);
+                for (int64_t c = c0; c < c1; c++)
+                    q[r * ldq + c] = (uint8_t)fp8o_encode(fp8o_bf16_to_f32(x[r * ldx + c]) * mult, fmt);
+            }
+            scales[((b / 4) * rows + r) * 4 + (b % 4)] = code;
+        }
+    }
+}
+
 /* Weight tiles: one scale per 128x128 tile ("128x128" on the NeMo RL page).
  * A partial last tile covers only the rows/columns that exist.
  * scales: [ceil(rows/128)][ceil(cols/128)]. */
@@ -260,7 +340,9 @@ void fp8o_amax_history_update(float* history, int32_t* head, int32_t L, float am
  *   GRAN_1x128   (transposed == 0 only): [ceil(K/128)][rows]
  *   GRAN_128x128, transposed == 0: [ceil(rows/128)][ceil(K/128)]
  *   GRAN_128x128, transposed == 1: [ceil(K/128)][ceil(rows/128)]
- *   GRAN_TENSOR: one value. */
+ *   GRAN_TENSOR: one value.
+ *   GRAN_1x32    (transposed == 0 only): MXFP8 codes, [ceil(K/128)][rows][4]
+ *                bytes (see fp8o_quantize_mx), the pointer cast to float*. */
 typedef struct {
     const uint8_t* data;
     int64_t ld;
@@ -276,7 +358,10 @@ static double deq(const fp8o_operand* o, const double* lut, int64_t rows, int64_
     uint8_t c = o->transposed ? o->data[k * o->ld + r] : o->data[r * o->ld + k];
     double s;
     int64_t nkb = (K + 127) / 128, nrb = (rows + 127) / 128;
-    if (o->gran == ORC_GRAN_1x128) s = o->scales[(k / 128) * rows + r];
+    if (o->gran == ORC_GRAN_1x32) {   /* MXFP8: code of the 32-element block, 2^(code - 127) */
+        uint8_t code = ((const uint8_t*)o->scales)[((k / 128) * rows + r) * 4 + (k % 128) / 32];
+        s = code == 255 ? NAN : ldexp(1.0, (int)code - 127);
+    } else if (o->gran == ORC_GRAN_1x128) s = o->scales[(k / 128) * rows + r];
     else if (o->gran == ORC_GRAN_128x128)
         s = o->transposed ? o->scales[(k / 128) * nrb + r / 128]
                           : o->scales[(r / 128) * nkb + k / 128];
@@ -301,8 +386,8 @@ int fp8o_gemm(int64_t M, int64_t N, int64_t K,
     double lutA[256], lutB[256];
     make_lut(A->fmt, lutA);
     make_lut(B->fmt, lutB);
-    if (A->transposed && A->gran == ORC_GRAN_1x128) return -1;
-    if (B->transposed && B->gran == ORC_GRAN_1x128) return -1;
+    if (A->transposed && (A->gran == ORC_GRAN_1x128 || A->gran == ORC_GRAN_1x32)) return -1;
+    if (B->transposed && (B->gran == ORC_GRAN_1x128 || B->gran == ORC_GRAN_1x32)) return -1;
     for (int64_t i = 0; i < nr; i++) {
         int64_t m = row_sel ? row_sel[i] : i;
         if (m < 0 || m >= M) return -1;

@@ -87,7 +87,9 @@ def test_gemm_validation(L):
     by = ctypes.byref
     assert g(256, 256, 500, by(A), by(B), 0, FAKE, 256, 1, None) == -2      # K % 128
     assert g(256, 250, 512, by(A), by(B), 0, FAKE, 256, 1, None) == -2      # N % 8
-    assert g(256, 256, 512, by(A), by(_op(gran=0)), 0, FAKE, 256, 1, None) == -2  # 1x128 on B
+    assert g(256, 256, 512, by(A), by(_op(gran=0, transposed=1, ld=256)), 0, FAKE, 256, 1, None) == -2
+    assert g(256, 256, 512, by(_op(gran=1, transposed=1, ld=256)), by(_op(gran=0)), 0, FAKE, 256, 1,
+             None) == -2                                                    # 1x128 B, A^T
     assert g(256, 256, 512, by(_op(gran=0, transposed=1, ld=256)), by(B), 0, FAKE, 256, 1, None) == -2
     assert g(256, 256, 512, by(A), by(B), 0, FAKE + 8, 256, 1, None) == -3  # Y alignment
     assert g(256, 256, 512, by(A), by(B), 0, FAKE, 260, 1, None) == -3      # ld_y pitch
@@ -105,6 +107,44 @@ def test_gemm_validation(L):
     assert gg(8, FAKE, 1024, 256, 512, by(A), by(_op(transposed=1, gran=1, ld=256)), 0, FAKE, 256, 1,
               None) == -2
     assert gg(8, FAKE, 1024, 256, 512, by(_op(gran=1)), by(B), 0, FAKE, 256, 1, None) == -2
+    assert gg(8, FAKE, 1024, 256, 512, by(A), by(_op(gran=0)), 0, FAKE, 256, 1, None) == -2
+
+
+def test_quantized_output_validation(L):
+    g = L.fp8_block_gemm_quant
+    A, B = _op(gran=0), _op(gran=1)
+    by = ctypes.byref
+    #        M    N    K    A      B      mode epi fmt qmode Q     ld_q  scales
+    assert g(256, 640, 512, by(A), by(B), 0, 1, 0, 0, FAKE, 320, FAKE, None) == -2  # SwiGLU N % 256
+    assert g(256, 200, 512, by(A), by(B), 0, 0, 0, 0, FAKE, 208, FAKE, None) == -2  # N % 128
+    assert g(256, 512, 512, by(A), by(B), 0, 7, 0, 0, FAKE, 512, FAKE, None) == -1  # bad epilogue
+    assert g(256, 512, 512, by(A), by(B), 0, 0, 4, 0, FAKE, 512, FAKE, None) == -1  # bad q format
+    assert g(256, 512, 512, by(A), by(B), 0, 0, 0, 9, FAKE, 512, FAKE, None) == -1  # bad q mode
+    assert g(256, 512, 512, by(A), by(B), 0, 0, 0, 0, None, 512, FAKE, None) == -1  # null Q
+    assert g(256, 512, 512, by(A), by(B), 0, 0, 0, 0, FAKE, 512, None, None) == -1  # null scales
+    assert g(256, 512, 512, by(A), by(B), 0, 0, 0, 0, FAKE + 8, 512, FAKE, None) == -3
+    assert g(256, 512, 512, by(A), by(B), 0, 0, 0, 0, FAKE, 520, FAKE, None) == -3  # ld_q % 16
+    assert g(256, 512, 512, by(A), by(B), 0, 0, 0, 0, FAKE, 512, FAKE + 2, None) == -3
+    assert g(256, 512, 512, by(A), by(B), 0, 1, 0, 0, FAKE, 128, FAKE, None) == -1  # ld_q < N/2
+    assert g(256, 512, 512, by(A), by(_op(gran=1, transposed=1, ld=512)), 0, 1, 0, 0, FAKE, 256, FAKE,
+             None) == -2                                                            # SwiGLU, B^T
+    assert g(0, 512, 512, by(A), by(B), 0, 1, 0, 0, FAKE, 256, FAKE, None) == 0     # empty
+    gg = L.fp8_grouped_block_gemm_quant
+    assert gg(4, None, 1024, 512, 512, by(A), by(B), 0, 1, 0, 0, FAKE, 256, FAKE, None) == -1
+    assert gg(0, FAKE, 1024, 512, 512, by(A), by(B), 0, 1, 0, 0, FAKE, 256, FAKE, None) == -1
+
+
+def test_colwise_quantizer_validation(L):
+    f = L.fp8_quantize_1x128_colwise
+    #        x     rows cols ld   fmt mode qt    ld_qt st    q     ld_q sc
+    assert f(FAKE, 200, 384, 384, 0, 0, FAKE, 208, FAKE, None, 0, None, None) == -2   # rows % 128
+    assert f(FAKE, 256, 200, 200, 0, 0, FAKE, 256, FAKE, None, 0, None, None) == -2   # cols % 128
+    assert f(FAKE, 256, 384, 384, 0, 0, None, 256, FAKE, None, 0, None, None) == -1   # null qt
+    assert f(FAKE, 256, 384, 384, 0, 0, FAKE, 256, FAKE, FAKE, 384, None, None) == -1  # q without scales
+    assert f(FAKE, 256, 384, 384, 0, 0, FAKE, 128, FAKE, None, 0, None, None) == -1   # ld_qt < rows
+    assert f(FAKE, 256, 384, 384, 0, 0, FAKE + 8, 256, FAKE, None, 0, None, None) == -3
+    assert f(FAKE, 256, 384, 384, 0, 2, FAKE, 256, FAKE, None, 0, None, None) == -1   # bad mode
+    assert f(FAKE, 0, 384, 384, 0, 0, FAKE, 0, FAKE, None, 0, None, None) == 0        # empty
 
 
 def test_binding_refuses_cpu_tensors():

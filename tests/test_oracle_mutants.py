@@ -97,7 +97,20 @@ def _delayed_pin():
     return got == want
 
 
-PINS = [_encoder_pin, _decode_pin, _tile_pin, _pow2_pin, _gemm_pin, _delayed_pin]
+def _f32_tile_pin():
+    """1x128 rule on fp32 input vs numpy reductions + the brute-force encoder."""
+    rng = np.random.default_rng(9)
+    y = (rng.standard_normal((6, 256)) * 5).astype(np.float32)
+    y[0, 127], y[1, 255], y[2, 128] = 100.0, -100.0, 90.0   # block maxima at the block edges
+    q, s = orc.quantize_1x128_f32(y)
+    amax = np.abs(y).reshape(6, 2, 128).max(axis=2)
+    want = (amax / np.float32(448.0)).astype(np.float32)
+    r = (np.float32(1.0) / np.repeat(want, 128, axis=1)).astype(np.float32)
+    return bool(np.array_equal(s, want.T) and
+                np.array_equal(q, _nearest_code((y * r).astype(np.float32), orc.E4M3)))
+
+
+PINS = [_encoder_pin, _decode_pin, _tile_pin, _pow2_pin, _gemm_pin, _delayed_pin, _f32_tile_pin]
 
 MUTANTS = {
     "ties_away_from_zero": ("if (rem > half || (rem == half && (n & 1))) n += 1;",
@@ -115,6 +128,9 @@ MUTANTS = {
     "history_head_stuck": ("*head = (*head + 1) % L;", "*head = (*head) % L;"),
     "amax_without_abs": ("float a = fabsf(fp8o_bf16_to_f32(x[r * ldx + c]));",
                          "float a = fp8o_bf16_to_f32(x[r * ldx + c]);"),
+    "f32_amax_without_abs": ("float a = fabsf(y[r * ldy + c]);", "float a = y[r * ldy + c];"),
+    "f32_block_one_short": ("for (int64_t c = c0; c < c1; c++) {\n                float a = fabsf(y",
+                            "for (int64_t c = c0; c < c1 - 1; c++) {\n                float a = fabsf(y"),
 }
 
 

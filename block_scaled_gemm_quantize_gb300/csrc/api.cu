@@ -201,8 +201,15 @@ int run_gemm(const char* fn, int32_t G, const int32_t* offsets, int64_t a_rows, 
     if ((rc = check_operand(fn, "B", B, N, K, true, grouped)) != FP8BS_OK) return rc;
     if (swiglu && (A->transposed || B->transposed))
         return fail(FP8BS_ERR_UNSUPPORTED, "%s: SwiGLU needs non-transposed operands", fn);
-    if (B->gran == FP8BS_GRAN_1x128 && (swiglu || A->transposed))
-        return fail(FP8BS_ERR_UNSUPPORTED, "%s: 1x128 B scales need a non-transposed A and no SwiGLU", fn);
+    if (B->gran == FP8BS_GRAN_1x128) {
+        // the kernel bulk-copies B's (and a 1x128 A's) scale rows per K block
+        if (o.quant || A->transposed)
+            return fail(FP8BS_ERR_UNSUPPORTED, "%s: 1x128 B scales need a non-transposed A and a float output", fn);
+        if (A->gran == FP8BS_GRAN_1x128 && a_rows % 4)
+            return fail(FP8BS_ERR_UNSUPPORTED, "%s: 1x128 B scales with a 1x128 A need rows of A %% 4 == 0", fn);
+        if (!aligned16(B->scales) || (A->gran == FP8BS_GRAN_1x128 && !aligned16(A->scales)))
+            return fail(FP8BS_ERR_MISALIGNED, "%s: 1x128 B scales need 16-byte aligned scale tables", fn);
+    }
     const bool mx32 = A->gran == FP8BS_GRAN_1x32 || B->gran == FP8BS_GRAN_1x32;
     if (mx32 && (A->gran != B->gran || swiglu))
         return fail(FP8BS_ERR_UNSUPPORTED, "%s: MXFP8 (1x32) needs both operands 1x32 and no SwiGLU", fn);
@@ -259,7 +266,8 @@ int run_gemm(const char* fn, int32_t G, const int32_t* offsets, int64_t a_rows, 
     p.swiglu = swiglu;
     p.swiglu_i = swiglu ? N / 2 : 0;
     p.mx32 = mx32;
-    p.idesc = fp8bs::make_idesc_f8f6f4(A->fmt, B->fmt, a_mn, b_mn, b_mn ? 128 : fp8bs::gemm_mma_n());
+    p.idesc = fp8bs::make_idesc_f8f6f4(A->fmt, B->fmt, a_mn, b_mn,
+                                       b_mn ? 128 : fp8bs::gemm_mma_n(B->gran == FP8BS_GRAN_1x128));
 
     // upper bound on tiles (the grouped count is only known on the device)
     const int64_t slots = grouped ? (a_rows + BM - 1) / BM + G : (M + BM - 1) / BM;

@@ -10,23 +10,26 @@
 //   warp 0      TMA producer: per 128-deep K block, one 128x128 A tile and
 //               one 256x128 B tile (8-bit, 128-byte swizzle) into a 4-stage
 //               shared-memory ring.
-//   warp 1      TMEM owner and MMA issuer: per K block, two N=128 halves of
-//               4 x tcgen05.mma.kind::f8f6f4 (M=128, N=128, K=32), each half
-//               into its own 128-column TMEM partial buffer.
-//   warps 2,3   idle (they complete the first warpgroup).
+//   warp 1      TMEM owner and MMA issuer: per K block, 4 x
+//               tcgen05.mma.kind::f8f6f4 (M=128, K=32) over the 256 columns,
+//               as one N=256 slice (H = 1: a ring of two 256-column TMEM
+//               buffers) or two N=128 slices (H = 2: four 128-column buffers).
+//   warp 2      idle; warp 3 loads per-column B scales (1x128 B) into a
+//               shared-memory ring when the product has them.
 //   warps 4..11 epilogue ("promotion"): each thread owns one output row (its
 //               TMEM lane) and 128 columns; per K block it loads the fp32
 //               partial from TMEM and folds it into fp32 registers with that
-//               block's two scales: acc = fma(partial, sA * sB, acc), two
-//               columns per packed f32x2 FMA.
+//               block's scales: acc = fma(partial, sA * sB, acc), two columns
+//               per packed f32x2 FMA.  At the end of a tile it stores bf16 or
+//               fp32, or quantizes (optionally after SwiGLU) to the next
+//               linear's FP8 operand.
 // Register split (setmaxnreg): the block launches with 168 registers per
 // thread (384 x 168 = 64512); the first warpgroup releases down to 72 and the
 // two epilogue warpgroups grow to 216: 128 x 72 + 256 x 216 = 64512.
-// TMEM holds a 4-deep ring of 128-column partial buffers (half 0 and half 1
-// of two K blocks); each epilogue warpgroup follows its own half, so three
-// MMA groups (~768 tensor cycles) cover the commit -> promote -> release
-// round trip before a buffer is needed again.  When both operands have one scale per tensor
-// the whole K accumulates in TMEM and is scaled once ("promote every K").
+// A TMEM buffer goes back to the MMA right after the epilogue's last load of
+// it, so the MMAs of the next block(s) overlap the promotion arithmetic.
+// When both operands have one scale per tensor the whole K accumulates in
+// TMEM and is scaled once ("promote every K").
 // Operands may be stored K-major or MN-major (transposed storage, used by
 // dgrad/wgrad); the instruction descriptor's major bits and the shared-memory
 // descriptor strides select the layout.
@@ -79,19 +82,27 @@ constexpr uint64_t DRAIN_LIMIT_NS = 200000000ull;
 
 // Shared memory: [align pad][A ring][B ring][barriers][tmem addr][group tables]
 constexpr uint32_t BAR_OFF = STAGES * STAGE_BYTES;
+// Each K block's MMAs run as H slices of N = 256 / H columns, each into its
+// own TMEM buffer of a ring of 512 / (256 / H) buffers: H = 1 (two 256-column
+// buffers) for the promotion epilogue, whose per-block work fits inside one
+// MMA block; H = 2 (four 128-column buffers, each epilogue warpgroup
+// following its own half) where the epilogue's per-block work is longer
+// (per-column B scales), trading MMA rate (N = 128) for slack.
 #ifndef FP8BS_HALVES
 #define FP8BS_HALVES 1
 #endif
-// Each K block's MMAs run as HALVES slices of N = 256 / HALVES columns, each
-// into its own TMEM buffer of a ring of 512 / MMA_N buffers.
+#ifndef FP8BS_BCOL_HALVES
+#define FP8BS_BCOL_HALVES 1
+#endif
 constexpr int HALVES = FP8BS_HALVES;
-constexpr int MMA_N = BN / HALVES;
-constexpr int TBUFS = 512 / MMA_N;
-// per-column B scales (1x128 B): a ring of BSF_SLOTS K blocks x 256 fp32
+constexpr int BCOL_HALVES = FP8BS_BCOL_HALVES;
+constexpr int MAX_TBUFS = 4;
+// per-column B scales (1x128 B): a ring of BSF_SLOTS K blocks, each slot the
+// tile's 256 B column scales (1 KiB) and, for a 1x128 A, its 128 row scales
 constexpr int BSF_SLOTS = 4;
-constexpr int BSF_LPF = 4;                            // loader prefetch distance (K blocks)
+constexpr uint32_t BSF_SLOT_BYTES = 1536;
 // full, empty, tfull, tempty, done, xchg[4], bsf_full, bsf_empty
-constexpr int NUM_BARS = 2 * STAGES + 2 * TBUFS + 1 + 4 + 2 * BSF_SLOTS;
+constexpr int NUM_BARS = 2 * STAGES + 2 * MAX_TBUFS + 1 + 4 + 2 * BSF_SLOTS;
 constexpr uint32_t TMEMSLOT_OFF = BAR_OFF + NUM_BARS * 8;
 constexpr uint32_t TABLE_OFF = (TMEMSLOT_OFF + 16 + 15) & ~15u;
 // output staging: one 2 KiB slab per epilogue warp (32 rows x 64 B, 64-B swizzle)
@@ -101,7 +112,7 @@ constexpr uint32_t OUT_OFF = (TABLE_OFF + 2 * (kMaxGroups + 1) * 4 + 1023) & ~10
 constexpr uint32_t XCHG_BYTES = 2 * 2 * 128 * 4;
 constexpr uint32_t XCHG_OFF = OUT_OFF + NUM_EPI_WARPS * OUT_SLAB;
 constexpr uint32_t BSF_OFF = XCHG_OFF + XCHG_BYTES;
-constexpr uint32_t SMEM_BYTES = 1024 + BSF_OFF + BSF_SLOTS * 1024;
+constexpr uint32_t SMEM_BYTES = 1024 + BSF_OFF + BSF_SLOTS * BSF_SLOT_BYTES;
 static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 
 __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
@@ -340,10 +351,12 @@ __device__ __forceinline__ bool finish_tile(const GemmParams& p, const CUtensorM
     return true;
 }
 
-template <bool A_MN, bool B_MN, bool SWIGLU, bool B_COL>
+template <bool A_MN, bool B_MN, bool SWIGLU, bool B_COL, int H>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     k_fp8_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                const __grid_constant__ CUtensorMap tmY, const GemmParams p) {
+    constexpr int MMA_N = BN / H;
+    constexpr int TBUFS = 512 / MMA_N;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     uint8_t* smem = smem_raw + ((1024u - (raw & 1023u)) & 1023u);
@@ -354,11 +367,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     auto full_bar = [&](int s) { return bars + 8u * s; };
     auto empty_bar = [&](int s) { return bars + 8u * (STAGES + s); };
     auto tfull_bar = [&](int b) { return bars + 8u * (2 * STAGES + b); };
-    auto tempty_bar = [&](int b) { return bars + 8u * (2 * STAGES + TBUFS + b); };
-    const uint32_t done_bar = bars + 8u * (2 * STAGES + 2 * TBUFS);
-    auto xchg_bar = [&](int q) { return bars + 8u * (2 * STAGES + 2 * TBUFS + 1 + q); };
-    auto bsf_full = [&](int q) { return bars + 8u * (2 * STAGES + 2 * TBUFS + 5 + q); };
-    auto bsf_empty = [&](int q) { return bars + 8u * (2 * STAGES + 2 * TBUFS + 5 + BSF_SLOTS + q); };
+    auto tempty_bar = [&](int b) { return bars + 8u * (2 * STAGES + MAX_TBUFS + b); };
+    const uint32_t done_bar = bars + 8u * (2 * STAGES + 2 * MAX_TBUFS);
+    auto xchg_bar = [&](int q) { return bars + 8u * (2 * STAGES + 2 * MAX_TBUFS + 1 + q); };
+    auto bsf_full = [&](int q) { return bars + 8u * (2 * STAGES + 2 * MAX_TBUFS + 5 + q); };
+    auto bsf_empty = [&](int q) { return bars + 8u * (2 * STAGES + 2 * MAX_TBUFS + 5 + BSF_SLOTS + q); };
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + TMEMSLOT_OFF);
     int* s_off = reinterpret_cast<int*>(smem + TABLE_OFF);
     int* s_slot = s_off + (kMaxGroups + 1);
@@ -376,13 +389,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
         for (int b = 0; b < TBUFS; b++) {
             mbar_init(tfull_bar(b), 1);
-            mbar_init(tempty_bar(b), NUM_EPI_WARPS / HALVES);   // the warps reading it
+            mbar_init(tempty_bar(b), NUM_EPI_WARPS / H);   // the warps reading it
         }
         mbar_init(done_bar, 1);
         for (int q = 0; q < 4; q++) mbar_init(xchg_bar(q), 64);
         for (int q = 0; q < BSF_SLOTS; q++) {
-            mbar_init(bsf_full(q), 32);                   // the loader warp's lanes
-            mbar_init(bsf_empty(q), 32 * NUM_EPI_WARPS);  // every epilogue thread
+            mbar_init(bsf_full(q), 1);                    // the loader's expect_tx arrival
+            mbar_init(bsf_empty(q), NUM_EPI_WARPS);       // one arrival per epilogue warp
         }
         fence_mbar_init();
         fence_proxy_async_smem();
@@ -483,8 +496,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     // two N=128 halves per K block, each into its own 128-column
                     // TMEM buffer of a 4-deep ring (chunk c = 2 * group + half)
 #pragma unroll
-                    for (int h = 0; h < HALVES; h++) {
-                        const uint32_t c = HALVES * group + h, buf = c % TBUFS;
+                    for (int h = 0; h < H; h++) {
+                        const uint32_t c = H * group + h, buf = c % TBUFS;
                         if (kb % P == 0) {
                             if (!wait_or_flag(tempty_bar(buf), ((c / TBUFS) & 1u) ^ 1u)) { ok = false; break; }
                         }
@@ -532,42 +545,136 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
       } else if (B_COL && warp == 3) {
         // ------------- per-column B scale loader (1x128 B: table [K/128][N])
-        // Each K block's 256 column scales of the tile go to a ring slot; the
-        // epilogue threads release a slot once they have read it.  Loads run
-        // BSF_LPF K blocks ahead in registers.
-        int slot = 0;
-        uint32_t ph = 0;
-        bool ok = true;
-        for (int t = blockIdx.x; ok && t < total_tiles; t += gridDim.x) {
-            const Tile tl = decode_tile(t, total_slots, p.tiles_n, G, s_slot, s_off);
-            const int64_t n0 = static_cast<int64_t>(tl.nt) * BN;
-            float pre[BSF_LPF][8];
-            auto load = [&](int kbi, float (&d)[8]) {
-#pragma unroll
-                for (int c = 0; c < 8; c++) {
-                    const int64_t n = n0 + 32 * c + lane;
-                    d[c] = (kbi < nkb && n < p.N) ? ld_scale(p.sb + static_cast<int64_t>(kbi) * p.N + n) : 0.0f;
-                }
-            };
-#pragma unroll
-            for (int i = 0; i < BSF_LPF; i++) load(i, pre[i]);
-            for (int kb0 = 0; ok && kb0 < nkb; kb0 += BSF_LPF) {
-#pragma unroll
-                for (int i = 0; i < BSF_LPF; i++) {
-                    const int kb = kb0 + i;
-                    if (kb >= nkb) break;
-                    ok = __all_sync(0xFFFFFFFFu, wait_or_flag(bsf_empty(slot), ph ^ 1u));
-                    if (!ok) break;
-                    const uint32_t dst = sbase + BSF_OFF + slot * 1024;
-#pragma unroll
-                    for (int c = 0; c < 8; c++) st_shared_f32(dst + (32 * c + lane) * 4, pre[i][c]);
-                    mbar_arrive(bsf_full(slot));
-                    load(kb + BSF_LPF, pre[i]);
+        // Per K block, two bulk copies into a ring slot: the tile's column
+        // scales (row kb of B's table) and, for a 1x128 A, its row scales
+        // (row kb of A's table); both tables are 16-byte aligned with row
+        // pitches that are multiples of 16 bytes (checked on the host), and the
+        // copies stop at the tables' ends.  A 128x128 or per-tensor A scale is
+        // stored into the slot directly.  The epilogue warps free a slot once
+        // they have read it.
+        if (lane == 0) {
+            int slot = 0;
+            uint32_t ph = 0;
+            bool ok = true;
+            int issued = 0;
+            for (int t = blockIdx.x; ok && t < total_tiles; t += gridDim.x) {
+                const Tile tl = decode_tile(t, total_slots, p.tiles_n, G, s_slot, s_off);
+                const int64_t n0 = static_cast<int64_t>(tl.nt) * BN;
+                const uint32_t nb = static_cast<uint32_t>(min(static_cast<int64_t>(BN), p.N - n0)) * 4u;
+                const uint32_t na = p.a_gran == 0
+                    ? static_cast<uint32_t>(min(static_cast<int64_t>(BM), p.a_rows - tl.row0)) * 4u : 0u;
+                for (int kb = 0; kb < nkb; kb++) {
+                    if (!wait_or_flag(bsf_empty(slot), ph ^ 1u)) { ok = false; break; }
+                    const uint32_t dst = sbase + BSF_OFF + slot * BSF_SLOT_BYTES;
+                    if (p.a_gran != 0)   // 128x128 / per-tensor A: its one scale of this K block
+                        st_shared_f32(dst + 1024, ld_scale(p.sa + (p.a_gran == 1 ? (min(static_cast<int64_t>(tl.row0),
+                                                                                        p.a_rows - 1) / 128) * nkb + kb : 0)));
+                    mbar_arrive_expect_tx(bsf_full(slot), nb + na);
+                    bulk_load_g2s(dst, p.sb + static_cast<int64_t>(kb) * p.N + n0, nb, bsf_full(slot));
+                    if (na) bulk_load_g2s(dst + 1024, p.sa + static_cast<int64_t>(kb) * p.a_rows + tl.row0, na,
+                                          bsf_full(slot));
+                    issued++;
                     if (++slot == BSF_SLOTS) { slot = 0; ph ^= 1u; }
+                }
+            }
+            if (!ok) {   // drain: let the copies already issued land
+                for (int i = 0; i < BSF_SLOTS && i < issued; i++) {
+                    if (--slot < 0) { slot = BSF_SLOTS - 1; ph ^= 1u; }
+                    wait_bounded(bsf_full(slot), ph, DRAIN_LIMIT_NS);
                 }
             }
         }
       }
+    } else if (B_COL) {
+        asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(REGS_HIGH));
+        // ------------------------------ epilogue with per-column B scales
+        // Every (row, column) needs its own product sa[row] * sb[col], so the
+        // scales are read from shared memory each K block.  To keep that
+        // traffic small each thread owns 4 rows x 32 columns (the 16x256b TMEM
+        // load shape: rows 32 q + 16 lh + t/4 + 8 e, columns 8 c + 2 (t%4) + e'),
+        // so it reads 32 B scales and 4 A scales per K block instead of 128.
+        const int quarter = warp & 3;
+        const int half = (warp - EPI_WARP0) >> 2;
+        const int tq = lane >> 2, tc = lane & 3;
+        uint32_t chunk = 0;
+        int bslot = 0;
+        uint32_t bph = 0;
+        bool ok = true;
+        for (int t = blockIdx.x; ok && t < total_tiles; t += gridDim.x) {
+            const Tile tl = decode_tile(t, total_slots, p.tiles_n, G, s_slot, s_off);
+            const int64_t col0 = static_cast<int64_t>(tl.nt) * BN + half * 128;
+            uint64_t acc[64];   // [row r (4)][column pair c (16)]
+#pragma unroll
+            for (int i = 0; i < 64; i++) acc[i] = 0;
+            for (int kb = 0; kb < nkb; kb++) {
+                const uint32_t buf = chunk % TBUFS;
+                ok = __all_sync(0xFFFFFFFFu, wait_or_flag(tfull_bar(buf), (chunk / TBUFS) & 1u));
+                if (!ok) break;
+                ok = __all_sync(0xFFFFFFFFu, wait_or_flag(bsf_full(bslot), bph));
+                if (!ok) break;
+                tc_fence_after();
+                const uint32_t slotb = sbase + BSF_OFF + bslot * BSF_SLOT_BYTES;
+                const uint32_t tb = tmem_base + buf * MMA_N + half * 128;
+                float a[4];   // A scales of rows 16 lh + 8 e (+ t/4): a[2 lh + e]
+#pragma unroll
+                for (int r = 0; r < 4; r++)
+                    a[r] = ld_shared_f32(slotb + 1024 +
+                                         (p.a_gran == 0 ? (32 * quarter + 16 * (r >> 1) + 8 * (r & 1) + tq) * 4 : 0));
+#pragma unroll
+                for (int cp = 0; cp < 2; cp++) {
+                    uint64_t sb2[8];   // B scale pairs of columns 64 cp + 8 k + 2 (t%4)
+#pragma unroll
+                    for (int k = 0; k < 8; k++) {
+                        const uint2 b = ld_shared_v2(slotb + (half * 128 + 64 * cp + 8 * k + 2 * tc) * 4);
+                        sb2[k] = pack_f32x2(b.x, b.y);
+                    }
+#pragma unroll
+                    for (int lh = 0; lh < 2; lh++) {
+                        uint32_t r[32];
+                        tmem_ld_16x256b_x8(tb + (static_cast<uint32_t>(32 * quarter + 16 * lh) << 16) + 64 * cp, r);
+                        tmem_wait_ld();
+                        if (lh == 1 && cp == 1) {   // last load of this buffer: hand it back
+                            tc_fence_before();
+                            __syncwarp();
+                            if (lane == 0) mbar_arrive(tempty_bar(buf));
+                        }
+                        const uint64_t s_lo = pack_f32x2(__float_as_uint(a[2 * lh]), __float_as_uint(a[2 * lh]));
+                        const uint64_t s_hi =
+                            pack_f32x2(__float_as_uint(a[2 * lh + 1]), __float_as_uint(a[2 * lh + 1]));
+#pragma unroll
+                        for (int k = 0; k < 8; k++) {
+                            fma_f32x2(acc[(2 * lh) * 16 + 8 * cp + k], pack_f32x2(r[4 * k], r[4 * k + 1]),
+                                      mul_f32x2(sb2[k], s_lo));
+                            fma_f32x2(acc[(2 * lh + 1) * 16 + 8 * cp + k], pack_f32x2(r[4 * k + 2], r[4 * k + 3]),
+                                      mul_f32x2(sb2[k], s_hi));
+                        }
+                    }
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bsf_empty(bslot));   // this warp read its scales
+                if (++bslot == BSF_SLOTS) { bslot = 0; bph ^= 1u; }
+                chunk++;
+            }
+            if (!ok) break;
+            // direct stores, two columns at a time (8 B fp32 / 4 B bf16 per pair)
+#pragma unroll
+            for (int r = 0; r < 4; r++) {
+                const int64_t row = static_cast<int64_t>(tl.row0) + 32 * quarter + 16 * (r >> 1) + tq + 8 * (r & 1);
+                const bool rok = row < tl.row_end;
+#pragma unroll
+                for (int c = 0; c < 16; c++) {
+                    const int64_t col = col0 + 8 * c + 2 * tc;
+                    if (!rok || col >= p.N) continue;
+                    const float2 v = unpack_f32x2(acc[r * 16 + c]);
+                    if (p.out_bf16) {
+                        __nv_bfloat162 h2 = __floats2bfloat162_rn(v.x, v.y);
+                        *reinterpret_cast<__nv_bfloat162*>(reinterpret_cast<uint16_t*>(p.y) + row * p.ldy + col) = h2;
+                    } else {
+                        *reinterpret_cast<float2*>(reinterpret_cast<float*>(p.y) + row * p.ldy + col) = v;
+                    }
+                }
+            }
+        }
     } else {
         asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(REGS_HIGH));
         // ----------------------------------------------------- epilogue
@@ -575,8 +682,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const int half = (warp - EPI_WARP0) >> 2;  // columns 128*half ..
         const int lrow = quarter * 32 + lane;
         uint32_t chunk = 0, tile_i = 0;
-        int bslot = 0;
-        uint32_t bph = 0;
         bool ok = true;
         const int64_t nkb64 = nkb;
         for (int t = blockIdx.x; ok && t < total_tiles; t += gridDim.x, tile_i++) {
@@ -633,25 +738,17 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     const uint64_t s2 = pack_f32x2(__float_as_uint(s), __float_as_uint(s));
                     const float su = sa_r[i] * sbu_r[i];
                     const uint64_t s2u = pack_f32x2(__float_as_uint(su), __float_as_uint(su));
-                    // A's scale alone, for per-column B scales (taken before the refill)
-                    const uint64_t sa2 = pack_f32x2(__float_as_uint(sa_r[i]), __float_as_uint(sa_r[i]));
                     if (kb + SPF * P < nkb) {
                         sa_r[i] = ld_scale(pa + (kb + SPF * P) * sa_step);
                         sb_r[i] = ld_scale(pb + (kb + SPF * P) * sb_step);
                         sbu_r[i] = SWIGLU ? ld_scale(pbu + (kb + SPF * P) * sb_step) : sb_r[i];
                     }
-                    const uint32_t c = HALVES * chunk + (HALVES == 2 ? half : 0), buf = c % TBUFS;
+                    const uint32_t c = H * chunk + (H == 2 ? half : 0), buf = c % TBUFS;
                     ok = __all_sync(0xFFFFFFFFu, wait_or_flag(tfull_bar(buf), (c / TBUFS) & 1u));
                     if (!ok) break;
-                    // per-column B scales of this K block (1x128 B): sa * sb[n] per pair
-                    const uint32_t sbb = sbase + BSF_OFF + bslot * 1024 + half * 512;
-                    if (B_COL) {
-                        ok = __all_sync(0xFFFFFFFFu, wait_or_flag(bsf_full(bslot), bph));
-                        if (!ok) break;
-                    }
                     tc_fence_after();
                     const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
-                                           buf * MMA_N + (HALVES == 1 ? half * 128 : 0);
+                                           buf * MMA_N + (H == 1 ? half * 128 : 0);
                     // EPI_LOADS x 32 columns in flight per wait (one TMEM round
                     // trip); the buffer is handed back right after the last load
 #pragma unroll
@@ -664,22 +761,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                             tc_fence_before();
                             __syncwarp();
                             if (lane == 0) mbar_arrive(tempty_bar(buf));
-                        }
-                        if (B_COL) {
-#pragma unroll
-                            for (int u = 0; u < EPI_LOADS; u++) {
-#pragma unroll
-                                for (int q4 = 0; q4 < 8; q4++) {
-                                    const uint4 b4 = ld_shared_v4(sbb + ((j + u) * 32 + 4 * q4) * 4);
-                                    const uint64_t s01 = mul_f32x2(pack_f32x2(b4.x, b4.y), sa2);
-                                    const uint64_t s23 = mul_f32x2(pack_f32x2(b4.z, b4.w), sa2);
-                                    fma_f32x2(acc[(j + u) * 16 + 2 * q4], pack_f32x2(r[u][4 * q4], r[u][4 * q4 + 1]),
-                                              s01);
-                                    fma_f32x2(acc[(j + u) * 16 + 2 * q4 + 1],
-                                              pack_f32x2(r[u][4 * q4 + 2], r[u][4 * q4 + 3]), s23);
-                                }
-                            }
-                            continue;
                         }
 #pragma unroll
                         for (int u = 0; u < EPI_LOADS; u++) {
@@ -697,10 +778,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 #endif
                             }
                         }
-                    }
-                    if (B_COL) {
-                        mbar_arrive(bsf_empty(bslot));             // this thread read its scales
-                        if (++bslot == BSF_SLOTS) { bslot = 0; bph ^= 1u; }
                     }
                     chunk++;
                 }
@@ -1122,17 +1199,18 @@ cudaError_t launch_fp8_gemm_mx(const CUtensorMap& tmA, const CUtensorMap& tmB, c
 }
 
 int gemm_tile_n() { return BN; }
-int gemm_mma_n() { return MMA_N; }
+int gemm_mma_n(bool b_col) { return BN / (b_col ? BCOL_HALVES : HALVES); }
 int gemm_tile_m() { return BM; }
 
 cudaError_t launch_fp8_gemm(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmY,
                             const GemmParams& p, bool a_mn, bool b_mn, int grid, cudaStream_t st) {
-    // SwiGLU runs only on K-major operands (the host checks it)
-    // (per-column B scales: K-major operands only; the host checks it)
-    auto k = p.swiglu ? k_fp8_gemm<false, false, true, false>
-             : p.b_gran == 0 ? k_fp8_gemm<false, false, false, true>
-             : a_mn ? (b_mn ? k_fp8_gemm<true, true, false, false> : k_fp8_gemm<true, false, false, false>)
-                    : (b_mn ? k_fp8_gemm<false, true, false, false> : k_fp8_gemm<false, false, false, false>);
+    // SwiGLU and per-column B scales run only on K-major operands (the host
+    // checks it); the latter with BCOL_HALVES MMA slices per K block
+    constexpr int h1 = HALVES, hb = BCOL_HALVES;
+    auto k = p.swiglu ? k_fp8_gemm<false, false, true, false, h1>
+             : p.b_gran == 0 ? k_fp8_gemm<false, false, false, true, hb>
+             : a_mn ? (b_mn ? k_fp8_gemm<true, true, false, false, h1> : k_fp8_gemm<true, false, false, false, h1>)
+                    : (b_mn ? k_fp8_gemm<false, true, false, false, h1> : k_fp8_gemm<false, false, false, false, h1>);
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
     if (e != cudaSuccess) return e;
     k<<<grid, NUM_THREADS, SMEM_BYTES, st>>>(tmA, tmB, tmY, p);

@@ -46,7 +46,8 @@ struct GemmParams {
 uint32_t gemm_smem_bytes();
 uint32_t make_idesc_f8f6f4(int a_fmt, int b_fmt, bool a_mn, bool b_mn, int n);
 int gemm_tile_n();
-int gemm_mma_n();   // N of one tcgen05.mma (a K-major B); an MN-major B always uses 128
+int gemm_mma_n(bool b_col);   // N of one tcgen05.mma (K-major B; b_col: per-column B scales);
+                              // an MN-major B always uses 128
 int gemm_tile_m();
 cudaError_t launch_fp8_gemm(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmY,
                             const GemmParams& p, bool a_mn, bool b_mn, int grid, cudaStream_t st);

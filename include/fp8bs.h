@@ -190,7 +190,10 @@ int fp8_amax_history_update(float* history, int32_t* head, int32_t history_len,
  *   GRAN_1x128   (transposed = 0 only): [K/128][rows].  On B (one scale per
  *                128 K-elements of each column of the product) it is the
  *                wgrad operand of the block recipe's backward pass (see
- *                fp8_quantize_1x128_colwise); not in grouped products.
+ *                fp8_quantize_1x128_colwise); not in grouped products, only
+ *                with a non-transposed A and a float output (fp8_block_gemm),
+ *                with 16-byte aligned scale tables, and, for a 1x128 A, rows
+ *                of A a multiple of 4.
  *   GRAN_128x128, transposed = 0: [ceil(rows/128)][K/128]
  *   GRAN_128x128, transposed = 1: [K/128][ceil(rows/128)]
  *   GRAN_TENSOR: one value.

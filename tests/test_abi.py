@@ -100,6 +100,10 @@ def test_gemm_validation(L):
     assert g(256, 256, 512, by(_op(fmt=3)), by(B), 0, FAKE, 256, 1, None) == -1
     assert g(0, 256, 512, by(A), by(B), 0, FAKE, 256, 1, None) == 0        # empty
     assert g(256, 0, 512, by(A), by(B), 0, FAKE, 256, 1, None) == 0
+    Bc = _op(gran=0)                                                        # 1x128 B (per-column scales)
+    assert g(254, 256, 512, by(A), by(Bc), 0, FAKE, 256, 1, None) == -2     # rows of A % 4
+    assert g(256, 256, 512, by(A), by(_op(gran=0, scales=FAKE + 4)), 0, FAKE, 256, 1, None) == -3
+    assert L.fp8_block_gemm_quant(256, 256, 512, by(A), by(Bc), 0, 0, 0, 0, FAKE, 256, FAKE, None) == -2
     gg = L.fp8_grouped_block_gemm
     assert gg(0, FAKE, 1024, 256, 512, by(A), by(B), 0, FAKE, 256, 1, None) == -1   # G < 1
     assert gg(2000, FAKE, 1024, 256, 512, by(A), by(B), 0, FAKE, 256, 1, None) == -1

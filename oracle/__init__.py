@@ -98,6 +98,10 @@ def _bind(lib):
             lib.fp8o_grouped_gemm.argtypes = [i32, vp, i64, i64, i64, ctypes.POINTER(Operand),
                                               ctypes.POINTER(Operand), i64, vp, i64, vp, vp, vp]
             lib.fp8o_grouped_gemm.restype = ctypes.c_int
+            lib.fp8o_attention.argtypes = [i64, i64, i32, i32, ctypes.c_int, ctypes.c_double,
+                                           vp, vp, ctypes.c_int, vp, vp, ctypes.c_int, vp, vp, ctypes.c_int,
+                                           i64, vp, vp, vp, vp, vp]
+            lib.fp8o_attention.restype = ctypes.c_int
     return lib
 
 
@@ -462,3 +466,55 @@ def check_quantized_1x128(q: np.ndarray, s: np.ndarray, lo: np.ndarray, hi: np.n
     o = _code_ordinal(q)
     ok_c = (o >= o_lo) & (o <= o_hi)
     return ~ok_s.T, ~ok_c
+
+
+# ------------------------------------------------------------ attention
+def attention(seq_q: int, seq_k: int, hq: int, hkv: int, causal: bool, scale: float,
+              q, sq, k, sk, v, sv, rows=None, heads=None, fmts=(E4M3, E4M3, E4M3)):
+    """FP8 attention over an FP8 KV cache (fp64 definition, see fp8o_attention).
+    q: [seq_q, hq*128] codes, sq: [hq, seq_q] (1x128 scales); k, v: [seq_k, hkv*128]
+    codes, sk, sv: [ceil(seq_k/128), hkv] (128x128 scales).  rows/heads select
+    (row, head) pairs (default: all).  Returns (o, oap, oav) of shape [n, 128]:
+    the output, sum_j P|V|/l and sum_j |V|/l."""
+    q = np.ascontiguousarray(q, dtype=np.uint8)
+    k = np.ascontiguousarray(k, dtype=np.uint8)
+    v = np.ascontiguousarray(v, dtype=np.uint8)
+    sq = np.ascontiguousarray(sq, dtype=np.float32)
+    sk = np.ascontiguousarray(sk, dtype=np.float32)
+    sv = np.ascontiguousarray(sv, dtype=np.float32)
+    if rows is None:
+        rr, hh = np.meshgrid(np.arange(seq_q), np.arange(hq), indexing="ij")
+        rows, heads = rr.ravel(), hh.ravel()
+    rows = np.ascontiguousarray(rows, dtype=np.int64)
+    heads = np.ascontiguousarray(heads, dtype=np.int32)
+    n = rows.size
+    o = np.empty((n, 128), np.float64)
+    oap = np.empty((n, 128), np.float64)
+    oav = np.empty((n, 128), np.float64)
+    rc = _load().fp8o_attention(seq_q, seq_k, hq, hkv, int(causal), float(scale),
+                                _ptr(q), _ptr(sq), fmts[0], _ptr(k), _ptr(sk), fmts[1], _ptr(v), _ptr(sv),
+                                fmts[2], n, _ptr(rows), _ptr(heads), _ptr(o), _ptr(oap), _ptr(oav))
+    if rc:
+        raise ValueError("oracle attention: bad arguments")
+    return o, oap, oav
+
+
+# Acceptance rule of the FP8 attention output.  The kernel quantizes the
+# softmax numerators P (in [0, 1] after the running-max subtraction) to E4M3
+# with the scale 1/448 (amax 1 by construction), so each P carries a rounding
+# error of at most 2^-4 P (normal range) or 2^-10 / 448 (subnormal range);
+# the row sum l uses the unrounded values.  Hence per output element
+#   |o - o_ref| <= (2^-4 + 1e-4) sum_j P_j |V_j| / l + (2^-10 / 448) sum_j |V_j| / l
+#                  + 1e-5 |o_ref|   (fp32 scores, exp2, accumulation)
+# plus half a bf16 unit of the stored value.
+ATTN_P_REL = 2.0 ** -4 + 1e-4
+ATTN_P_ABS = 2.0 ** -10 / 448.0
+
+
+def check_attention_bf16(o_bits: np.ndarray, o_ref: np.ndarray, oap: np.ndarray, oav: np.ndarray):
+    """FAIL mask for a bf16 attention output (bit patterns) under the rule above."""
+    import torch
+    o = torch.from_numpy(np.ascontiguousarray(o_bits, dtype=np.uint16).view(np.int16)).view(
+        torch.bfloat16).to(torch.float64).numpy()
+    tol = ATTN_P_REL * oap + ATTN_P_ABS * oav + 1e-5 * np.abs(o_ref) + 2.0 ** -8 * np.abs(o_ref) + 1e-30
+    return ~(np.abs(o - o_ref) <= tol)

@@ -15,7 +15,8 @@ operands), llama3.1-8b-mlp-bwd-blockwise (the same backward under the block
 recipe: row-wise and column-wise transposed 1x128 copies of dY and X),
 qwen3-30b-a3b-moe (grouped expert GEMMs), llama3.1-8b-mlp-fused and
 qwen3-30b-a3b-moe-fused (gate/up product with a SwiGLU + FP8-quantizing
-epilogue feeding the down product directly).
+epilogue feeding the down product directly), llama3.1-8b-attn-fp8 (causal
+prefill attention over an FP8 KV cache, both products on FP8 tensor cores).
 
 Inputs are synthetic (seeded), resident in HBM; every step streams more than
 the 129 MB L2.
@@ -515,6 +516,57 @@ class FusedMlp:
         return [self.x, self.w_gu, self.w_dn], [self.y]
 
 
+class Attn:
+    """Llama-3.1-8B attention prefill over an FP8 KV cache: quantize Q (1x128:
+    one scale per token and head), write the KV cache (K and V quantized
+    128x128: one scale per 128 tokens and head), FP8 attention forward
+    (causal, GQA 32/8 heads, head_dim 128) -> O bf16."""
+
+    def __init__(self, cfg, fp8, device, seed=0, only=None):
+        import torch
+        self.fp8 = fp8
+        S, hq, hkv = cfg["seq"], cfg["heads_q"], cfg["heads_kv"]
+        self.S, self.hq, self.hkv = S, hq, hkv
+        g = torch.Generator(device=device)
+        g.manual_seed(seed * 1000 + 900)
+        self.q = _randn(g, (S, hq * 128), device).to(torch.bfloat16)
+        self.k = _randn(g, (S, hkv * 128), device).to(torch.bfloat16)
+        self.v = _randn(g, (S, hkv * 128), device).to(torch.bfloat16)
+        u8, f32 = torch.uint8, torch.float32
+        self.qq = torch.empty((S, hq * 128), dtype=u8, device=device)
+        self.sq = torch.empty((hq, S), dtype=f32, device=device)
+        self.kq = torch.empty((S, hkv * 128), dtype=u8, device=device)
+        self.sk = torch.empty(((S + 127) // 128, hkv), dtype=f32, device=device)
+        self.vq = torch.empty((S, hkv * 128), dtype=u8, device=device)
+        self.sv = torch.empty(((S + 127) // 128, hkv), dtype=f32, device=device)
+        self.o = torch.empty((S, hq * 128), dtype=torch.bfloat16, device=device)
+        self.Q = fp8.attn_input(self.qq, self.sq)
+        self.K = fp8.attn_input(self.kq, self.sk)
+        self.V = fp8.attn_input(self.vq, self.sv)
+        pairs = S * (S + 1) // 2 if cfg["causal"] else S * S
+        self.causal = cfg["causal"]
+        qbytes = 3 * S * (hq + 2 * hkv) * 128 + 4 * S * hq + 8 * ((S + 127) // 128) * hkv
+        self.units = [("attn", 4.0 * 128 * hq * pairs, qbytes)]
+        self.flops = self.units[0][1]
+        self.launches = 4
+        self.config = {"workload": cfg["name"], "seq": S, "heads_q": hq, "heads_kv": hkv, "head_dim": 128,
+                       "causal": bool(cfg["causal"]),
+                       "scales": "Q 1x128 (token, head); K, V 128x128 (128 tokens, head); P E4M3 / 448",
+                       "out": "bf16", "flops": "4 * 128 * heads_q * visible (query, key) pairs"}
+
+    def step(self, rec=None):
+        fp8 = self.fp8
+        _run(rec, "quant:attn", lambda: (
+            fp8.fp8_quantize_1x128(self.q, q=self.qq, scales=self.sq),
+            fp8.fp8_quantize_128x128(self.k, q=self.kq, scales=self.sk),
+            fp8.fp8_quantize_128x128(self.v, q=self.vq, scales=self.sv)))
+        _run(rec, "gemm:attn", lambda: fp8.fp8_attention_fwd(
+            self.Q, self.K, self.V, self.S, self.S, self.hq, self.hkv, self.causal, 128 ** -0.5, o=self.o))
+
+    def host_io(self):
+        return [self.q, self.k, self.v], [self.o]
+
+
 WORKLOADS = {"llama3.1-8b-fprop": (Fprop, W_.LLAMA31_8B_FPROP),
              "llama3.1-8b-fprop-mxfp8": (Fprop, W_.LLAMA31_8B_FPROP_MX),
              "llama2-7b-fprop": (Fprop, W_.LLAMA2_7B_FPROP),
@@ -523,7 +575,8 @@ WORKLOADS = {"llama3.1-8b-fprop": (Fprop, W_.LLAMA31_8B_FPROP),
              "llama3.1-8b-mlp-bwd-blockwise": (MlpBwdBlock, W_.LLAMA31_8B_MLP_BWD_BLOCK),
              "qwen3-30b-a3b-moe": (MoE, W_.QWEN3_30B_MOE),
              "llama3.1-8b-mlp-fused": (FusedMlp, W_.LLAMA31_8B_MLP_FUSED),
-             "qwen3-30b-a3b-moe-fused": (FusedMlp, W_.QWEN3_30B_MOE_FUSED)}
+             "qwen3-30b-a3b-moe-fused": (FusedMlp, W_.QWEN3_30B_MOE_FUSED),
+             "llama3.1-8b-attn-fp8": (Attn, W_.LLAMA31_8B_ATTN)}
 
 
 # ------------------------------------------------------------ CPU oracle

@@ -37,6 +37,12 @@ class Fp8bsError(RuntimeError):
         self.code = code
 
 
+class AttnInput(ctypes.Structure):
+    """fp8bs_attn_input: FP8 codes [tokens, heads*128] + scale table."""
+    _fields_ = [("data", ctypes.c_void_p), ("ld", ctypes.c_int64), ("fmt", ctypes.c_int32),
+                ("reserved", ctypes.c_int32), ("scales", ctypes.c_void_p)]
+
+
 class Operand(ctypes.Structure):
     """fp8bs_operand: FP8 data + scale table of one GEMM operand."""
     _fields_ = [("data", ctypes.c_void_p), ("ld", ctypes.c_int64),
@@ -74,6 +80,9 @@ def lib() -> ctypes.CDLL:
             "fp8_block_gemm_quant": [i64, i64, i64, op, op, i32, i32, i32, i32, vp, i64, vp, vp],
             "fp8_grouped_block_gemm_quant": [i32, vp, i64, i64, i64, op, op, i32, i32, i32, i32, vp, i64,
                                              vp, vp],
+            "fp8_attention_fwd": [i64, i64, i32, i32, i32, i32, ctypes.c_float,
+                                  ctypes.POINTER(AttnInput), ctypes.POINTER(AttnInput),
+                                  ctypes.POINTER(AttnInput), vp, i64, vp],
             "fp8bs_device_status": [vp],
             "fp8bs_selftest_wait_timeout": [i32, vp, vp],
             "fp8bs_version": [],
@@ -359,6 +368,31 @@ def linear_fprop(x, w, mode=SCALE_FP32, out_dtype=OUT_BF16, stream=None):
     A = operand(qx, sx, E4M3, GRAN_1x128)
     B = operand(qw, sw, E4M3, GRAN_128x128)
     return fp8_block_gemm(A, B, x.shape[0], w.shape[0], x.shape[1], out_dtype, mode, stream=stream)
+
+
+def attn_input(q, scales, fmt=E4M3) -> AttnInput:
+    """Describe an attention input: codes [tokens, heads*128] (uint8), scales
+    (Q: [heads, tokens]; K, V: [ceil(tokens/128), heads])."""
+    torch = _torch()
+    _rowmajor(_dev(q, "q", torch.uint8), "q")
+    _dev(scales, "scales", torch.float32)
+    a = AttnInput(data=q.data_ptr(), ld=q.stride(0), fmt=fmt, reserved=0, scales=scales.data_ptr())
+    a._keep = (q, scales)
+    return a
+
+
+def fp8_attention_fwd(Q: AttnInput, K: AttnInput, V: AttnInput, seq_q: int, seq_k: int, heads_q: int,
+                      heads_kv: int, causal=True, softmax_scale=None, o=None, stream=None):
+    """FP8 attention forward over an FP8 KV cache; returns O bf16 [seq_q, heads_q*128]."""
+    torch = _torch()
+    if softmax_scale is None:
+        softmax_scale = 128 ** -0.5
+    if o is None:
+        o = torch.empty((seq_q, heads_q * 128), dtype=torch.bfloat16, device=Q._keep[0].device)
+    _rowmajor(_dev(o, "o", torch.bfloat16), "o")
+    _call("fp8_attention_fwd", seq_q, seq_k, heads_q, heads_kv, 128, int(bool(causal)), float(softmax_scale),
+          ctypes.byref(Q), ctypes.byref(K), ctypes.byref(V), o.data_ptr(), o.stride(0), _stream(stream))
+    return o
 
 
 def device_status(stream=None) -> None:

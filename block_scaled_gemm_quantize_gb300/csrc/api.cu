@@ -10,6 +10,7 @@
 #include <mutex>
 
 #include "fp8bs.h"
+#include "attn_kernels.h"
 #include "gemm_kernels.h"
 #include "quant_kernels.h"
 
@@ -451,6 +452,67 @@ int fp8_grouped_block_gemm_quant(int32_t num_groups, const int32_t* row_offsets,
                     mode, quant_out(Q, ld_q, epilogue, q_fmt, q_mode, q_scales), (cudaStream_t)stream);
 }
 
+int fp8_attention_fwd(int64_t seq_q, int64_t seq_k, int32_t heads_q, int32_t heads_kv, int32_t head_dim,
+                      int32_t causal, float softmax_scale, const fp8bs_attn_input* Q, const fp8bs_attn_input* K,
+                      const fp8bs_attn_input* V, void* O, int64_t ld_o, fp8bs_stream_t stream) {
+    const char* fn = "fp8_attention_fwd";
+    if (seq_q < 0 || seq_k < 0) return fail(FP8BS_ERR_INVALID_ARG, "%s: negative size", fn);
+    if (heads_q < 1 || heads_kv < 1 || heads_q % heads_kv)
+        return fail(FP8BS_ERR_INVALID_ARG, "%s: heads_q must be a positive multiple of heads_kv", fn);
+    if (head_dim != 128) return fail(FP8BS_ERR_UNSUPPORTED, "%s: head_dim must be 128", fn);
+    if (causal != 0 && causal != 1) return fail(FP8BS_ERR_INVALID_ARG, "%s: causal must be 0 or 1", fn);
+    if (!(softmax_scale > 0.0f) || !(softmax_scale < 1e30f))
+        return fail(FP8BS_ERR_INVALID_ARG, "%s: softmax_scale must be positive and finite", fn);
+    if (!Q || !K || !V) return fail(FP8BS_ERR_INVALID_ARG, "%s: null input descriptor", fn);
+    if (seq_q == 0) return FP8BS_OK;
+    if (!O) return fail(FP8BS_ERR_INVALID_ARG, "%s: O is null", fn);
+    const int64_t wq = (int64_t)heads_q * 128, wkv = (int64_t)heads_kv * 128;
+    if (ld_o < wq) return fail(FP8BS_ERR_INVALID_ARG, "%s: ld_o < heads_q * 128", fn);
+    if (!aligned16(O) || (ld_o * 2) % 16) return fail(FP8BS_ERR_MISALIGNED, "%s: O alignment", fn);
+    const fp8bs_attn_input* in[3] = {Q, K, V};
+    const int64_t width[3] = {wq, wkv, wkv};
+    const int64_t rows[3] = {seq_q, seq_k, seq_k};
+    for (int i = 0; i < 3; i++) {
+        if (!valid_fmt(in[i]->fmt) || in[i]->reserved != 0)
+            return fail(FP8BS_ERR_INVALID_ARG, "%s: bad format of input %d", fn, i);
+        if (rows[i] == 0) continue;
+        if (!in[i]->data || !in[i]->scales) return fail(FP8BS_ERR_INVALID_ARG, "%s: null data/scales (%d)", fn, i);
+        if (in[i]->ld < width[i]) return fail(FP8BS_ERR_INVALID_ARG, "%s: ld too small (%d)", fn, i);
+        if (!aligned16(in[i]->data) || in[i]->ld % 16 || !aligned4(in[i]->scales))
+            return fail(FP8BS_ERR_MISALIGNED, "%s: input %d alignment", fn, i);
+    }
+    if (seq_q > (int64_t)INT32_MAX - 256 || seq_k > (int64_t)INT32_MAX - 256 || heads_q > 65535)
+        return fail(FP8BS_ERR_UNSUPPORTED, "%s: dimension too large", fn);
+    int rc;
+    if ((rc = get_encoder()) != FP8BS_OK) return rc;
+    CUtensorMap tmQ, tmK, tmV;
+    if ((rc = make_map(&tmQ, Q->data, wq, seq_q, Q->ld, 128)) != FP8BS_OK) return rc;
+    if (seq_k > 0) {
+        if ((rc = make_map(&tmK, K->data, wkv, seq_k, K->ld, 128)) != FP8BS_OK) return rc;
+        if ((rc = make_map(&tmV, V->data, wkv, seq_k, V->ld, 128)) != FP8BS_OK) return rc;
+    } else {
+        tmK = tmQ;   // never read: no key tile exists
+        tmV = tmQ;
+    }
+    fp8bs::AttnParams p;
+    memset(&p, 0, sizeof(p));
+    p.seq_q = seq_q;
+    p.seq_k = seq_k;
+    p.hq = heads_q;
+    p.hkv = heads_kv;
+    p.causal = causal;
+    p.scale_log2 = softmax_scale * 1.4426950408889634f;
+    p.sq = Q->scales;
+    p.sk = K->scales;
+    p.sv = V->scales;
+    p.o = O;
+    p.ldo = ld_o;
+    p.idesc_s = fp8bs::make_idesc_f8f6f4(Q->fmt, K->fmt, false, false, 128);
+    p.idesc_o = fp8bs::make_idesc_f8f6f4(FP8BS_E4M3, V->fmt, false, true, 128);
+    cudaError_t e = fp8bs::launch_fp8_attn_fwd(tmQ, tmK, tmV, p, (cudaStream_t)stream);
+    return e == cudaSuccess ? FP8BS_OK : cuda_fail(e, fn);
+}
+
 int fp8bs_selftest_wait_timeout(int32_t limit_ms, int32_t* waited_ok, fp8bs_stream_t stream) {
     const char* fn = "fp8bs_selftest_wait_timeout";
     if (!waited_ok) return fail(FP8BS_ERR_INVALID_ARG, "%s: null output", fn);
@@ -463,9 +525,11 @@ int fp8bs_selftest_wait_timeout(int32_t limit_ms, int32_t* waited_ok, fp8bs_stre
 int fp8bs_device_status(fp8bs_stream_t stream) {
     cudaError_t e = cudaStreamSynchronize((cudaStream_t)stream);
     if (e != cudaSuccess) return cuda_fail(e, "fp8bs_device_status");
-    int st = 0;
+    int st = 0, sta = 0;
     e = fp8bs::read_and_clear_status(&st);
+    if (e == cudaSuccess) e = fp8bs::read_and_clear_attn_status(&sta);
     if (e != cudaSuccess) return cuda_fail(e, "fp8bs_device_status");
+    if (sta != 0) st = sta;
     if (st != 0) return fail(FP8BS_ERR_DEVICE_TIMEOUT, "a kernel gave up on a bounded device wait");
     return FP8BS_OK;
 }

@@ -1,0 +1,382 @@
+// attn.cu -- FP8 attention over an FP8 KV cache on sm_103a (tcgen05 + TMA + TMEM).
+//
+// "NVIDIA NeMo RL logra una aceleracion del 48%..." (hotbookzone.com),
+// "Ganancias de rendimiento en el mundo real": extending FP8 to the KV cache
+// and the attention operations takes the speedup from the linear layers'
+// 15-25 % to about 48 %; "El avance tecnico": attention otherwise stays in
+// BF16.  Here both attention products run in FP8 on the tensor cores:
+//   S = Q K^T  (Q one scale per token and head, 1x128; K one scale per 128
+//               tokens and head, 128x128 -- the KV cache layout)
+//   P = exp(S - running max)   in fp32, then E4M3 with the scale 1/448 (its
+//               maximum is 1 by construction)
+//   O = P V    (V per 128 tokens and head), rescaled online in fp32.
+//
+// One CTA per (128 query rows, head), 8 warps:
+//   warp 0     TMA: the Q tile once, then K and V tiles of 128 keys into a
+//              3-stage ring.
+//   warp 1     TMEM owner and MMA issuer: S_j into one of two 128-column TMEM
+//              buffers (4 x tcgen05.mma.kind::f8f6f4, K-major operands), and
+//              O_j = P_j V_j into one of two more (P from shared memory,
+//              K-major; V MN-major), issued one tile behind S so that the
+//              softmax of tile j overlaps the MMAs of tile j+1.
+//   warps 4-7  softmax, one thread per query row (its TMEM lane): two passes
+//              over S_j (row max, then exp2 / row sum / E4M3 codes written
+//              into the 128-byte-swizzled P buffer), then the previous tile's
+//              O partial folded into fp32 registers with the running-max
+//              factor.  At the end O / l is stored as bf16.
+// Every wait is bounded; a role that gives up records the timeout in a
+// status word read by fp8bs_device_status, and the CTA leaves after draining
+// its own asynchronous work.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <cstdint>
+
+#include "attn_kernels.h"
+#include "fp8_math.cuh"
+#include "gemm_kernels.h"
+#include "ptx_sm100.cuh"
+
+namespace fp8bs {
+
+__device__ int g_attn_status;   // 0 = ok, else a negative fp8bs status (bounded wait expired)
+
+namespace {
+
+constexpr int AT_ROWS = 128, AT_KEYS = 128, AT_D = 128;
+constexpr int AT_STAGES = 3;
+constexpr int AT_THREADS = 256;
+constexpr int AT_SM_WARP0 = 4;   // first softmax warp
+constexpr uint32_t AT_TILE = AT_ROWS * AT_D;          // 16 KiB of codes
+constexpr uint32_t AT_Q_OFF = 0;
+constexpr uint32_t AT_KV_OFF = AT_TILE;               // stage s: K at +0, V at +16 KiB
+constexpr uint32_t AT_P_OFF = AT_KV_OFF + AT_STAGES * 2 * AT_TILE;
+constexpr uint32_t AT_BAR_OFF = AT_P_OFF + 2 * AT_TILE;
+// q_full, kv_full[3], kv_empty[3], s_full[2], s_empty[2], p_full[2], p_empty[2],
+// o_full[2], o_empty[2], done
+constexpr int AT_NUM_BARS = 1 + 2 * AT_STAGES + 6 * 2 + 1;
+constexpr uint32_t AT_TMEMSLOT_OFF = AT_BAR_OFF + AT_NUM_BARS * 8;
+constexpr uint32_t AT_SMEM_BYTES = 1024 + AT_TMEMSLOT_OFF + 16;
+static_assert(AT_SMEM_BYTES <= 232448, "shared memory budget (attention)");
+constexpr uint64_t AT_WAIT_NS = 4000000000ull;
+constexpr uint64_t AT_DRAIN_NS = 200000000ull;
+
+__device__ __forceinline__ bool at_wait(uint32_t bar, uint32_t parity) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = global_timer_ns();
+    uint32_t n = 0;
+    while (true) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((++n & 63u) == 0 && global_timer_ns() - t0 > AT_WAIT_NS) {
+            atomicExch(&g_attn_status, kStatusDeviceTimeout);
+            return false;
+        }
+    }
+}
+
+__device__ __forceinline__ bool at_drain(uint32_t bar, uint32_t parity) {
+    const uint64_t t0 = global_timer_ns();
+    while (!mbar_try_wait(bar, parity))
+        if (global_timer_ns() - t0 > AT_DRAIN_NS) return false;
+    return true;
+}
+
+__device__ __forceinline__ float ex2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+// number of 128-key tiles a CTA visits (0: no visible key for any of its rows)
+__device__ __forceinline__ int kv_tiles(const AttnParams& p, int64_t q0) {
+    const int64_t n_all = (p.seq_k + AT_KEYS - 1) / AT_KEYS;
+    if (!p.causal) return static_cast<int>(n_all);
+    const int64_t last_row = min(q0 + AT_ROWS - 1, p.seq_q - 1);
+    const int64_t last_key = min(last_row + (p.seq_k - p.seq_q), p.seq_k - 1);
+    if (last_key < 0) return 0;
+    return static_cast<int>(min(n_all, last_key / AT_KEYS + 1));
+}
+
+__global__ void __launch_bounds__(AT_THREADS, 1)
+    k_fp8_attn_fwd(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                   const __grid_constant__ CUtensorMap tmV, const AttnParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    uint8_t* smem = smem_raw + ((1024u - (raw & 1023u)) & 1023u);
+    const uint32_t sbase = smem_u32(smem);
+    const uint32_t bars = sbase + AT_BAR_OFF;
+    const uint32_t q_full = bars;
+    auto kv_full = [&](int s) { return bars + 8u * (1 + s); };
+    auto kv_empty = [&](int s) { return bars + 8u * (1 + AT_STAGES + s); };
+    auto s_full = [&](int b) { return bars + 8u * (1 + 2 * AT_STAGES + b); };
+    auto s_empty = [&](int b) { return bars + 8u * (3 + 2 * AT_STAGES + b); };
+    auto p_full = [&](int b) { return bars + 8u * (5 + 2 * AT_STAGES + b); };
+    auto p_empty = [&](int b) { return bars + 8u * (7 + 2 * AT_STAGES + b); };
+    auto o_full = [&](int b) { return bars + 8u * (9 + 2 * AT_STAGES + b); };
+    auto o_empty = [&](int b) { return bars + 8u * (11 + 2 * AT_STAGES + b); };
+    const uint32_t done_bar = bars + 8u * (13 + 2 * AT_STAGES);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + AT_TMEMSLOT_OFF);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int h = blockIdx.y;
+    const int g = h / (p.hq / p.hkv);
+    const int64_t q0 = static_cast<int64_t>(blockIdx.x) * AT_ROWS;
+    const int n = kv_tiles(p, q0);
+
+    if (warp == 0 && lane == 0) {
+        tma_prefetch_desc(&tmQ);
+        tma_prefetch_desc(&tmK);
+        tma_prefetch_desc(&tmV);
+        mbar_init(q_full, 1);
+        for (int s = 0; s < AT_STAGES; s++) {
+            mbar_init(kv_full(s), 1);
+            mbar_init(kv_empty(s), 1);
+        }
+        for (int b = 0; b < 2; b++) {
+            mbar_init(s_full(b), 1);
+            mbar_init(s_empty(b), 4);   // the 4 softmax warps
+            mbar_init(p_full(b), 4);
+            mbar_init(p_empty(b), 1);
+            mbar_init(o_full(b), 1);
+            mbar_init(o_empty(b), 4);
+        }
+        mbar_init(done_bar, 1);
+        fence_mbar_init();
+        fence_proxy_async_smem();
+    }
+    if (warp == 1) tmem_alloc(smem_u32(tmem_slot), 512);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ TMA
+        if (lane == 0 && n > 0) {
+            bool ok = true;
+            int issued = 0;
+            mbar_arrive_expect_tx(q_full, AT_TILE);
+            tma_load_2d(sbase + AT_Q_OFF, &tmQ, h * AT_D, static_cast<int32_t>(q0), q_full);
+            for (int j = 0; j < n; j++) {
+                const int s = j % AT_STAGES;
+                if (!at_wait(kv_empty(s), ((j / AT_STAGES) & 1u) ^ 1u)) { ok = false; break; }
+                const uint32_t dst = sbase + AT_KV_OFF + s * 2 * AT_TILE;
+                mbar_arrive_expect_tx(kv_full(s), 2 * AT_TILE);
+                tma_load_2d(dst, &tmK, g * AT_D, j * AT_KEYS, kv_full(s));
+                tma_load_2d(dst + AT_TILE, &tmV, g * AT_D, j * AT_KEYS, kv_full(s));
+                issued++;
+            }
+            at_drain(q_full, 0);   // the Q copy has landed before this thread leaves
+            if (!ok) {
+                for (int i = 0; i < AT_STAGES && i < issued; i++) {
+                    const int j = issued - 1 - i;
+                    at_drain(kv_full(j % AT_STAGES), (j / AT_STAGES) & 1u);
+                }
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA
+        if (lane == 0 && n > 0) {
+            bool ok = at_wait(q_full, 0), issued_mma = false;
+            auto issue_s = [&](int j) -> bool {
+                const int s = j % AT_STAGES, b = j & 1;
+                if (!at_wait(kv_full(s), (j / AT_STAGES) & 1u)) return false;
+                if (!at_wait(s_empty(b), ((j >> 1) & 1u) ^ 1u)) return false;
+                tc_fence_after();
+                const uint32_t kS = sbase + AT_KV_OFF + s * 2 * AT_TILE;
+#pragma unroll
+                for (int k4 = 0; k4 < AT_D / 32; k4++)
+                    mma_f8f6f4(tmem + b * 128, smem_desc_sw128(sbase + AT_Q_OFF + k4 * 32, 16, 1024),
+                               smem_desc_sw128(kS + k4 * 32, 16, 1024), p.idesc_s, k4 > 0 ? 1u : 0u);
+                issued_mma = true;
+                mma_commit(s_full(b));
+                return true;
+            };
+            auto issue_o = [&](int j) -> bool {
+                const int s = j % AT_STAGES, b = j & 1;
+                if (!at_wait(p_full(b), (j >> 1) & 1u)) return false;
+                if (!at_wait(o_empty(b), ((j >> 1) & 1u) ^ 1u)) return false;
+                tc_fence_after();
+                const uint32_t vS = sbase + AT_KV_OFF + s * 2 * AT_TILE + AT_TILE;
+                const uint32_t pS = sbase + AT_P_OFF + b * AT_TILE;
+#pragma unroll
+                for (int k4 = 0; k4 < AT_KEYS / 32; k4++)
+                    // P: K-major (keys contiguous in a row); V: MN-major, one
+                    // 128-wide atom, 32 keys x 128 B further per K step
+                    mma_f8f6f4(tmem + 256 + b * 128, smem_desc_sw128(pS + k4 * 32, 16, 1024),
+                               smem_desc_sw128(vS + k4 * 4096, 1024, 1024), p.idesc_o, k4 > 0 ? 1u : 0u);
+                mma_commit(o_full(b));
+                mma_commit(p_empty(b));
+                mma_commit(kv_empty(s));
+                return true;
+            };
+            if (ok) ok = issue_s(0);
+            for (int j = 0; ok && j < n; j++) {
+                if (j + 1 < n && !issue_s(j + 1)) { ok = false; break; }
+                if (!issue_o(j)) { ok = false; break; }
+            }
+            if (!ok && issued_mma) {
+                mma_commit(done_bar);
+                at_drain(done_bar, 0);
+            }
+        }
+    } else if (warp >= AT_SM_WARP0) {
+        // -------------------------------------------------------- softmax
+        const int quarter = warp & 3;
+        const int r = quarter * 32 + lane;                       // TMEM lane = query row in the tile
+        const int64_t row = q0 + r;
+        const bool row_ok = row < p.seq_q;
+        const int64_t crow = row_ok ? row : p.seq_q - 1;
+        const int64_t last_key =
+            p.causal ? min(crow + (p.seq_k - p.seq_q), p.seq_k - 1) : p.seq_k - 1;
+        const float qs = __ldg(p.sq + static_cast<int64_t>(h) * p.seq_q + crow);
+        const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
+        float m = -INFINITY, l = 0.0f;
+        uint64_t acc[64];   // O row, 128 fp32 as packed pairs
+#pragma unroll
+        for (int i = 0; i < 64; i++) acc[i] = 0;
+        float alpha_prev = 1.0f;
+        bool ok = true;
+
+        // fold O partial of tile t into acc: acc = acc * alpha + partial * sv_t / 448
+        auto consume_o = [&](int t, float alpha) -> bool {
+            const int b = t & 1;
+            if (!__all_sync(0xFFFFFFFFu, at_wait(o_full(b), (t >> 1) & 1u))) return false;
+            tc_fence_after();
+            const float vs = __ldg(p.sv + static_cast<int64_t>(t) * p.hkv + g) * (1.0f / 448.0f);
+            const uint64_t a2 = pack_f32x2(__float_as_uint(alpha), __float_as_uint(alpha));
+            const uint64_t v2 = pack_f32x2(__float_as_uint(vs), __float_as_uint(vs));
+#pragma unroll
+            for (int ch = 0; ch < 4; ch++) {
+                uint32_t rr[32];
+                tmem_ld_32x32b_x32(tmem + lane_off + 256 + b * 128 + ch * 32, rr);
+                tmem_wait_ld();
+                if (ch == 3) {
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(o_empty(b));
+                }
+#pragma unroll
+                for (int q = 0; q < 16; q++) {
+                    const uint64_t pv = mul_f32x2(pack_f32x2(rr[2 * q], rr[2 * q + 1]), v2);
+                    uint64_t a = acc[ch * 16 + q];
+                    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(acc[ch * 16 + q]) : "l"(a), "l"(a2), "l"(pv));
+                }
+            }
+            return true;
+        };
+
+        for (int j = 0; ok && j < n; j++) {
+            const int b = j & 1;
+            ok = __all_sync(0xFFFFFFFFu, at_wait(s_full(b), (j >> 1) & 1u));
+            if (!ok) break;
+            tc_fence_after();
+            const float c = qs * __ldg(p.sk + static_cast<int64_t>(j) * p.hkv + g) * p.scale_log2;
+            const uint32_t sS = tmem + lane_off + b * 128;
+            const int64_t key0 = static_cast<int64_t>(j) * AT_KEYS;
+            // pass 1: row max of the scaled scores (log2 units)
+            float tmax = -INFINITY;
+#pragma unroll
+            for (int ch = 0; ch < 4; ch++) {
+                uint32_t rr[32];
+                tmem_ld_32x32b_x32(sS + ch * 32, rr);
+                tmem_wait_ld();
+#pragma unroll
+                for (int e = 0; e < 32; e++)
+                    if (key0 + ch * 32 + e <= last_key) tmax = fmaxf(tmax, __uint_as_float(rr[e]) * c);
+            }
+            const float m_new = fmaxf(m, tmax);
+            const float alpha = m_new == -INFINITY ? 1.0f : ex2(m - m_new);
+            // pass 2: P = 2^(s - m_new), row sum, E4M3 codes of 448 P into the P buffer
+            ok = __all_sync(0xFFFFFFFFu, at_wait(p_empty(b), ((j >> 1) & 1u) ^ 1u));
+            if (!ok) break;
+            const uint32_t prow = sbase + AT_P_OFF + b * AT_TILE + r * 128;
+            float rsum = 0.0f;
+#pragma unroll
+            for (int ch = 0; ch < 4; ch++) {
+                uint32_t rr[32];
+                tmem_ld_32x32b_x32(sS + ch * 32, rr);
+                tmem_wait_ld();
+                if (ch == 3) {   // S buffer read: hand it back
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(s_empty(b));
+                }
+                float pv[32];
+#pragma unroll
+                for (int e = 0; e < 32; e++) {
+                    const bool vis = key0 + ch * 32 + e <= last_key;
+                    const float pe = vis ? ex2(__uint_as_float(rr[e]) * c - m_new) : 0.0f;
+                    rsum += pe;
+                    pv[e] = pe * 448.0f;
+                }
+#pragma unroll
+                for (int half = 0; half < 2; half++) {   // 16 keys = one 16-byte chunk
+                    uint32_t w[4];
+#pragma unroll
+                    for (int i = 0; i < 4; i++) {
+                        const int e = half * 16 + 4 * i;
+                        w[i] = cvt2<0>(pv[e], pv[e + 1]) | (cvt2<0>(pv[e + 2], pv[e + 3]) << 16);
+                    }
+                    const uint32_t cc = static_cast<uint32_t>(ch * 2 + half);
+                    st_shared_v4(prow + ((cc ^ (static_cast<uint32_t>(r) & 7u)) << 4), w[0], w[1], w[2], w[3]);
+                }
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(p_full(b));
+            l = l * alpha + rsum;
+            m = m_new;
+            if (j > 0) {
+                ok = consume_o(j - 1, alpha_prev);
+                if (!ok) break;
+            }
+            alpha_prev = alpha;
+        }
+        if (ok && n > 0) ok = consume_o(n - 1, alpha_prev);
+        if (ok && row_ok) {
+            const float inv_l = l > 0.0f ? 1.0f / l : 0.0f;
+            uint16_t* o = reinterpret_cast<uint16_t*>(p.o) + row * p.ldo + static_cast<int64_t>(h) * AT_D;
+#pragma unroll
+            for (int c8 = 0; c8 < 16; c8++) {
+                uint32_t w[4];
+#pragma unroll
+                for (int i = 0; i < 4; i++) {
+                    const float2 f = unpack_f32x2(acc[c8 * 4 + i]);
+                    __nv_bfloat162 h2 = __floats2bfloat162_rn(f.x * inv_l, f.y * inv_l);
+                    w[i] = *reinterpret_cast<uint32_t*>(&h2);
+                }
+                *reinterpret_cast<uint4*>(o + c8 * 8) = make_uint4(w[0], w[1], w[2], w[3]);
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, 512);
+    }
+}
+
+}  // namespace
+
+cudaError_t read_and_clear_attn_status(int* status) {
+    int zero = 0;
+    cudaError_t e = cudaMemcpyFromSymbol(status, g_attn_status, sizeof(int));
+    if (e != cudaSuccess) return e;
+    return cudaMemcpyToSymbol(g_attn_status, &zero, sizeof(int));
+}
+
+cudaError_t launch_fp8_attn_fwd(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensorMap& tmV,
+                                const AttnParams& p, cudaStream_t st) {
+    auto k = k_fp8_attn_fwd;
+    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, AT_SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    const int64_t qt = (p.seq_q + AT_ROWS - 1) / AT_ROWS;
+    k<<<dim3(static_cast<unsigned>(qt), static_cast<unsigned>(p.hq)), AT_THREADS, AT_SMEM_BYTES, st>>>(tmQ, tmK,
+                                                                                                        tmV, p);
+    return cudaGetLastError();
+}
+
+}  // namespace fp8bs

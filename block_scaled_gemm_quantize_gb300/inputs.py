@@ -106,3 +106,7 @@ LLAMA31_8B_FPROP_MX = dict(
     name="llama3.1-8b-fprop-mxfp8", M=8192, scale_mode="mx",
     linears=[("qkv", 6144, 4096), ("o", 4096, 4096), ("gate_up", 28672, 4096),
              ("down", 4096, 14336)])
+
+# Llama-3.1-8B attention prefill over an FP8 KV cache: 8192 tokens, 32 query
+# heads sharing 8 key/value heads, head_dim 128, causal.
+LLAMA31_8B_ATTN = dict(name="llama3.1-8b-attn-fp8", seq=8192, heads_q=32, heads_kv=8, causal=True)

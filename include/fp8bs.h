@@ -305,6 +305,44 @@ int fp8_grouped_block_gemm_quant(int32_t num_groups, const int32_t* row_offsets,
                                  int32_t epilogue, int32_t q_fmt, int32_t q_mode,
                                  uint8_t* Q, int64_t ld_q, float* q_scales, fp8bs_stream_t stream);
 
+/* ----------------------------------------------------------- attention */
+
+/* One FP8 input of the attention: codes [rows][ld], head h (of its heads) at
+ * columns 128 h .. 128 h + 127, with its scale table. */
+typedef struct {
+    const uint8_t* data;
+    int64_t ld;            /* bytes between rows (tokens) */
+    int32_t fmt;           /* fp8bs_format */
+    int32_t reserved;      /* must be 0 */
+    const float* scales;
+} fp8bs_attn_input;
+
+/*
+ * FP8 attention over an FP8 KV cache, forward, one sequence ("NVIDIA NeMo RL
+ * logra una aceleracion del 48%...", hotbookzone.com, "Ganancias de
+ * rendimiento en el mundo real": FP8 extended to the KV cache and the
+ * attention operations).  Both products run on the FP8 tensor cores:
+ *   S = scale * deq(Q_h) deq(K_g)^T, masked (causal: key j visible to query
+ *       i iff j <= i + seq_k - seq_q), g = h / (heads_q / heads_kv);
+ *   P = exp(S - running row max) in fp32, quantized to E4M3 with the scale
+ *       1/448 (its maximum is 1), row sums l from the unrounded values;
+ *   O = (P deq(V_g)) / l, accumulated in fp32, stored as bf16.
+ * Scales (readings; the pages give none): Q one per token and head, as the
+ * 1x128 activation tiles -- fp8_quantize_1x128 of the [seq_q][heads_q * 128]
+ * matrix, table [heads_q][seq_q]; K and V (the KV cache) one per 128 tokens
+ * and head, as the 128x128 tiles -- fp8_quantize_128x128 of the
+ * [seq_k][heads_kv * 128] matrices, tables [ceil(seq_k/128)][heads_kv].
+ *   O: bf16 [seq_q][ld_o], head h at columns 128 h.  Rows that see no key
+ *   are 0.  softmax_scale > 0 (typically 1/sqrt(128)).
+ * Errors: INVALID_ARG (sizes, heads_q % heads_kv, nulls, bad format),
+ * UNSUPPORTED (head_dim != 128), MISALIGNED (data and O 16-byte aligned,
+ * ld % 16 bytes, scales 4-byte aligned).
+ */
+int fp8_attention_fwd(int64_t seq_q, int64_t seq_k, int32_t heads_q, int32_t heads_kv, int32_t head_dim,
+                      int32_t causal, float softmax_scale, const fp8bs_attn_input* Q,
+                      const fp8bs_attn_input* K, const fp8bs_attn_input* V, void* O, int64_t ld_o,
+                      fp8bs_stream_t stream);
+
 /* ------------------------------------------------------------ diagnostics */
 
 /* Message for the last non-OK status returned on the calling host thread. */

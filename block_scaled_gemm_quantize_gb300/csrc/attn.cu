@@ -19,11 +19,14 @@
 //              O_j = P_j V_j into one of two more (P from shared memory,
 //              K-major; V MN-major), issued one tile behind S so that the
 //              softmax of tile j overlaps the MMAs of tile j+1.
-//   warps 4-7  softmax, one thread per query row (its TMEM lane): two passes
-//              over S_j (row max, then exp2 / row sum / E4M3 codes written
-//              into the 128-byte-swizzled P buffer), then the previous tile's
-//              O partial folded into fp32 registers with the running-max
-//              factor.  At the end O / l is stored as bf16.
+//   warps 4-11 softmax, two threads per query row (its TMEM lane; warps w
+//              and w + 4 own columns 0-63 and 64-127): one TMEM read of the
+//              thread's 64 scores, the row max exchanged with the partner
+//              through shared memory and a bounded mbarrier, then exp2, the
+//              partial row sum and the E4M3 codes of 448 P written into the
+//              128-byte-swizzled P buffer; then the previous tile's O partial
+//              (the thread's 64 columns) folded into fp32 registers with the
+//              running-max factor.  At the end O / l is stored as bf16.
 // Every wait is bounded; a role that gives up records the timeout in a
 // status word read by fp8bs_device_status, and the CTA leaves after draining
 // its own asynchronous work.
@@ -45,18 +48,22 @@ namespace {
 
 constexpr int AT_ROWS = 128, AT_KEYS = 128, AT_D = 128;
 constexpr int AT_STAGES = 3;
-constexpr int AT_THREADS = 256;
-constexpr int AT_SM_WARP0 = 4;   // first softmax warp
+constexpr int AT_THREADS = 384;
+constexpr int AT_SM_WARP0 = 4;   // first softmax warp (8 softmax warps)
+constexpr int AT_REGS_LOW = 72, AT_REGS_HIGH = 216;   // 128*72 + 256*216 == 384*168
 constexpr uint32_t AT_TILE = AT_ROWS * AT_D;          // 16 KiB of codes
 constexpr uint32_t AT_Q_OFF = 0;
 constexpr uint32_t AT_KV_OFF = AT_TILE;               // stage s: K at +0, V at +16 KiB
 constexpr uint32_t AT_P_OFF = AT_KV_OFF + AT_STAGES * 2 * AT_TILE;
 constexpr uint32_t AT_BAR_OFF = AT_P_OFF + 2 * AT_TILE;
 // q_full, kv_full[3], kv_empty[3], s_full[2], s_empty[2], p_full[2], p_empty[2],
-// o_full[2], o_empty[2], done
-constexpr int AT_NUM_BARS = 1 + 2 * AT_STAGES + 6 * 2 + 1;
+// o_full[2], o_empty[2], done, xchg[4]
+constexpr int AT_NUM_BARS = 1 + 2 * AT_STAGES + 6 * 2 + 1 + 4;
 constexpr uint32_t AT_TMEMSLOT_OFF = AT_BAR_OFF + AT_NUM_BARS * 8;
-constexpr uint32_t AT_SMEM_BYTES = 1024 + AT_TMEMSLOT_OFF + 16;
+// row-max / row-sum exchange between the two threads of a row: [parity][half][row]
+constexpr uint32_t AT_XCHG_OFF = (AT_TMEMSLOT_OFF + 16 + 15) & ~15u;
+constexpr uint32_t AT_SMEM_BYTES = 1024 + AT_XCHG_OFF + 2 * 2 * 128 * 4;
+constexpr float AT_LOG2_448 = 8.807354922057604f;   // log2(448)
 static_assert(AT_SMEM_BYTES <= 232448, "shared memory budget (attention)");
 constexpr uint64_t AT_WAIT_NS = 4000000000ull;
 constexpr uint64_t AT_DRAIN_NS = 200000000ull;
@@ -115,12 +122,14 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
     auto o_full = [&](int b) { return bars + 8u * (9 + 2 * AT_STAGES + b); };
     auto o_empty = [&](int b) { return bars + 8u * (11 + 2 * AT_STAGES + b); };
     const uint32_t done_bar = bars + 8u * (13 + 2 * AT_STAGES);
+    auto xchg_bar = [&](int q) { return bars + 8u * (14 + 2 * AT_STAGES + q); };
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + AT_TMEMSLOT_OFF);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int h = blockIdx.y;
     const int g = h / (p.hq / p.hkv);
-    const int64_t q0 = static_cast<int64_t>(blockIdx.x) * AT_ROWS;
+    // causal: the last query tiles see the most keys, so they start first
+    const int64_t q0 = static_cast<int64_t>(p.causal ? gridDim.x - 1 - blockIdx.x : blockIdx.x) * AT_ROWS;
     const int n = kv_tiles(p, q0);
 
     if (warp == 0 && lane == 0) {
@@ -134,13 +143,14 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
         }
         for (int b = 0; b < 2; b++) {
             mbar_init(s_full(b), 1);
-            mbar_init(s_empty(b), 4);   // the 4 softmax warps
-            mbar_init(p_full(b), 4);
+            mbar_init(s_empty(b), 8);   // the 8 softmax warps
+            mbar_init(p_full(b), 8);
             mbar_init(p_empty(b), 1);
             mbar_init(o_full(b), 1);
-            mbar_init(o_empty(b), 4);
+            mbar_init(o_empty(b), 8);
         }
         mbar_init(done_bar, 1);
+        for (int q = 0; q < 4; q++) mbar_init(xchg_bar(q), 64);   // the two warps of a lane quarter
         fence_mbar_init();
         fence_proxy_async_smem();
     }
@@ -150,6 +160,7 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
+    if (warp < AT_SM_WARP0) asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(AT_REGS_LOW));
     if (warp == 0) {
         // ------------------------------------------------------------ TMA
         if (lane == 0 && n > 0) {
@@ -221,48 +232,63 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
             }
         }
     } else if (warp >= AT_SM_WARP0) {
+        asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(AT_REGS_HIGH));
         // -------------------------------------------------------- softmax
         const int quarter = warp & 3;
+        const int hf = (warp - AT_SM_WARP0) >> 2;                 // column half: 64 hf .. 64 hf + 63
         const int r = quarter * 32 + lane;                       // TMEM lane = query row in the tile
         const int64_t row = q0 + r;
         const bool row_ok = row < p.seq_q;
         const int64_t crow = row_ok ? row : p.seq_q - 1;
-        const int64_t last_key =
-            p.causal ? min(crow + (p.seq_k - p.seq_q), p.seq_k - 1) : p.seq_k - 1;
+        const int64_t offs = p.seq_k - p.seq_q;
+        const int64_t last_key = p.causal ? min(crow + offs, p.seq_k - 1) : p.seq_k - 1;
+        // keys every row of this CTA sees: a tile below this needs no mask
+        const int64_t all_vis = p.causal ? min(q0 + offs, p.seq_k - 1) : p.seq_k - 1;
         const float qs = __ldg(p.sq + static_cast<int64_t>(h) * p.seq_q + crow);
         const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
-        float m = -INFINITY, l = 0.0f;
-        uint64_t acc[64];   // O row, 128 fp32 as packed pairs
+        const uint32_t xbuf = sbase + AT_XCHG_OFF;
+        uint32_t xc = 0;                                          // exchanges done (parity)
+        // exchange v with the row's partner thread; false on timeout
+        auto exchange = [&](float& v, bool take_max) -> bool {
+            const uint32_t par = xc & 1u;
+            st_shared_f32(xbuf + ((par * 2 + hf) * 128 + r) * 4, v);
+            mbar_arrive(xchg_bar(quarter));
+            if (!__all_sync(0xFFFFFFFFu, at_wait(xchg_bar(quarter), par))) return false;
+            const float o = ld_shared_f32(xbuf + ((par * 2 + (hf ^ 1)) * 128 + r) * 4);
+            v = take_max ? fmaxf(v, o) : v + o;
+            xc++;
+            return true;
+        };
+        float m = -INFINITY, l = 0.0f;   // l: this half's sum of 448 P (same max as the partner)
+        uint64_t acc[32];                // O row, this thread's 64 columns as packed pairs
 #pragma unroll
-        for (int i = 0; i < 64; i++) acc[i] = 0;
-        float alpha_prev = 1.0f;
+        for (int i = 0; i < 32; i++) acc[i] = 0;
+        float alpha_prev = 1.0f;   // running-max factor of the tile whose O partial is pending
         bool ok = true;
 
-        // fold O partial of tile t into acc: acc = acc * alpha + partial * sv_t / 448
+        // fold O partial of tile t into acc: acc = acc * alpha + partial * sv_t
         auto consume_o = [&](int t, float alpha) -> bool {
             const int b = t & 1;
             if (!__all_sync(0xFFFFFFFFu, at_wait(o_full(b), (t >> 1) & 1u))) return false;
             tc_fence_after();
-            const float vs = __ldg(p.sv + static_cast<int64_t>(t) * p.hkv + g) * (1.0f / 448.0f);
+            const float vs = __ldg(p.sv + static_cast<int64_t>(t) * p.hkv + g);
             const uint64_t a2 = pack_f32x2(__float_as_uint(alpha), __float_as_uint(alpha));
             const uint64_t v2 = pack_f32x2(__float_as_uint(vs), __float_as_uint(vs));
+            uint32_t rr[2][32];
+            tmem_ld_32x32b_x32(tmem + lane_off + 256 + b * 128 + hf * 64, rr[0]);
+            tmem_ld_32x32b_x32(tmem + lane_off + 256 + b * 128 + hf * 64 + 32, rr[1]);
+            tmem_wait_ld();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(o_empty(b));
 #pragma unroll
-            for (int ch = 0; ch < 4; ch++) {
-                uint32_t rr[32];
-                tmem_ld_32x32b_x32(tmem + lane_off + 256 + b * 128 + ch * 32, rr);
-                tmem_wait_ld();
-                if (ch == 3) {
-                    tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(o_empty(b));
-                }
+            for (int u = 0; u < 2; u++)
 #pragma unroll
                 for (int q = 0; q < 16; q++) {
-                    const uint64_t pv = mul_f32x2(pack_f32x2(rr[2 * q], rr[2 * q + 1]), v2);
-                    uint64_t a = acc[ch * 16 + q];
-                    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(acc[ch * 16 + q]) : "l"(a), "l"(a2), "l"(pv));
+                    const uint64_t pv = mul_f32x2(pack_f32x2(rr[u][2 * q], rr[u][2 * q + 1]), v2);
+                    uint64_t a = acc[u * 16 + q];
+                    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(acc[u * 16 + q]) : "l"(a), "l"(a2), "l"(pv));
                 }
-            }
             return true;
         };
 
@@ -271,62 +297,67 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
             ok = __all_sync(0xFFFFFFFFu, at_wait(s_full(b), (j >> 1) & 1u));
             if (!ok) break;
             tc_fence_after();
+            uint32_t sr[2][32];
+            tmem_ld_32x32b_x32(tmem + lane_off + b * 128 + hf * 64, sr[0]);
+            tmem_ld_32x32b_x32(tmem + lane_off + b * 128 + hf * 64 + 32, sr[1]);
+            tmem_wait_ld();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(s_empty(b));   // S buffer read: hand it back
             const float c = qs * __ldg(p.sk + static_cast<int64_t>(j) * p.hkv + g) * p.scale_log2;
-            const uint32_t sS = tmem + lane_off + b * 128;
-            const int64_t key0 = static_cast<int64_t>(j) * AT_KEYS;
-            // pass 1: row max of the scaled scores (log2 units)
-            float tmax = -INFINITY;
+            const int64_t key0 = static_cast<int64_t>(j) * AT_KEYS + hf * 64;
+            const bool full = static_cast<int64_t>(j) * AT_KEYS + AT_KEYS - 1 <= all_vis;   // CTA-uniform
+            // scores in log2 units are raw * c with c > 0, so the row max is
+            // max(raw) * c; masked keys become -inf.  Eight independent
+            // partial maxima / sums keep the dependency chains short.
+            float tm[8];
 #pragma unroll
-            for (int ch = 0; ch < 4; ch++) {
-                uint32_t rr[32];
-                tmem_ld_32x32b_x32(sS + ch * 32, rr);
-                tmem_wait_ld();
+            for (int i = 0; i < 8; i++) tm[i] = -INFINITY;
 #pragma unroll
-                for (int e = 0; e < 32; e++)
-                    if (key0 + ch * 32 + e <= last_key) tmax = fmaxf(tmax, __uint_as_float(rr[e]) * c);
+            for (int e = 0; e < 64; e++) {
+                float v = __uint_as_float(sr[e >> 5][e & 31]);
+                v = (full || key0 + e <= last_key) ? v : -INFINITY;
+                sr[e >> 5][e & 31] = __float_as_uint(v);
+                tm[e & 7] = fmaxf(tm[e & 7], v);
             }
+            float tmax = fmaxf(fmaxf(fmaxf(tm[0], tm[1]), fmaxf(tm[2], tm[3])),
+                               fmaxf(fmaxf(tm[4], tm[5]), fmaxf(tm[6], tm[7])));
+            tmax = tmax == -INFINITY ? -INFINITY : tmax * c;
+            ok = exchange(tmax, true);
+            if (!ok) break;
             const float m_new = fmaxf(m, tmax);
             const float alpha = m_new == -INFINITY ? 1.0f : ex2(m - m_new);
-            // pass 2: P = 2^(s - m_new), row sum, E4M3 codes of 448 P into the P buffer
+            const float shift = AT_LOG2_448 - (m_new == -INFINITY ? 0.0f : m_new);
             ok = __all_sync(0xFFFFFFFFu, at_wait(p_empty(b), ((j >> 1) & 1u) ^ 1u));
             if (!ok) break;
+            // 448 P = 2^(raw c - m_new + log2 448) (masked: 2^-inf = 0), row sum, codes
             const uint32_t prow = sbase + AT_P_OFF + b * AT_TILE + r * 128;
-            float rsum = 0.0f;
+            float rs[8];
 #pragma unroll
-            for (int ch = 0; ch < 4; ch++) {
-                uint32_t rr[32];
-                tmem_ld_32x32b_x32(sS + ch * 32, rr);
-                tmem_wait_ld();
-                if (ch == 3) {   // S buffer read: hand it back
-                    tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(s_empty(b));
+            for (int i = 0; i < 8; i++) rs[i] = 0.0f;
+#pragma unroll
+            for (int ch = 0; ch < 4; ch++) {                      // 16 keys = one 16-byte chunk
+                float pv[16];
+#pragma unroll
+                for (int e = 0; e < 16; e++) {
+                    const int k = ch * 16 + e;
+                    pv[e] = ex2(fmaf(__uint_as_float(sr[k >> 5][k & 31]), c, shift));
+                    rs[e & 7] += pv[e];
                 }
-                float pv[32];
+                uint32_t w[4];
 #pragma unroll
-                for (int e = 0; e < 32; e++) {
-                    const bool vis = key0 + ch * 32 + e <= last_key;
-                    const float pe = vis ? ex2(__uint_as_float(rr[e]) * c - m_new) : 0.0f;
-                    rsum += pe;
-                    pv[e] = pe * 448.0f;
-                }
-#pragma unroll
-                for (int half = 0; half < 2; half++) {   // 16 keys = one 16-byte chunk
-                    uint32_t w[4];
-#pragma unroll
-                    for (int i = 0; i < 4; i++) {
-                        const int e = half * 16 + 4 * i;
-                        w[i] = cvt2<0>(pv[e], pv[e + 1]) | (cvt2<0>(pv[e + 2], pv[e + 3]) << 16);
-                    }
-                    const uint32_t cc = static_cast<uint32_t>(ch * 2 + half);
-                    st_shared_v4(prow + ((cc ^ (static_cast<uint32_t>(r) & 7u)) << 4), w[0], w[1], w[2], w[3]);
-                }
+                for (int i = 0; i < 4; i++)
+                    w[i] = cvt2<0>(pv[4 * i], pv[4 * i + 1]) | (cvt2<0>(pv[4 * i + 2], pv[4 * i + 3]) << 16);
+                const uint32_t cc = static_cast<uint32_t>(hf * 4 + ch);
+                st_shared_v4(prow + ((cc ^ (static_cast<uint32_t>(r) & 7u)) << 4), w[0], w[1], w[2], w[3]);
             }
+            const float rsum = ((rs[0] + rs[1]) + (rs[2] + rs[3])) + ((rs[4] + rs[5]) + (rs[6] + rs[7]));
             fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) mbar_arrive(p_full(b));
             l = l * alpha + rsum;
             m = m_new;
+            // the previous tile's O partial (its MMA ran during this tile's softmax)
             if (j > 0) {
                 ok = consume_o(j - 1, alpha_prev);
                 if (!ok) break;
@@ -334,11 +365,13 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
             alpha_prev = alpha;
         }
         if (ok && n > 0) ok = consume_o(n - 1, alpha_prev);
+        if (ok && n > 0) ok = exchange(l, false);                 // row sum of both halves
         if (ok && row_ok) {
+            // O = sum(448 P * V * sv) / sum(448 P)
             const float inv_l = l > 0.0f ? 1.0f / l : 0.0f;
-            uint16_t* o = reinterpret_cast<uint16_t*>(p.o) + row * p.ldo + static_cast<int64_t>(h) * AT_D;
+            uint16_t* o = reinterpret_cast<uint16_t*>(p.o) + row * p.ldo + static_cast<int64_t>(h) * AT_D + hf * 64;
 #pragma unroll
-            for (int c8 = 0; c8 < 16; c8++) {
+            for (int c8 = 0; c8 < 8; c8++) {
                 uint32_t w[4];
 #pragma unroll
                 for (int i = 0; i < 4; i++) {

@@ -19,13 +19,14 @@
 //              O_j = P_j V_j into one of two more (P from shared memory,
 //              K-major; V MN-major), issued one tile behind S so that the
 //              softmax of tile j overlaps the MMAs of tile j+1.
-//   warps 4-11 softmax, two threads per query row (its TMEM lane; warps w
-//              and w + 4 own columns 0-63 and 64-127): one TMEM read of the
-//              thread's 64 scores, the row max exchanged with the partner
-//              through shared memory and a bounded mbarrier, then exp2, the
-//              partial row sum and the E4M3 codes of 448 P written into the
+//   warps 4..  softmax, AT_SPLIT threads per query row (its TMEM lane; the
+//              warps w, w + 4, ... of a lane quarter own consecutive
+//              128/AT_SPLIT-column parts): one TMEM read of the thread's
+//              scores, the row max exchanged among the row's threads through
+//              shared memory and a bounded mbarrier, then exp2, the partial row
+//              sum and the E4M3 codes of 448 P written into the
 //              128-byte-swizzled P buffer; then the previous tile's O partial
-//              (the thread's 64 columns) folded into fp32 registers with the
+//              (the thread's columns) folded into fp32 registers with the
 //              running-max factor.  At the end O / l is stored as bf16.
 // Every wait is bounded; a role that gives up records the timeout in a
 // status word read by fp8bs_device_status, and the CTA leaves after draining
@@ -48,9 +49,22 @@ namespace {
 
 constexpr int AT_ROWS = 128, AT_KEYS = 128, AT_D = 128;
 constexpr int AT_STAGES = 3;
-constexpr int AT_THREADS = 384;
-constexpr int AT_SM_WARP0 = 4;   // first softmax warp (8 softmax warps)
-constexpr int AT_REGS_LOW = 72, AT_REGS_HIGH = 216;   // 128*72 + 256*216 == 384*168
+#ifndef FP8BS_ATTN_SPLIT
+#define FP8BS_ATTN_SPLIT 2
+#endif
+// softmax threads per query row: each owns 128 / AT_SPLIT columns of S and O
+constexpr int AT_SPLIT = FP8BS_ATTN_SPLIT;
+constexpr int AT_CPT = 128 / AT_SPLIT;
+constexpr int AT_SM_WARPS = 4 * AT_SPLIT;
+constexpr int AT_THREADS = 128 + 32 * AT_SM_WARPS;
+constexpr int AT_SM_WARP0 = 4;   // first softmax warp
+// setmaxnreg split of the launch's registers (65536 / threads, in steps of 8)
+constexpr int AT_REGS_LAUNCH = (65536 / AT_THREADS) & ~7;
+constexpr int AT_REGS_LOW = 56;
+constexpr int AT_REGS_HIGH =
+    ((AT_REGS_LAUNCH * AT_THREADS - 128 * AT_REGS_LOW) / (32 * AT_SM_WARPS)) & ~7;
+static_assert(AT_REGS_HIGH <= 256 && 128 * AT_REGS_LOW + 32 * AT_SM_WARPS * AT_REGS_HIGH <=
+                                         AT_REGS_LAUNCH * AT_THREADS, "register split");
 constexpr uint32_t AT_TILE = AT_ROWS * AT_D;          // 16 KiB of codes
 constexpr uint32_t AT_Q_OFF = 0;
 constexpr uint32_t AT_KV_OFF = AT_TILE;               // stage s: K at +0, V at +16 KiB
@@ -60,9 +74,9 @@ constexpr uint32_t AT_BAR_OFF = AT_P_OFF + 2 * AT_TILE;
 // o_full[2], o_empty[2], done, xchg[4]
 constexpr int AT_NUM_BARS = 1 + 2 * AT_STAGES + 6 * 2 + 1 + 4;
 constexpr uint32_t AT_TMEMSLOT_OFF = AT_BAR_OFF + AT_NUM_BARS * 8;
-// row-max / row-sum exchange between the two threads of a row: [parity][half][row]
+// row-max / row-sum exchange among the threads of a row: [parity][part][row]
 constexpr uint32_t AT_XCHG_OFF = (AT_TMEMSLOT_OFF + 16 + 15) & ~15u;
-constexpr uint32_t AT_SMEM_BYTES = 1024 + AT_XCHG_OFF + 2 * 2 * 128 * 4;
+constexpr uint32_t AT_SMEM_BYTES = 1024 + AT_XCHG_OFF + 2 * AT_SPLIT * 128 * 4;
 constexpr float AT_LOG2_448 = 8.807354922057604f;   // log2(448)
 static_assert(AT_SMEM_BYTES <= 232448, "shared memory budget (attention)");
 constexpr uint64_t AT_WAIT_NS = 4000000000ull;
@@ -143,14 +157,14 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
         }
         for (int b = 0; b < 2; b++) {
             mbar_init(s_full(b), 1);
-            mbar_init(s_empty(b), 8);   // the 8 softmax warps
-            mbar_init(p_full(b), 8);
+            mbar_init(s_empty(b), AT_SM_WARPS);   // one arrival per softmax warp
+            mbar_init(p_full(b), AT_SM_WARPS);
             mbar_init(p_empty(b), 1);
             mbar_init(o_full(b), 1);
-            mbar_init(o_empty(b), 8);
+            mbar_init(o_empty(b), AT_SM_WARPS);
         }
         mbar_init(done_bar, 1);
-        for (int q = 0; q < 4; q++) mbar_init(xchg_bar(q), 64);   // the two warps of a lane quarter
+        for (int q = 0; q < 4; q++) mbar_init(xchg_bar(q), 32 * AT_SPLIT);   // the warps of a lane quarter
         fence_mbar_init();
         fence_proxy_async_smem();
     }
@@ -235,7 +249,7 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
         asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(AT_REGS_HIGH));
         // -------------------------------------------------------- softmax
         const int quarter = warp & 3;
-        const int hf = (warp - AT_SM_WARP0) >> 2;                 // column half: 64 hf .. 64 hf + 63
+        const int cq = (warp - AT_SM_WARP0) >> 2;                 // column part: AT_CPT cq ..
         const int r = quarter * 32 + lane;                       // TMEM lane = query row in the tile
         const int64_t row = q0 + r;
         const bool row_ok = row < p.seq_q;
@@ -246,43 +260,49 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
         const int64_t all_vis = p.causal ? min(q0 + offs, p.seq_k - 1) : p.seq_k - 1;
         const float qs = __ldg(p.sq + static_cast<int64_t>(h) * p.seq_q + crow);
         const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
+        const uint32_t col_off = static_cast<uint32_t>(cq * AT_CPT);
         const uint32_t xbuf = sbase + AT_XCHG_OFF;
         uint32_t xc = 0;                                          // exchanges done (parity)
-        // exchange v with the row's partner thread; false on timeout
+        // combine v over the row's AT_SPLIT threads (max or sum); false on timeout
         auto exchange = [&](float& v, bool take_max) -> bool {
             const uint32_t par = xc & 1u;
-            st_shared_f32(xbuf + ((par * 2 + hf) * 128 + r) * 4, v);
+            st_shared_f32(xbuf + ((par * AT_SPLIT + cq) * 128 + r) * 4, v);
             mbar_arrive(xchg_bar(quarter));
             if (!__all_sync(0xFFFFFFFFu, at_wait(xchg_bar(quarter), par))) return false;
-            const float o = ld_shared_f32(xbuf + ((par * 2 + (hf ^ 1)) * 128 + r) * 4);
-            v = take_max ? fmaxf(v, o) : v + o;
+            float t = take_max ? -INFINITY : 0.0f;
+#pragma unroll
+            for (int k = 0; k < AT_SPLIT; k++) {
+                const float o = ld_shared_f32(xbuf + ((par * AT_SPLIT + k) * 128 + r) * 4);
+                t = take_max ? fmaxf(t, o) : t + o;
+            }
+            v = t;
             xc++;
             return true;
         };
-        float m = -INFINITY, l = 0.0f;   // l: this half's sum of 448 P (same max as the partner)
-        uint64_t acc[32];                // O row, this thread's 64 columns as packed pairs
+        float m = -INFINITY, l = 0.0f;   // l: this part's sum of 448 P (same max for all parts)
+        uint64_t acc[AT_CPT / 2];        // this thread's O columns as packed pairs
 #pragma unroll
-        for (int i = 0; i < 32; i++) acc[i] = 0;
+        for (int i = 0; i < AT_CPT / 2; i++) acc[i] = 0;
         float alpha_prev = 1.0f;   // running-max factor of the tile whose O partial is pending
         bool ok = true;
 
         // fold O partial of tile t into acc: acc = acc * alpha + partial * sv_t
-        auto consume_o = [&](int t, float alpha) -> bool {
+        auto consume_o = [&](int t, float alpha, float vs) -> bool {
             const int b = t & 1;
             if (!__all_sync(0xFFFFFFFFu, at_wait(o_full(b), (t >> 1) & 1u))) return false;
             tc_fence_after();
-            const float vs = __ldg(p.sv + static_cast<int64_t>(t) * p.hkv + g);
             const uint64_t a2 = pack_f32x2(__float_as_uint(alpha), __float_as_uint(alpha));
             const uint64_t v2 = pack_f32x2(__float_as_uint(vs), __float_as_uint(vs));
-            uint32_t rr[2][32];
-            tmem_ld_32x32b_x32(tmem + lane_off + 256 + b * 128 + hf * 64, rr[0]);
-            tmem_ld_32x32b_x32(tmem + lane_off + 256 + b * 128 + hf * 64 + 32, rr[1]);
+            uint32_t rr[AT_CPT / 32][32];
+#pragma unroll
+            for (int u = 0; u < AT_CPT / 32; u++)
+                tmem_ld_32x32b_x32(tmem + lane_off + 256 + b * 128 + col_off + u * 32, rr[u]);
             tmem_wait_ld();
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(o_empty(b));
 #pragma unroll
-            for (int u = 0; u < 2; u++)
+            for (int u = 0; u < AT_CPT / 32; u++)
 #pragma unroll
                 for (int q = 0; q < 16; q++) {
                     const uint64_t pv = mul_f32x2(pack_f32x2(rr[u][2 * q], rr[u][2 * q + 1]), v2);
@@ -292,20 +312,28 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
             return true;
         };
 
+        // K and V tile scales, loaded one tile ahead (off the per-tile path)
+        auto ksc = [&](int t) { return t < n ? __ldg(p.sk + static_cast<int64_t>(t) * p.hkv + g) : 0.0f; };
+        auto vsc = [&](int t) { return t < n ? __ldg(p.sv + static_cast<int64_t>(t) * p.hkv + g) : 0.0f; };
+        float sk_cur = ksc(0), sk_next = ksc(1), sv_prev = 0.0f, sv_cur = vsc(0);
         for (int j = 0; ok && j < n; j++) {
             const int b = j & 1;
+            const float sk_j = sk_cur, sv_j = sv_cur;
+            sk_cur = sk_next;
+            sk_next = ksc(j + 2);
+            sv_cur = vsc(j + 1);
             ok = __all_sync(0xFFFFFFFFu, at_wait(s_full(b), (j >> 1) & 1u));
             if (!ok) break;
             tc_fence_after();
-            uint32_t sr[2][32];
-            tmem_ld_32x32b_x32(tmem + lane_off + b * 128 + hf * 64, sr[0]);
-            tmem_ld_32x32b_x32(tmem + lane_off + b * 128 + hf * 64 + 32, sr[1]);
+            uint32_t sr[AT_CPT / 32][32];
+#pragma unroll
+            for (int u = 0; u < AT_CPT / 32; u++) tmem_ld_32x32b_x32(tmem + lane_off + b * 128 + col_off + u * 32, sr[u]);
             tmem_wait_ld();
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(s_empty(b));   // S buffer read: hand it back
-            const float c = qs * __ldg(p.sk + static_cast<int64_t>(j) * p.hkv + g) * p.scale_log2;
-            const int64_t key0 = static_cast<int64_t>(j) * AT_KEYS + hf * 64;
+            const float c = qs * sk_j * p.scale_log2;
+            const int64_t key0 = static_cast<int64_t>(j) * AT_KEYS + col_off;
             const bool full = static_cast<int64_t>(j) * AT_KEYS + AT_KEYS - 1 <= all_vis;   // CTA-uniform
             // scores in log2 units are raw * c with c > 0, so the row max is
             // max(raw) * c; masked keys become -inf.  Eight independent
@@ -314,7 +342,7 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
 #pragma unroll
             for (int i = 0; i < 8; i++) tm[i] = -INFINITY;
 #pragma unroll
-            for (int e = 0; e < 64; e++) {
+            for (int e = 0; e < AT_CPT; e++) {
                 float v = __uint_as_float(sr[e >> 5][e & 31]);
                 v = (full || key0 + e <= last_key) ? v : -INFINITY;
                 sr[e >> 5][e & 31] = __float_as_uint(v);
@@ -336,7 +364,7 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
 #pragma unroll
             for (int i = 0; i < 8; i++) rs[i] = 0.0f;
 #pragma unroll
-            for (int ch = 0; ch < 4; ch++) {                      // 16 keys = one 16-byte chunk
+            for (int ch = 0; ch < AT_CPT / 16; ch++) {            // 16 keys = one 16-byte chunk
                 float pv[16];
 #pragma unroll
                 for (int e = 0; e < 16; e++) {
@@ -348,7 +376,7 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
 #pragma unroll
                 for (int i = 0; i < 4; i++)
                     w[i] = cvt2<0>(pv[4 * i], pv[4 * i + 1]) | (cvt2<0>(pv[4 * i + 2], pv[4 * i + 3]) << 16);
-                const uint32_t cc = static_cast<uint32_t>(hf * 4 + ch);
+                const uint32_t cc = col_off / 16 + static_cast<uint32_t>(ch);
                 st_shared_v4(prow + ((cc ^ (static_cast<uint32_t>(r) & 7u)) << 4), w[0], w[1], w[2], w[3]);
             }
             const float rsum = ((rs[0] + rs[1]) + (rs[2] + rs[3])) + ((rs[4] + rs[5]) + (rs[6] + rs[7]));
@@ -359,19 +387,20 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
             m = m_new;
             // the previous tile's O partial (its MMA ran during this tile's softmax)
             if (j > 0) {
-                ok = consume_o(j - 1, alpha_prev);
+                ok = consume_o(j - 1, alpha_prev, sv_prev);
                 if (!ok) break;
             }
             alpha_prev = alpha;
+            sv_prev = sv_j;
         }
-        if (ok && n > 0) ok = consume_o(n - 1, alpha_prev);
-        if (ok && n > 0) ok = exchange(l, false);                 // row sum of both halves
+        if (ok && n > 0) ok = consume_o(n - 1, alpha_prev, sv_prev);
+        if (ok && n > 0) ok = exchange(l, false);                 // row sum over all parts
         if (ok && row_ok) {
             // O = sum(448 P * V * sv) / sum(448 P)
             const float inv_l = l > 0.0f ? 1.0f / l : 0.0f;
-            uint16_t* o = reinterpret_cast<uint16_t*>(p.o) + row * p.ldo + static_cast<int64_t>(h) * AT_D + hf * 64;
+            uint16_t* o = reinterpret_cast<uint16_t*>(p.o) + row * p.ldo + static_cast<int64_t>(h) * AT_D + col_off;
 #pragma unroll
-            for (int c8 = 0; c8 < 8; c8++) {
+            for (int c8 = 0; c8 < AT_CPT / 8; c8++) {
                 uint32_t w[4];
 #pragma unroll
                 for (int i = 0; i < 4; i++) {

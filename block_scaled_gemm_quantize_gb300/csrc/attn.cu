@@ -341,12 +341,18 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
             float tm[8];
 #pragma unroll
             for (int i = 0; i < 8; i++) tm[i] = -INFINITY;
+            if (full) {   // every key of the tile is visible to every row of the CTA
 #pragma unroll
-            for (int e = 0; e < AT_CPT; e++) {
-                float v = __uint_as_float(sr[e >> 5][e & 31]);
-                v = (full || key0 + e <= last_key) ? v : -INFINITY;
-                sr[e >> 5][e & 31] = __float_as_uint(v);
-                tm[e & 7] = fmaxf(tm[e & 7], v);
+                for (int e = 0; e < AT_CPT; e++) tm[e & 7] = fmaxf(tm[e & 7], __uint_as_float(sr[e >> 5][e & 31]));
+            } else {      // keys e <= lim are visible to this row
+                const int lim = static_cast<int>(max(min(last_key - key0, static_cast<int64_t>(AT_CPT)),
+                                                     static_cast<int64_t>(-1)));
+#pragma unroll
+                for (int e = 0; e < AT_CPT; e++) {
+                    const float v = e <= lim ? __uint_as_float(sr[e >> 5][e & 31]) : -INFINITY;
+                    sr[e >> 5][e & 31] = __float_as_uint(v);
+                    tm[e & 7] = fmaxf(tm[e & 7], v);
+                }
             }
             float tmax = fmaxf(fmaxf(fmaxf(tm[0], tm[1]), fmaxf(tm[2], tm[3])),
                                fmaxf(fmaxf(tm[4], tm[5]), fmaxf(tm[6], tm[7])));
@@ -375,7 +381,7 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
                 uint32_t w[4];
 #pragma unroll
                 for (int i = 0; i < 4; i++)
-                    w[i] = cvt2<0>(pv[4 * i], pv[4 * i + 1]) | (cvt2<0>(pv[4 * i + 2], pv[4 * i + 3]) << 16);
+                    w[i] = cvt4_e4m3(pv[4 * i], pv[4 * i + 1], pv[4 * i + 2], pv[4 * i + 3]);
                 const uint32_t cc = col_off / 16 + static_cast<uint32_t>(ch);
                 st_shared_v4(prow + ((cc ^ (static_cast<uint32_t>(r) & 7u)) << 4), w[0], w[1], w[2], w[3]);
             }

@@ -91,6 +91,19 @@ __device__ __forceinline__ uint32_t cvt2(float lo, float hi) {
     return r;
 }
 
+// Four fp32 values -> four E4M3 codes in one word (element 0 in the low byte),
+// the two halves packed by a register-pair move.
+__device__ __forceinline__ uint32_t cvt4_e4m3(float a, float b, float c, float d) {
+    uint32_t w;
+    asm("{\n.reg .b16 lo, hi;\n"
+        "cvt.rn.satfinite.e4m3x2.f32 lo, %2, %1;\n"
+        "cvt.rn.satfinite.e4m3x2.f32 hi, %4, %3;\n"
+        "mov.b32 %0, {lo, hi};\n}"
+        : "=r"(w)
+        : "f"(a), "f"(b), "f"(c), "f"(d));
+    return w;
+}
+
 __device__ __forceinline__ uint32_t cvt2_rt(float lo, float hi, int fmt) {
     return fmt == 0 ? cvt2<0>(lo, hi) : cvt2<1>(lo, hi);
 }

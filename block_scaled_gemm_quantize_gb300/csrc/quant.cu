@@ -70,12 +70,45 @@ __device__ __forceinline__ void quant8(const float (&f)[8], float r, uint32_t& l
 // K block, x = group of 16*U rows; the 16 half-warps of a CTA take 16
 // consecutive rows, so each of the U rounds writes 16 consecutive scales, and
 // each thread keeps U loads in flight.
+#ifndef FP8BS_Q1_ALONG_K
+#define FP8BS_Q1_ALONG_K 1
+#endif
 template <int FMT, int MODE, int U>
 __global__ void __launch_bounds__(256) k_quant_1x128(const uint16_t* __restrict__ x, int64_t rows,
-                                                    int64_t ldx, uint8_t* __restrict__ q, int64_t ldq,
-                                                    float* __restrict__ scales) {
+                                                    int64_t ldx, int64_t nkb, uint8_t* __restrict__ q,
+                                                    int64_t ldq, float* __restrict__ scales) {
     const int l16 = threadIdx.x & 15;
     const int hw = threadIdx.x >> 4;
+#if FP8BS_Q1_ALONG_K
+    // a half-warp walks U consecutive K blocks of one row (U x 256 contiguous bytes)
+    const int64_t r = static_cast<int64_t>(blockIdx.x) * 16 + hw;
+    const int64_t kb0 = static_cast<int64_t>(blockIdx.y) * U;
+    const bool rok = r < rows;
+    const uint16_t* xr = x + r * ldx + kb0 * 128 + l16 * 8;
+    uint4 v[U];
+#pragma unroll
+    for (int i = 0; i < U; i++) {
+        v[i] = make_uint4(0, 0, 0, 0);
+        if (rok && kb0 + i < nkb) v[i] = ld_stream_v4(xr + i * 128);
+    }
+#pragma unroll
+    for (int i = 0; i < U; i++) {
+        const int64_t kb = kb0 + i;
+        float f[8];
+        unpack8(v[i], f);
+        float m = amax8(f);
+#pragma unroll
+        for (int o = 8; o >= 1; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
+        if (rok && kb < nkb) {
+            const float s = block_scale<FMT, MODE>(m);
+            const float rc = __frcp_rn(s);
+            uint32_t lo, hi;
+            quant8<FMT>(f, rc, lo, hi);
+            st_v2(q + r * ldq + kb * 128 + l16 * 8, lo, hi);
+            if (l16 == 0) scales[kb * rows + r] = s;
+        }
+    }
+#else
     const int64_t kb = blockIdx.y;
     const int64_t r0 = static_cast<int64_t>(blockIdx.x) * (16 * U) + hw;
     const uint16_t* xk = x + kb * 128 + l16 * 8;
@@ -103,6 +136,8 @@ __global__ void __launch_bounds__(256) k_quant_1x128(const uint16_t* __restrict_
             if (l16 == 0) scales[kb * rows + r] = s;
         }
     }
+    (void)nkb;
+#endif
 }
 
 // -------------------------------------------------------------- 128x128
@@ -392,11 +427,16 @@ constexpr int kUT = FP8BS_UT;   // vectors in flight per thread (per-tensor)
 cudaError_t launch_quant_1x128(const uint16_t* x, int64_t rows, int64_t cols, int64_t ldx,
                                int fmt, int mode, uint8_t* q, int64_t ldq, float* scales,
                                cudaStream_t st) {
-    const int64_t gx = (rows + 16 * kU1 - 1) / (16 * kU1), gy = cols / 128;
+    const int64_t nkb = cols / 128;
+#if FP8BS_Q1_ALONG_K
+    const int64_t gx = (rows + 15) / 16, gy = (nkb + kU1 - 1) / kU1;
+#else
+    const int64_t gx = (rows + 16 * kU1 - 1) / (16 * kU1), gy = nkb;
+#endif
     if (gx > 0x7FFFFFFF || gy > 65535) return cudaErrorInvalidValue;
     auto k = fmt == 0 ? (mode == 0 ? k_quant_1x128<0, 0, kU1> : k_quant_1x128<0, 1, kU1>)
                       : (mode == 0 ? k_quant_1x128<1, 0, kU1> : k_quant_1x128<1, 1, kU1>);
-    k<<<dim3(static_cast<unsigned>(gx), static_cast<unsigned>(gy)), 256, 0, st>>>(x, rows, ldx, q, ldq,
+    k<<<dim3(static_cast<unsigned>(gx), static_cast<unsigned>(gy)), 256, 0, st>>>(x, rows, ldx, nkb, q, ldq,
                                                                                  scales);
     return cudaGetLastError();
 }

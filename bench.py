@@ -78,6 +78,17 @@ def _dist():
             int(os.environ.get("LOCAL_RANK", "0")))
 
 
+def dominant_kernel(wl):
+    """Name of the kernel the roofline object describes (the workload's
+    products): the attention kernel, the block-scaled (MX) GEMM for power-of-two
+    or 1x32 scales on K-major operands, else the promotion GEMM."""
+    if isinstance(wl, Attn):
+        return "k_fp8_attn_fwd"
+    if getattr(wl, "mx", False) or (isinstance(wl, (Fprop, FusedMlp)) and wl.mode == wl.fp8.SCALE_POW2):
+        return "k_fp8_gemm_mx"
+    return "k_fp8_gemm"
+
+
 class Clocks:
     """nvidia-smi sampler running while the timed region runs."""
 
@@ -826,7 +837,7 @@ def run_ours(args):
         "vs_baseline": None, "dtype": "e4m3/e5m2 (fp32 accumulate)", "data": "synthetic",
         "config": config,
         "pct_of_fp8_peak": 100.0 * value / fp8_peak,
-        "roofline": {"bound": "tensor", "kernel": "k_fp8_gemm", "achieved": achieved,
+        "roofline": {"bound": "tensor", "kernel": dominant_kernel(wl), "achieved": achieved,
                      "peak": fp8_peak, "unit": "TFLOP/s", "frac": achieved / fp8_peak,
                      "traffic": traffic, "traffic_unit": "bytes per launch (mean, ncu)",
                      "peak_src": f"{peaks['src']}: 2 x bf16_tflops_sustained "

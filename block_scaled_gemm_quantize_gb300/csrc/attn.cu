@@ -312,16 +312,21 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
             return true;
         };
 
-        // K and V tile scales, loaded one tile ahead (off the per-tile path)
+        // K and V tile scales: lane i holds those of tile 32 w + i while the
+        // loop is in window w (reloaded every 32 tiles) and a tile's pair is
+        // taken by a shuffle.  A global load issued every tile would hold up
+        // the warp's next TMEM-load wait until it lands.
         auto ksc = [&](int t) { return t < n ? __ldg(p.sk + static_cast<int64_t>(t) * p.hkv + g) : 0.0f; };
         auto vsc = [&](int t) { return t < n ? __ldg(p.sv + static_cast<int64_t>(t) * p.hkv + g) : 0.0f; };
-        float sk_cur = ksc(0), sk_next = ksc(1), sv_prev = 0.0f, sv_cur = vsc(0);
+        float skw = 0.0f, svw = 0.0f, sv_prev = 0.0f;
         for (int j = 0; ok && j < n; j++) {
             const int b = j & 1;
-            const float sk_j = sk_cur, sv_j = sv_cur;
-            sk_cur = sk_next;
-            sk_next = ksc(j + 2);
-            sv_cur = vsc(j + 1);
+            if ((j & 31) == 0) {
+                skw = ksc(j + lane);
+                svw = vsc(j + lane);
+            }
+            const float sk_j = __shfl_sync(0xFFFFFFFFu, skw, j & 31);
+            const float sv_j = __shfl_sync(0xFFFFFFFFu, svw, j & 31);
             ok = __all_sync(0xFFFFFFFFu, at_wait(s_full(b), (j >> 1) & 1u));
             if (!ok) break;
             tc_fence_after();

@@ -11,7 +11,7 @@
 //               maximum is 1 by construction)
 //   O = P V    (V per 128 tokens and head), rescaled online in fp32.
 //
-// One CTA per (128 query rows, head), 8 warps:
+// One CTA per (128 query rows, head), 16 warps:
 //   warp 0     TMA: the Q tile once, then K and V tiles of 128 keys into a
 //              3-stage ring.
 //   warp 1     TMEM owner and MMA issuer: S_j into one of two 128-column TMEM
@@ -19,15 +19,18 @@
 //              O_j = P_j V_j into one of two more (P from shared memory,
 //              K-major; V MN-major), issued one tile behind S so that the
 //              softmax of tile j overlaps the MMAs of tile j+1.
-//   warps 4..  softmax, AT_SPLIT threads per query row (its TMEM lane; the
+//   warps 4-11 softmax, AT_SPLIT threads per query row (its TMEM lane; the
 //              warps w, w + 4, ... of a lane quarter own consecutive
 //              128/AT_SPLIT-column parts): one TMEM read of the thread's
 //              scores, the row max exchanged among the row's threads through
-//              shared memory and a bounded mbarrier, then exp2, the partial row
-//              sum and the E4M3 codes of 448 P written into the
-//              128-byte-swizzled P buffer; then the previous tile's O partial
-//              (the thread's columns) folded into fp32 registers with the
-//              running-max factor.  At the end O / l is stored as bf16.
+//              shared memory and a bounded mbarrier, the tile's running-max
+//              factor handed to the correction warps, then exp2, the partial
+//              row sum and the E4M3 codes of 448 P written into the
+//              128-byte-swizzled P buffer.
+//   warps 12-15 O correction, one thread per query row: each tile's O partial
+//              read from TMEM and folded into the row's 128 fp32 accumulators
+//              with the running-max factor and the V tile's scale, off the
+//              softmax warps' path.  At the end O / l is stored as bf16.
 // Every wait is bounded; a role that gives up records the timeout in a
 // status word read by fp8bs_device_status, and the CTA leaves after draining
 // its own asynchronous work.
@@ -56,27 +59,36 @@ constexpr int AT_STAGES = 3;
 constexpr int AT_SPLIT = FP8BS_ATTN_SPLIT;
 constexpr int AT_CPT = 128 / AT_SPLIT;
 constexpr int AT_SM_WARPS = 4 * AT_SPLIT;
-constexpr int AT_THREADS = 128 + 32 * AT_SM_WARPS;
-constexpr int AT_SM_WARP0 = 4;   // first softmax warp
-// setmaxnreg split of the launch's registers (65536 / threads, in steps of 8)
+constexpr int AT_SM_WARP0 = 4;                            // first softmax warp
+constexpr int AT_CO_WARP0 = AT_SM_WARP0 + AT_SM_WARPS;    // first O-correction warp (4 of them)
+constexpr int AT_THREADS = 128 + 32 * AT_SM_WARPS + 128;
+// setmaxnreg split of the launch's registers (65536 / threads, in steps of 8):
+// control warps, softmax warps, O-correction warps (128 fp32 accumulators)
 constexpr int AT_REGS_LAUNCH = (65536 / AT_THREADS) & ~7;
-constexpr int AT_REGS_LOW = 56;
+constexpr int AT_REGS_LOW = 48;
+constexpr int AT_REGS_CO = 176;
 constexpr int AT_REGS_HIGH =
-    ((AT_REGS_LAUNCH * AT_THREADS - 128 * AT_REGS_LOW) / (32 * AT_SM_WARPS)) & ~7;
-static_assert(AT_REGS_HIGH <= 256 && 128 * AT_REGS_LOW + 32 * AT_SM_WARPS * AT_REGS_HIGH <=
-                                         AT_REGS_LAUNCH * AT_THREADS, "register split");
+    ((AT_REGS_LAUNCH * AT_THREADS - 128 * AT_REGS_LOW - 128 * AT_REGS_CO) / (32 * AT_SM_WARPS)) & ~7;
+static_assert(AT_REGS_HIGH <= 256 && AT_REGS_HIGH >= 128 &&
+                  128 * AT_REGS_LOW + 32 * AT_SM_WARPS * AT_REGS_HIGH + 128 * AT_REGS_CO <=
+                      AT_REGS_LAUNCH * AT_THREADS,
+              "register split");
 constexpr uint32_t AT_TILE = AT_ROWS * AT_D;          // 16 KiB of codes
 constexpr uint32_t AT_Q_OFF = 0;
 constexpr uint32_t AT_KV_OFF = AT_TILE;               // stage s: K at +0, V at +16 KiB
 constexpr uint32_t AT_P_OFF = AT_KV_OFF + AT_STAGES * 2 * AT_TILE;
 constexpr uint32_t AT_BAR_OFF = AT_P_OFF + 2 * AT_TILE;
 // q_full, kv_full[3], kv_empty[3], s_full[2], s_empty[2], p_full[2], p_empty[2],
-// o_full[2], o_empty[2], done, xchg[4]
-constexpr int AT_NUM_BARS = 1 + 2 * AT_STAGES + 6 * 2 + 1 + 4;
+// o_full[2], o_empty[2], done, xchg[4], a_full[2], a_empty[2], l_full
+constexpr int AT_NUM_BARS = 1 + 2 * AT_STAGES + 6 * 2 + 1 + 4 + 5;
 constexpr uint32_t AT_TMEMSLOT_OFF = AT_BAR_OFF + AT_NUM_BARS * 8;
 // row-max / row-sum exchange among the threads of a row: [parity][part][row]
 constexpr uint32_t AT_XCHG_OFF = (AT_TMEMSLOT_OFF + 16 + 15) & ~15u;
-constexpr uint32_t AT_SMEM_BYTES = 1024 + AT_XCHG_OFF + 2 * AT_SPLIT * 128 * 4;
+// running-max factors handed to the O-correction warps ([tile parity][row]) and
+// the final row sums ([row])
+constexpr uint32_t AT_ALPHA_OFF = AT_XCHG_OFF + 2 * AT_SPLIT * 128 * 4;
+constexpr uint32_t AT_L_OFF = AT_ALPHA_OFF + 2 * 128 * 4;
+constexpr uint32_t AT_SMEM_BYTES = 1024 + AT_L_OFF + 128 * 4;
 constexpr float AT_LOG2_448 = 8.807354922057604f;   // log2(448)
 static_assert(AT_SMEM_BYTES <= 232448, "shared memory budget (attention)");
 constexpr uint64_t AT_WAIT_NS = 4000000000ull;
@@ -137,6 +149,9 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
     auto o_empty = [&](int b) { return bars + 8u * (11 + 2 * AT_STAGES + b); };
     const uint32_t done_bar = bars + 8u * (13 + 2 * AT_STAGES);
     auto xchg_bar = [&](int q) { return bars + 8u * (14 + 2 * AT_STAGES + q); };
+    auto a_full = [&](int b) { return bars + 8u * (18 + 2 * AT_STAGES + b); };
+    auto a_empty = [&](int b) { return bars + 8u * (20 + 2 * AT_STAGES + b); };
+    const uint32_t l_full = bars + 8u * (22 + 2 * AT_STAGES);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + AT_TMEMSLOT_OFF);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -161,8 +176,11 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
             mbar_init(p_full(b), AT_SM_WARPS);
             mbar_init(p_empty(b), 1);
             mbar_init(o_full(b), 1);
-            mbar_init(o_empty(b), AT_SM_WARPS);
+            mbar_init(o_empty(b), 4);             // the O-correction warps
+            mbar_init(a_full(b), AT_SM_WARPS);
+            mbar_init(a_empty(b), 4);
         }
+        mbar_init(l_full, AT_SM_WARPS);
         mbar_init(done_bar, 1);
         for (int q = 0; q < 4; q++) mbar_init(xchg_bar(q), 32 * AT_SPLIT);   // the warps of a lane quarter
         fence_mbar_init();
@@ -245,7 +263,7 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
                 at_drain(done_bar, 0);
             }
         }
-    } else if (warp >= AT_SM_WARP0) {
+    } else if (warp >= AT_SM_WARP0 && warp < AT_CO_WARP0) {
         asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(AT_REGS_HIGH));
         // -------------------------------------------------------- softmax
         const int quarter = warp & 3;
@@ -280,53 +298,18 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
             return true;
         };
         float m = -INFINITY, l = 0.0f;   // l: this part's sum of 448 P (same max for all parts)
-        uint64_t acc[AT_CPT / 2];        // this thread's O columns as packed pairs
-#pragma unroll
-        for (int i = 0; i < AT_CPT / 2; i++) acc[i] = 0;
-        float alpha_prev = 1.0f;   // running-max factor of the tile whose O partial is pending
         bool ok = true;
 
-        // fold O partial of tile t into acc: acc = acc * alpha + partial * sv_t
-        auto consume_o = [&](int t, float alpha, float vs) -> bool {
-            const int b = t & 1;
-            if (!__all_sync(0xFFFFFFFFu, at_wait(o_full(b), (t >> 1) & 1u))) return false;
-            tc_fence_after();
-            const uint64_t a2 = pack_f32x2(__float_as_uint(alpha), __float_as_uint(alpha));
-            const uint64_t v2 = pack_f32x2(__float_as_uint(vs), __float_as_uint(vs));
-            uint32_t rr[AT_CPT / 32][32];
-#pragma unroll
-            for (int u = 0; u < AT_CPT / 32; u++)
-                tmem_ld_32x32b_x32(tmem + lane_off + 256 + b * 128 + col_off + u * 32, rr[u]);
-            tmem_wait_ld();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(o_empty(b));
-#pragma unroll
-            for (int u = 0; u < AT_CPT / 32; u++)
-#pragma unroll
-                for (int q = 0; q < 16; q++) {
-                    const uint64_t pv = mul_f32x2(pack_f32x2(rr[u][2 * q], rr[u][2 * q + 1]), v2);
-                    uint64_t a = acc[u * 16 + q];
-                    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(acc[u * 16 + q]) : "l"(a), "l"(a2), "l"(pv));
-                }
-            return true;
-        };
-
-        // K and V tile scales: lane i holds those of tile 32 w + i while the
-        // loop is in window w (reloaded every 32 tiles) and a tile's pair is
-        // taken by a shuffle.  A global load issued every tile would hold up
-        // the warp's next TMEM-load wait until it lands.
+        // K tile scales: lane i holds that of tile 32 w + i while the loop is
+        // in window w (reloaded every 32 tiles) and a tile's is taken by a
+        // shuffle.  A global load issued every tile would hold up the warp's
+        // next TMEM-load wait until it lands.
         auto ksc = [&](int t) { return t < n ? __ldg(p.sk + static_cast<int64_t>(t) * p.hkv + g) : 0.0f; };
-        auto vsc = [&](int t) { return t < n ? __ldg(p.sv + static_cast<int64_t>(t) * p.hkv + g) : 0.0f; };
-        float skw = 0.0f, svw = 0.0f, sv_prev = 0.0f;
+        float skw = 0.0f;
         for (int j = 0; ok && j < n; j++) {
             const int b = j & 1;
-            if ((j & 31) == 0) {
-                skw = ksc(j + lane);
-                svw = vsc(j + lane);
-            }
+            if ((j & 31) == 0) skw = ksc(j + lane);
             const float sk_j = __shfl_sync(0xFFFFFFFFu, skw, j & 31);
-            const float sv_j = __shfl_sync(0xFFFFFFFFu, svw, j & 31);
             ok = __all_sync(0xFFFFFFFFu, at_wait(s_full(b), (j >> 1) & 1u));
             if (!ok) break;
             tc_fence_after();
@@ -367,6 +350,12 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
             const float m_new = fmaxf(m, tmax);
             const float alpha = m_new == -INFINITY ? 1.0f : ex2(m - m_new);
             const float shift = AT_LOG2_448 - (m_new == -INFINITY ? 0.0f : m_new);
+            // hand this tile's running-max factor to the O-correction warps
+            ok = __all_sync(0xFFFFFFFFu, at_wait(a_empty(b), ((j >> 1) & 1u) ^ 1u));
+            if (!ok) break;
+            if (cq == 0) st_shared_f32(sbase + AT_ALPHA_OFF + (b * 128 + r) * 4, alpha);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(a_full(b));
             ok = __all_sync(0xFFFFFFFFu, at_wait(p_empty(b), ((j >> 1) & 1u) ^ 1u));
             if (!ok) break;
             // 448 P = 2^(raw c - m_new + log2 448) (masked: 2^-inf = 0), row sum, codes
@@ -396,22 +385,70 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
             if (lane == 0) mbar_arrive(p_full(b));
             l = l * alpha + rsum;
             m = m_new;
-            // the previous tile's O partial (its MMA ran during this tile's softmax)
-            if (j > 0) {
-                ok = consume_o(j - 1, alpha_prev, sv_prev);
-                if (!ok) break;
-            }
-            alpha_prev = alpha;
-            sv_prev = sv_j;
         }
-        if (ok && n > 0) ok = consume_o(n - 1, alpha_prev, sv_prev);
         if (ok && n > 0) ok = exchange(l, false);                 // row sum over all parts
-        if (ok && row_ok) {
-            // O = sum(448 P * V * sv) / sum(448 P)
-            const float inv_l = l > 0.0f ? 1.0f / l : 0.0f;
-            uint16_t* o = reinterpret_cast<uint16_t*>(p.o) + row * p.ldo + static_cast<int64_t>(h) * AT_D + col_off;
+        // the row sum for the O-correction warps (always handed over, so that
+        // they never wait for it in vain; a timeout above is already recorded)
+        if (cq == 0) st_shared_f32(sbase + AT_L_OFF + r * 4, ok ? l : 0.0f);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(l_full);
+    } else if (warp >= AT_CO_WARP0) {
+        asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(AT_REGS_CO));
+        // ---------------------------------------------------- O correction
+        // One thread per query row holds the row's 128 O columns in fp32:
+        // per tile, acc = acc * alpha_t + (P_t V_t) * sv_t, with P_t V_t read
+        // from TMEM and alpha_t from the softmax warps; at the end O / l.
+        const int quarter = warp & 3;
+        const int r = quarter * 32 + lane;
+        const int64_t row = q0 + r;
+        const bool row_ok = row < p.seq_q;
+        const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
+        uint64_t acc[64];   // the row's O columns as packed pairs
 #pragma unroll
-            for (int c8 = 0; c8 < AT_CPT / 8; c8++) {
+        for (int i = 0; i < 64; i++) acc[i] = 0;
+        bool ok = true;
+        auto vsc = [&](int t) { return t < n ? __ldg(p.sv + static_cast<int64_t>(t) * p.hkv + g) : 0.0f; };
+        float svw = 0.0f;   // V scales: a window of 32 tiles across the lanes (as for K)
+        for (int j = 0; ok && j < n; j++) {
+            const int b = j & 1;
+            if ((j & 31) == 0) svw = vsc(j + lane);
+            const float sv_j = __shfl_sync(0xFFFFFFFFu, svw, j & 31);
+            ok = __all_sync(0xFFFFFFFFu, at_wait(a_full(b), (j >> 1) & 1u));
+            if (!ok) break;
+            const float alpha = ld_shared_f32(sbase + AT_ALPHA_OFF + (b * 128 + r) * 4);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(a_empty(b));
+            ok = __all_sync(0xFFFFFFFFu, at_wait(o_full(b), (j >> 1) & 1u));
+            if (!ok) break;
+            tc_fence_after();
+            const uint64_t a2 = pack_f32x2(__float_as_uint(alpha), __float_as_uint(alpha));
+            const uint64_t v2 = pack_f32x2(__float_as_uint(sv_j), __float_as_uint(sv_j));
+#pragma unroll
+            for (int u = 0; u < 4; u++) {
+                uint32_t rr[32];
+                tmem_ld_32x32b_x32(tmem + lane_off + 256 + b * 128 + u * 32, rr);
+                tmem_wait_ld();
+                if (u == 3) {   // last read of this O partial: hand the buffer back
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(o_empty(b));
+                }
+#pragma unroll
+                for (int q = 0; q < 16; q++) {
+                    const uint64_t pv = mul_f32x2(pack_f32x2(rr[2 * q], rr[2 * q + 1]), v2);
+                    uint64_t a = acc[u * 16 + q];
+                    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(acc[u * 16 + q]) : "l"(a), "l"(a2), "l"(pv));
+                }
+            }
+        }
+        // O = sum(448 P * V * sv) / sum(448 P)
+        if (ok) ok = __all_sync(0xFFFFFFFFu, at_wait(l_full, 0));
+        if (ok && row_ok) {
+            const float l = ld_shared_f32(sbase + AT_L_OFF + r * 4);
+            const float inv_l = l > 0.0f ? 1.0f / l : 0.0f;
+            uint16_t* o = reinterpret_cast<uint16_t*>(p.o) + row * p.ldo + static_cast<int64_t>(h) * AT_D;
+#pragma unroll
+            for (int c8 = 0; c8 < AT_D / 8; c8++) {
                 uint32_t w[4];
 #pragma unroll
                 for (int i = 0; i < 4; i++) {
@@ -423,7 +460,6 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
             }
         }
     }
-
     tc_fence_before();
     __syncthreads();
     if (warp == 1) {

@@ -313,25 +313,33 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
             ok = __all_sync(0xFFFFFFFFu, at_wait(s_full(b), (j >> 1) & 1u));
             if (!ok) break;
             tc_fence_after();
+            const bool full = static_cast<int64_t>(j) * AT_KEYS + AT_KEYS - 1 <= all_vis;   // CTA-uniform
             uint32_t sr[AT_CPT / 32][32];
+            float lm[AT_CPT / 32];   // per-load maxima (fully visible tiles)
+            if (full) {
 #pragma unroll
-            for (int u = 0; u < AT_CPT / 32; u++) tmem_ld_32x32b_x32(tmem + lane_off + b * 128 + col_off + u * 32, sr[u]);
+                for (int u = 0; u < AT_CPT / 32; u++)
+                    tmem_ld_max_32x32b_x32(tmem + lane_off + b * 128 + col_off + u * 32, sr[u], lm[u]);
+            } else {
+#pragma unroll
+                for (int u = 0; u < AT_CPT / 32; u++)
+                    tmem_ld_32x32b_x32(tmem + lane_off + b * 128 + col_off + u * 32, sr[u]);
+            }
             tmem_wait_ld();
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(s_empty(b));   // S buffer read: hand it back
             const float c = qs * sk_j * p.scale_log2;
             const int64_t key0 = static_cast<int64_t>(j) * AT_KEYS + col_off;
-            const bool full = static_cast<int64_t>(j) * AT_KEYS + AT_KEYS - 1 <= all_vis;   // CTA-uniform
             // scores in log2 units are raw * c with c > 0, so the row max is
             // max(raw) * c; masked keys become -inf.  Eight independent
             // partial maxima / sums keep the dependency chains short.
             float tm[8];
 #pragma unroll
             for (int i = 0; i < 8; i++) tm[i] = -INFINITY;
-            if (full) {   // every key of the tile is visible to every row of the CTA
+            if (full) {   // every key of the tile is visible: the loads reduced the maxima
 #pragma unroll
-                for (int e = 0; e < AT_CPT; e++) tm[e & 7] = fmaxf(tm[e & 7], __uint_as_float(sr[e >> 5][e & 31]));
+                for (int u = 0; u < AT_CPT / 32; u++) tm[u] = lm[u];
             } else {      // keys e <= lim are visible to this row
                 const int lim = static_cast<int>(max(min(last_key - key0, static_cast<int64_t>(AT_CPT)),
                                                      static_cast<int64_t>(-1)));

@@ -80,8 +80,6 @@ constexpr int SPF = FP8BS_SPF;               // scale prefetch distance (chunks)
 constexpr uint64_t WAIT_LIMIT_NS = 4000000000ull;
 constexpr uint64_t DRAIN_LIMIT_NS = 200000000ull;
 
-// Shared memory: [align pad][A ring][B ring][barriers][tmem addr][group tables]
-constexpr uint32_t BAR_OFF = STAGES * STAGE_BYTES;
 // Each K block's MMAs run as H slices of N = 256 / H columns, each into its
 // own TMEM buffer of a ring of 512 / (256 / H) buffers: H = 1 (two 256-column
 // buffers) for the promotion epilogue, whose per-block work fits inside one
@@ -101,19 +99,41 @@ constexpr int MAX_TBUFS = 4;
 // tile's 256 B column scales (1 KiB) and, for a 1x128 A, its 128 row scales
 constexpr int BSF_SLOTS = 4;
 constexpr uint32_t BSF_SLOT_BYTES = 1536;
-// full, empty, tfull, tempty, done, xchg[4], bsf_full, bsf_empty
-constexpr int NUM_BARS = 2 * STAGES + 2 * MAX_TBUFS + 1 + 4 + 2 * BSF_SLOTS;
-constexpr uint32_t TMEMSLOT_OFF = BAR_OFF + NUM_BARS * 8;
-constexpr uint32_t TABLE_OFF = (TMEMSLOT_OFF + 16 + 15) & ~15u;
-// output staging: one 2 KiB slab per epilogue warp (32 rows x 64 B, 64-B swizzle)
-constexpr uint32_t OUT_SLAB = 2048;
-constexpr uint32_t OUT_OFF = (TABLE_OFF + 2 * (kMaxGroups + 1) * 4 + 1023) & ~1023u;
+// output staging: 2 KiB sub-slabs (32 rows x 64 B, 64-B swizzle), one or four
+// per epilogue warp
+constexpr uint32_t OUT_SUB = 2048;
+constexpr uint32_t OUT_SLAB = OUT_SUB;   // the MX kernel's slab
 // amax exchange of the SwiGLU epilogue: [tile parity][column half][row] fp32
 constexpr uint32_t XCHG_BYTES = 2 * 2 * 128 * 4;
-constexpr uint32_t XCHG_OFF = OUT_OFF + NUM_EPI_WARPS * OUT_SLAB;
-constexpr uint32_t BSF_OFF = XCHG_OFF + XCHG_BYTES;
-constexpr uint32_t SMEM_BYTES = 1024 + BSF_OFF + BSF_SLOTS * BSF_SLOT_BYTES;
-static_assert(SMEM_BYTES <= 232448, "shared memory budget");
+
+// Shared memory of k_fp8_gemm: [align pad][A ring][B ring][barriers][tmem
+// addr][group tables][output slabs][SwiGLU exchange][B-scale ring], for S
+// operand stages and SUBS output sub-slabs per epilogue warp.  With four
+// sub-slabs a tile's four store passes never wait for an earlier pass's
+// store to finish reading its slab; the plain K-major kernel (the promotion
+// products) gives up one operand stage for them, as its K blocks are paced by
+// the promotion rather than by the loads.  The kernels that accumulate the
+// whole K in TMEM (MN-major, per-tensor scales) and the SwiGLU / per-column-B
+// epilogues keep four stages.
+template <int S, int SUBS>
+struct GemmLayout {
+    static constexpr int kStages = S;
+    static constexpr int kSubs = SUBS;
+    static constexpr uint32_t kBarOff = S * STAGE_BYTES;
+    // full, empty, tfull, tempty, done, xchg[4], bsf_full, bsf_empty
+    static constexpr int kNumBars = 2 * S + 2 * MAX_TBUFS + 1 + 4 + 2 * BSF_SLOTS;
+    static constexpr uint32_t kTmemSlotOff = kBarOff + kNumBars * 8;
+    static constexpr uint32_t kTableOff = (kTmemSlotOff + 16 + 15) & ~15u;
+    static constexpr uint32_t kSlab = SUBS * OUT_SUB;
+    static constexpr uint32_t kOutOff = (kTableOff + 2 * (kMaxGroups + 1) * 4 + 1023) & ~1023u;
+    static constexpr uint32_t kXchgOff = kOutOff + NUM_EPI_WARPS * kSlab;
+    static constexpr uint32_t kBsfOff = kXchgOff + XCHG_BYTES;
+    static constexpr uint32_t kSmemBytes = 1024 + kBsfOff + BSF_SLOTS * BSF_SLOT_BYTES;
+    static_assert(kSmemBytes <= 232448, "shared memory budget");
+};
+template <bool A_MN, bool B_MN, bool SWIGLU, bool B_COL>
+using GemmLayoutFor = GemmLayout<(A_MN || B_MN || SWIGLU || B_COL) ? STAGES : STAGES - 1,
+                                 (A_MN || B_MN || SWIGLU || B_COL) ? 1 : 4>;
 
 __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
     if (mbar_try_wait(bar, parity)) return true;
@@ -163,22 +183,28 @@ __device__ __forceinline__ Tile decode_tile(int t, int total_slots, int tiles_n,
 __device__ __forceinline__ float ld_scale(const float* p) { return __ldg(p); }
 
 // Store one warp's 32 rows x 128 columns of a finished tile (acc = 128 fp32
-// as packed pairs): TMA bulk stores of 32 x 64-byte slabs when the warp's 32
-// rows all belong to the tile's group (TMA clips only at the tensor edge),
-// otherwise masked direct stores.
+// as packed pairs): TMA bulk stores of 32 x 64-byte boxes staged in the warp's
+// `subs` 2 KiB sub-slabs when the warp's 32 rows all belong to the tile's
+// group (TMA clips only at the tensor edge), otherwise masked direct stores.
 __device__ __forceinline__ void store_tile(const GemmParams& p, const CUtensorMap& tmY,
                                            const uint64_t (&acc)[64], const Tile& tl, int64_t row,
                                            bool row_ok, int64_t col0, int quarter, int lane,
-                                           uint32_t slab) {
+                                           uint32_t slab, int subs) {
     const int64_t wrow0 = static_cast<int64_t>(tl.row0) + quarter * 32;
     if (p.tma_store && (p.offsets == nullptr || wrow0 + 32 <= tl.row_end)) {
-        const uint32_t rbase = slab + lane * 64;
         const uint32_t sw = (lane >> 1) & 3;          // 64-B swizzle: chunk ^= (row/2)%4
         const int passes = p.out_bf16 ? 4 : 8;        // 32 bf16 or 16 fp32 columns each
 #pragma unroll
         for (int ps = 0; ps < 8; ps++) {
             if (ps >= passes) break;
-            if (lane == 0) bulk_wait_group_read0();   // slab free again
+            // pass ps uses sub-slab ps % subs, free once the store issued from
+            // it subs passes ago has read it
+            const uint32_t sub = slab + static_cast<uint32_t>(ps % subs) * OUT_SUB;
+            const uint32_t rbase = sub + lane * 64;
+            if (lane == 0) {
+                if (subs == 4) bulk_wait_group_read3();
+                else bulk_wait_group_read0();
+            }
             __syncwarp();
 #pragma unroll
             for (int c = 0; c < 4; c++) {
@@ -201,7 +227,7 @@ __device__ __forceinline__ void store_tile(const GemmParams& p, const CUtensorMa
             fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) {
-                tma_store_2d(&tmY, slab, static_cast<int32_t>(col0 + ps * (p.out_bf16 ? 32 : 16)),
+                tma_store_2d(&tmY, sub, static_cast<int32_t>(col0 + ps * (p.out_bf16 ? 32 : 16)),
                              static_cast<int32_t>(wrow0));
                 bulk_commit_group();
             }
@@ -316,9 +342,9 @@ __device__ __forceinline__ bool finish_tile(const GemmParams& p, const CUtensorM
                                             uint64_t (&acc)[64], const Tile& tl, int64_t row,
                                             bool row_ok, int64_t col0, int quarter, int half,
                                             int lane, uint32_t slab, uint32_t xbuf, uint32_t xbar,
-                                            uint32_t tile_par) {
+                                            uint32_t tile_par, int subs = 1) {
     if (!p.out_q) {
-        store_tile(p, tmY, acc, tl, row, row_ok, col0, quarter, lane, slab);
+        store_tile(p, tmY, acc, tl, row, row_ok, col0, quarter, lane, slab, subs);
         return true;
     }
     int nv = 128;
@@ -362,8 +388,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     uint8_t* smem = smem_raw + ((1024u - (raw & 1023u)) & 1023u);
     const uint32_t sbase = smem_u32(smem);
     const uint32_t sA = sbase;
+    using L = GemmLayoutFor<A_MN, B_MN, SWIGLU, B_COL>;
+    constexpr int STAGES = L::kStages;
     const uint32_t sB = sbase + STAGES * A_STAGE;
-    const uint32_t bars = sbase + BAR_OFF;
+    const uint32_t bars = sbase + L::kBarOff;
     auto full_bar = [&](int s) { return bars + 8u * s; };
     auto empty_bar = [&](int s) { return bars + 8u * (STAGES + s); };
     auto tfull_bar = [&](int b) { return bars + 8u * (2 * STAGES + b); };
@@ -372,8 +400,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     auto xchg_bar = [&](int q) { return bars + 8u * (2 * STAGES + 2 * MAX_TBUFS + 1 + q); };
     auto bsf_full = [&](int q) { return bars + 8u * (2 * STAGES + 2 * MAX_TBUFS + 5 + q); };
     auto bsf_empty = [&](int q) { return bars + 8u * (2 * STAGES + 2 * MAX_TBUFS + 5 + BSF_SLOTS + q); };
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + TMEMSLOT_OFF);
-    int* s_off = reinterpret_cast<int*>(smem + TABLE_OFF);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kTmemSlotOff);
+    int* s_off = reinterpret_cast<int*>(smem + L::kTableOff);
     int* s_slot = s_off + (kMaxGroups + 1);
 
     const int warp = threadIdx.x >> 5;
@@ -565,7 +593,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     ? static_cast<uint32_t>(min(static_cast<int64_t>(BM), p.a_rows - tl.row0)) * 4u : 0u;
                 for (int kb = 0; kb < nkb; kb++) {
                     if (!wait_or_flag(bsf_empty(slot), ph ^ 1u)) { ok = false; break; }
-                    const uint32_t dst = sbase + BSF_OFF + slot * BSF_SLOT_BYTES;
+                    const uint32_t dst = sbase + L::kBsfOff + slot * BSF_SLOT_BYTES;
                     if (p.a_gran != 0)   // 128x128 / per-tensor A: its one scale of this K block
                         st_shared_f32(dst + 1024, ld_scale(p.sa + (p.a_gran == 1 ? (min(static_cast<int64_t>(tl.row0),
                                                                                         p.a_rows - 1) / 128) * nkb + kb : 0)));
@@ -613,7 +641,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 ok = __all_sync(0xFFFFFFFFu, wait_or_flag(bsf_full(bslot), bph));
                 if (!ok) break;
                 tc_fence_after();
-                const uint32_t slotb = sbase + BSF_OFF + bslot * BSF_SLOT_BYTES;
+                const uint32_t slotb = sbase + L::kBsfOff + bslot * BSF_SLOT_BYTES;
                 const uint32_t tb = tmem_base + buf * MMA_N + half * 128;
                 float a[4];   // A scales of rows 16 lh + 8 e (+ t/4): a[2 lh + e]
 #pragma unroll
@@ -784,8 +812,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             }
             if (!ok) break;
             ok = finish_tile<SWIGLU>(p, tmY, acc, tl, row, row_ok, col0, quarter, half, lane,
-                             sbase + OUT_OFF + (warp - EPI_WARP0) * OUT_SLAB, sbase + XCHG_OFF,
-                             xchg_bar(quarter), tile_i & 1u);
+                             sbase + L::kOutOff + (warp - EPI_WARP0) * L::kSlab, sbase + L::kXchgOff,
+                             xchg_bar(quarter), tile_i & 1u, L::kSubs);
         }
         if (lane == 0) bulk_wait_group0();   // every store of this warp has landed
     }
@@ -1158,7 +1186,7 @@ cudaError_t launch_wait_selftest(uint64_t limit_ns, int* out, cudaStream_t st) {
     return cudaGetLastError();
 }
 
-uint32_t gemm_smem_bytes() { return SMEM_BYTES; }
+uint32_t gemm_smem_bytes() { return GemmLayoutFor<true, false, false, false>::kSmemBytes; }
 
 // kind::f8f6f4 instruction descriptor: D fp32 (bits 4-5 = 1), A/B formats
 // (bits 7-9, 10-12: E4M3 = 0, E5M2 = 1), A/B major (bits 15, 16: 1 = MN),
@@ -1211,9 +1239,12 @@ cudaError_t launch_fp8_gemm(const CUtensorMap& tmA, const CUtensorMap& tmB, cons
              : p.b_gran == 0 ? k_fp8_gemm<false, false, false, true, hb>
              : a_mn ? (b_mn ? k_fp8_gemm<true, true, false, false, h1> : k_fp8_gemm<true, false, false, false, h1>)
                     : (b_mn ? k_fp8_gemm<false, true, false, false, h1> : k_fp8_gemm<false, false, false, false, h1>);
-    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+    const uint32_t smem = p.swiglu || p.b_gran == 0 || a_mn || b_mn
+                              ? GemmLayoutFor<true, false, false, false>::kSmemBytes
+                              : GemmLayoutFor<false, false, false, false>::kSmemBytes;
+    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    k<<<grid, NUM_THREADS, SMEM_BYTES, st>>>(tmA, tmB, tmY, p);
+    k<<<grid, NUM_THREADS, smem, st>>>(tmA, tmB, tmY, p);
     return cudaGetLastError();
 }
 

@@ -91,6 +91,10 @@ __device__ __forceinline__ void bulk_commit_group() {
 __device__ __forceinline__ void bulk_wait_group_read0() {
     asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
 }
+// ... at most three groups of this thread still reading shared memory
+__device__ __forceinline__ void bulk_wait_group_read3() {
+    asm volatile("cp.async.bulk.wait_group.read 3;" ::: "memory");
+}
 // Wait until all committed bulk stores have completed.
 __device__ __forceinline__ void bulk_wait_group0() {
     asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");

@@ -46,8 +46,8 @@ from block_scaled_gemm_quantize_gb300 import inputs as W_  # noqa: E402
 METRIC = "block-scaled FP8 linear TFLOPS (quant+GEMM) and % of GB300 dense FP8 peak"
 # DRAM read+write bytes per GEMM launch of the default workload, from one ncu capture of the
 # current kernel (profiles/k_fp8_gemm_llama31_8b_gate_up.md); None for other workloads.
-GEMM_TRAFFIC_BYTES = {"llama3.1-8b-fprop": {"qkv": 134.6e6, "o": 80.8e6, "gate_up": 936.7e6,
-                                            "down": 515.7e6}}
+GEMM_TRAFFIC_BYTES = {"llama3.1-8b-fprop": {"qkv": 135.2e6, "o": 81.1e6, "gate_up": 936.6e6,
+                                            "down": 517.0e6}}
 FP8_OVER_BF16 = 2.0      # nominal dense fp8 / bf16 tensor ratio (4.5 / 2.25 PFLOP/s)
 
 

@@ -54,6 +54,16 @@ def test_attention_small(causal, S_q, S_k, hq, hkv):
     _check(o_bits, orc.attention(S_q, S_k, hq, hkv, causal, SCALE, *arrs))
 
 
+@pytest.mark.parametrize("causal", [False, True])
+def test_attention_more_than_32_key_tiles(causal):
+    """Keys spanning 33 tiles of 128 plus a ragged one: the per-tile K and V
+    scales come from a window of 32 tiles that is reloaded past tile 31."""
+    S_q, S_k, hq, hkv = 200, 4300, 2, 1
+    arrs = _inputs(S_q, S_k, hq, hkv, seed=33)
+    o_bits = _run(S_q, S_k, hq, hkv, causal, arrs)
+    _check(o_bits, orc.attention(S_q, S_k, hq, hkv, causal, SCALE, *arrs))
+
+
 def test_attention_equal_scores_give_the_mean_of_the_visible_values():
     import torch
     S, hq, hkv = 384, 2, 1

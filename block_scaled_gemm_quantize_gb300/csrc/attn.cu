@@ -79,15 +79,15 @@ constexpr uint32_t AT_KV_OFF = AT_TILE;               // stage s: K at +0, V at 
 constexpr uint32_t AT_P_OFF = AT_KV_OFF + AT_STAGES * 2 * AT_TILE;
 constexpr uint32_t AT_BAR_OFF = AT_P_OFF + 2 * AT_TILE;
 // q_full, kv_full[3], kv_empty[3], s_full[2], s_empty[2], p_full[2], p_empty[2],
-// o_full[2], o_empty[2], done, xchg[4], a_full[2], a_empty[2], l_full
+// o_full[2], o_empty[2], done, xchg[4], a_full[4], l_full
 constexpr int AT_NUM_BARS = 1 + 2 * AT_STAGES + 6 * 2 + 1 + 4 + 5;
 constexpr uint32_t AT_TMEMSLOT_OFF = AT_BAR_OFF + AT_NUM_BARS * 8;
 // row-max / row-sum exchange among the threads of a row: [parity][part][row]
 constexpr uint32_t AT_XCHG_OFF = (AT_TMEMSLOT_OFF + 16 + 15) & ~15u;
-// running-max factors handed to the O-correction warps ([tile parity][row]) and
+// running-max factors handed to the O-correction warps ([tile % 4][row]) and
 // the final row sums ([row])
 constexpr uint32_t AT_ALPHA_OFF = AT_XCHG_OFF + 2 * AT_SPLIT * 128 * 4;
-constexpr uint32_t AT_L_OFF = AT_ALPHA_OFF + 2 * 128 * 4;
+constexpr uint32_t AT_L_OFF = AT_ALPHA_OFF + 4 * 128 * 4;
 constexpr uint32_t AT_SMEM_BYTES = 1024 + AT_L_OFF + 128 * 4;
 constexpr float AT_LOG2_448 = 8.807354922057604f;   // log2(448)
 static_assert(AT_SMEM_BYTES <= 232448, "shared memory budget (attention)");
@@ -150,7 +150,6 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
     const uint32_t done_bar = bars + 8u * (13 + 2 * AT_STAGES);
     auto xchg_bar = [&](int q) { return bars + 8u * (14 + 2 * AT_STAGES + q); };
     auto a_full = [&](int b) { return bars + 8u * (18 + 2 * AT_STAGES + b); };
-    auto a_empty = [&](int b) { return bars + 8u * (20 + 2 * AT_STAGES + b); };
     const uint32_t l_full = bars + 8u * (22 + 2 * AT_STAGES);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + AT_TMEMSLOT_OFF);
 
@@ -178,7 +177,7 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
             mbar_init(o_full(b), 1);
             mbar_init(o_empty(b), 4);             // the O-correction warps
             mbar_init(a_full(b), AT_SM_WARPS);
-            mbar_init(a_empty(b), 4);
+            mbar_init(a_full(b + 2), AT_SM_WARPS);
         }
         mbar_init(l_full, AT_SM_WARPS);
         mbar_init(done_bar, 1);
@@ -358,14 +357,16 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
             const float m_new = fmaxf(m, tmax);
             const float alpha = m_new == -INFINITY ? 1.0f : ex2(m - m_new);
             const float shift = AT_LOG2_448 - (m_new == -INFINITY ? 0.0f : m_new);
-            // hand this tile's running-max factor to the O-correction warps
-            ok = __all_sync(0xFFFFFFFFu, at_wait(a_empty(b), ((j >> 1) & 1u) ^ 1u));
-            if (!ok) break;
-            if (cq == 0) st_shared_f32(sbase + AT_ALPHA_OFF + (b * 128 + r) * 4, alpha);
-            __syncwarp();
-            if (lane == 0) mbar_arrive(a_full(b));
             ok = __all_sync(0xFFFFFFFFu, at_wait(p_empty(b), ((j >> 1) & 1u) ^ 1u));
             if (!ok) break;
+            // hand this tile's running-max factor to the O-correction warps, in
+            // slot j % 4.  That slot's previous factor (tile j - 4) has been
+            // read: P_j's buffer is free, so O_{j-2} = P_{j-2} V was issued, which
+            // waited for the correction warps to drain O_{j-4}, and they read a
+            // tile's factor before draining its O.
+            if (cq == 0) st_shared_f32(sbase + AT_ALPHA_OFF + ((j & 3) * 128 + r) * 4, alpha);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(a_full(j & 3));
             // 448 P = 2^(raw c - m_new + log2 448) (masked: 2^-inf = 0), row sum, codes
             const uint32_t prow = sbase + AT_P_OFF + b * AT_TILE + r * 128;
             float rs[8];
@@ -421,11 +422,9 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
             const int b = j & 1;
             if ((j & 31) == 0) svw = vsc(j + lane);
             const float sv_j = __shfl_sync(0xFFFFFFFFu, svw, j & 31);
-            ok = __all_sync(0xFFFFFFFFu, at_wait(a_full(b), (j >> 1) & 1u));
+            ok = __all_sync(0xFFFFFFFFu, at_wait(a_full(j & 3), (j >> 2) & 1u));
             if (!ok) break;
-            const float alpha = ld_shared_f32(sbase + AT_ALPHA_OFF + (b * 128 + r) * 4);
-            __syncwarp();
-            if (lane == 0) mbar_arrive(a_empty(b));
+            const float alpha = ld_shared_f32(sbase + AT_ALPHA_OFF + ((j & 3) * 128 + r) * 4);
             ok = __all_sync(0xFFFFFFFFu, at_wait(o_full(b), (j >> 1) & 1u));
             if (!ok) break;
             tc_fence_after();

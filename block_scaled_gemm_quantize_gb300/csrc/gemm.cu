@@ -1186,7 +1186,6 @@ cudaError_t launch_wait_selftest(uint64_t limit_ns, int* out, cudaStream_t st) {
     return cudaGetLastError();
 }
 
-uint32_t gemm_smem_bytes() { return GemmLayoutFor<true, false, false, false>::kSmemBytes; }
 
 // kind::f8f6f4 instruction descriptor: D fp32 (bits 4-5 = 1), A/B formats
 // (bits 7-9, 10-12: E4M3 = 0, E5M2 = 1), A/B major (bits 15, 16: 1 = MN),

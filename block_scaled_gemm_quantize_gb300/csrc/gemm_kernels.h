@@ -43,7 +43,6 @@ struct GemmParams {
     int32_t mx32;
 };
 
-uint32_t gemm_smem_bytes();
 uint32_t make_idesc_f8f6f4(int a_fmt, int b_fmt, bool a_mn, bool b_mn, int n);
 int gemm_tile_n();
 int gemm_mma_n(bool b_col);   // N of one tcgen05.mma (K-major B; b_col: per-column B scales);

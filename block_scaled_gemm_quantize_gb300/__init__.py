@@ -250,10 +250,13 @@ class DelayedScaling:
         self.scale = torch.ones(1, dtype=torch.float32, device=device)
         self.amax = torch.zeros(1, dtype=torch.float32, device=device)
 
-    def quantize(self, x, q=None, stream=None, update=True):
-        """Quantize x with the scale in use, then (update=True) fold its amax
-        into the state.  With update=False the caller runs update() later --
-        e.g. after the GEMMs that read `scale` as this step's dequant scale."""
+    def quantize(self, x, q=None, stream=None, update=False):
+        """Quantize x with the scale in use (`self.scale`, built from earlier
+        steps) and record its amax in `self.amax`.  The products that read these
+        codes must dequantize with that same `self.scale`, so the state is
+        advanced separately, by update(), once they have been enqueued;
+        update=True advances it right away (for callers that read no product
+        from `self.scale` in between)."""
         q, _ = fp8_quantize_tensor_delayed(x, self.fmt, self.scale, q=q, amax=self.amax, stream=stream)
         if update:
             self.update(stream=stream)

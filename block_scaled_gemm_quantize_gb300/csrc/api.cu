@@ -289,9 +289,12 @@ int run_gemm(const char* fn, int32_t G, const int32_t* offsets, int64_t a_rows, 
         return e == cudaSuccess ? FP8BS_OK : cuda_fail(e, fn);
     }
 #ifndef FP8BS_NO_MX
-    // (1x128 A scales reach the kernel by TMA: a row pitch of 16 bytes needed)
+    // (1x128 A scales reach the kernel by TMA: a row pitch of 16 bytes needed).
+    // Only block-scaled operands: a per-tensor scale (delayed scaling) is in
+    // general not a power of two, so those products keep the promotion kernel.
     const bool sa_tma_ok = A->gran != FP8BS_GRAN_1x128 || (a_rows % 4 == 0 && aligned16(A->scales));
-    if (mode == FP8BS_SCALE_POW2 && !a_mn && !b_mn && !grouped && sa_tma_ok &&
+    const bool blocks_only = A->gran != FP8BS_GRAN_TENSOR && B->gran != FP8BS_GRAN_TENSOR;
+    if (mode == FP8BS_SCALE_POW2 && !a_mn && !b_mn && !grouped && sa_tma_ok && blocks_only &&
         B->gran != FP8BS_GRAN_1x128) {
         CUtensorMap tmSA;
         memset(&tmSA, 0, sizeof(tmSA));
@@ -529,6 +532,8 @@ int fp8bs_device_status(fp8bs_stream_t stream) {
     e = fp8bs::read_and_clear_status(&st);
     if (e == cudaSuccess) e = fp8bs::read_and_clear_attn_status(&sta);
     if (e != cudaSuccess) return cuda_fail(e, "fp8bs_device_status");
+    if (st == fp8bs::kStatusBadOffsets)
+        return fail(FP8BS_ERR_INVALID_ARG, "a grouped product found decreasing row_offsets and wrote nothing");
     if (sta != 0) st = sta;
     if (st != 0) return fail(FP8BS_ERR_DEVICE_TIMEOUT, "a kernel gave up on a bounded device wait");
     return FP8BS_OK;

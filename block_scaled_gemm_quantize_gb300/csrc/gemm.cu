@@ -59,7 +59,21 @@ constexpr uint32_t B_STAGE = BN * BK;   // 32 KiB
 constexpr uint32_t STAGE_BYTES = A_STAGE + B_STAGE;
 constexpr int NUM_THREADS = 384;
 constexpr int EPI_WARP0 = 4;
-constexpr int REGS_LOW = 72, REGS_HIGH = 216;   // 128*72 + 256*216 == 384*168
+#ifndef FP8BS_REGS_LOW
+#define FP8BS_REGS_LOW 72
+#endif
+// the two epilogue warpgroups share what the first warpgroup gives up:
+// 128 * REGS_LOW + 256 * REGS_HIGH == 384 * 168, the launch allocation
+constexpr int REGS_LOW = FP8BS_REGS_LOW, REGS_HIGH = (384 * 168 - 128 * REGS_LOW) / 256;
+static_assert(REGS_LOW % 8 == 0 && REGS_HIGH % 8 == 0 && 128 * REGS_LOW + 256 * REGS_HIGH == 384 * 168,
+              "register split");
+#ifndef FP8BS_EPI_PIPE
+#define FP8BS_EPI_PIPE 0
+#endif
+#ifndef FP8BS_EPI_CW
+#define FP8BS_EPI_CW 16
+#endif
+constexpr int CW = FP8BS_EPI_CW;             // columns per pipelined TMEM load
 constexpr int NUM_EPI_WARPS = 8;
 constexpr uint32_t TMEM_COLS = 512;
 #ifndef FP8BS_RASTER_M
@@ -181,6 +195,23 @@ __device__ __forceinline__ Tile decode_tile(int t, int total_slots, int tiles_n,
 }
 
 __device__ __forceinline__ float ld_scale(const float* p) { return __ldg(p); }
+
+// acc[a0 .. a0 + CW/2) += r (CW fp32, as pairs) * s2, as volatile packed
+// FMAs so that they stay between the TMEM load they overlap and its wait.
+template <int CW>
+__device__ __forceinline__ void fma_cw_v(uint64_t (&acc)[64], int a0, const uint32_t (&r)[CW], uint64_t s2) {
+#pragma unroll
+    for (int q = 0; q < CW / 2; q++)
+        asm volatile("fma.rn.f32x2 %0, %1, %2, %0;"
+                     : "+l"(acc[a0 + q])
+                     : "l"(pack_f32x2(r[2 * q], r[2 * q + 1])), "l"(s2));
+}
+
+template <int CW>
+__device__ __forceinline__ void tmem_ld_cw(uint32_t taddr, uint32_t (&r)[CW]) {
+    if constexpr (CW == 32) tmem_ld_32x32b_x32(taddr, r);
+    else tmem_ld_32x32b_x16(taddr, r);
+}
 
 // Store one warp's 32 rows x 128 columns of a finished tile (acc = 128 fp32
 // as packed pairs): TMA bulk stores of 32 x 64-byte boxes staged in the warp's
@@ -438,14 +469,18 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     }
     __syncthreads();
     if (warp == 2) {
-        int carry = 0;
+        // prefix count of m-slots; a decreasing offset table (overlapping
+        // groups, whose tiles would write the same rows) is rejected: every
+        // CTA sees the same table, so all of them skip the product
+        int carry = 0, bad = 0;
         if (lane == 0) s_slot[0] = 0;
         for (int base = 0; base < G; base += 32) {
             const int g = base + lane;
             int cnt = 0;
             if (g < G) {
-                const int rows = max(0, s_off[g + 1] - s_off[g]);
-                cnt = (rows + BM - 1) / BM;
+                const int rows = s_off[g + 1] - s_off[g];
+                bad |= rows < 0;
+                cnt = (max(0, rows) + BM - 1) / BM;
             }
 #pragma unroll
             for (int o = 1; o < 32; o <<= 1) {
@@ -455,12 +490,17 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             if (g < G) s_slot[g + 1] = carry + cnt;
             carry += __shfl_sync(0xFFFFFFFFu, cnt, 31);
         }
+        bad = __any_sync(0xFFFFFFFFu, bad);
+        if (lane == 0) {
+            tmem_slot[1] = bad;
+            if (bad && blockIdx.x == 0) atomicCAS(&g_status, 0, kStatusBadOffsets);
+        }
     }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
-    const int total_slots = s_slot[G];
+    const int total_slots = tmem_slot[1] ? 0 : s_slot[G];
     const int total_tiles = total_slots * p.tiles_n;
     const int nkb = static_cast<int>(p.K / BK);
     const int P = p.promote ? 1 : nkb;  // K blocks per TMEM partial
@@ -757,6 +797,76 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 sb_r[i] = ld_scale(pb + kbi * sb_step);
                 sbu_r[i] = SWIGLU ? ld_scale(pbu + kbi * sb_step) : sb_r[i];
             }
+#if FP8BS_EPI_PIPE
+            if (H == 1) {
+                // Software-pipelined promotion: the TMEM load of the next CW
+                // columns (across K blocks too) is in flight while the FMAs of
+                // the current CW issue; R[0] / R[1] alternate.  A buffer goes
+                // back to the MMA once its last load has completed.
+                constexpr int NCH = 128 / CW;
+                const int ngroups = (nkb + P - 1) / P;
+                const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
+                uint32_t R[2][CW];
+                {
+                    const uint32_t buf = chunk % TBUFS;
+                    ok = __all_sync(0xFFFFFFFFu, wait_or_flag(tfull_bar(buf), (chunk / TBUFS) & 1u));
+                    if (ok) {
+                        tc_fence_after();
+                        tmem_ld_cw<CW>(tmem_base + lane_off + buf * MMA_N + half * 128, R[0]);
+                        tmem_wait_ld();
+                    }
+                }
+                for (int g0 = 0; ok && g0 < ngroups; g0 += SPF) {
+#pragma unroll
+                    for (int i = 0; i < SPF; i++) {
+                        const int g = g0 + i;
+                        if (g >= ngroups) break;
+                        const int kb = g * P;
+                        const float s = sa_r[i] * sb_r[i];
+                        const uint64_t s2 = pack_f32x2(__float_as_uint(s), __float_as_uint(s));
+                        const float su = sa_r[i] * sbu_r[i];
+                        const uint64_t s2u = pack_f32x2(__float_as_uint(su), __float_as_uint(su));
+                        if (kb + SPF * P < nkb) {
+                            sa_r[i] = ld_scale(pa + (kb + SPF * P) * sa_step);
+                            sb_r[i] = ld_scale(pb + (kb + SPF * P) * sb_step);
+                            sbu_r[i] = SWIGLU ? ld_scale(pbu + (kb + SPF * P) * sb_step) : sb_r[i];
+                        }
+                        const uint32_t buf = chunk % TBUFS;
+                        const uint32_t ta = tmem_base + lane_off + buf * MMA_N + half * 128;
+                        const bool more = g + 1 < ngroups;
+#pragma unroll
+                        for (int c = 0; c < NCH; c++) {
+                            bool issued = true;
+                            if (c + 1 < NCH) {
+                                tmem_ld_cw<CW>(ta + (c + 1) * CW, R[(c + 1) & 1]);
+                            } else {
+                                // every load of this buffer has completed: hand it back,
+                                // then start on the next K block's buffer
+                                tc_fence_before();
+                                __syncwarp();
+                                if (lane == 0) mbar_arrive(tempty_bar(buf));
+                                chunk++;
+                                issued = false;
+                                if (more) {
+                                    const uint32_t nbuf = chunk % TBUFS;
+                                    ok = __all_sync(0xFFFFFFFFu,
+                                                    wait_or_flag(tfull_bar(nbuf), (chunk / TBUFS) & 1u));
+                                    if (ok) {
+                                        tc_fence_after();
+                                        tmem_ld_cw<CW>(tmem_base + lane_off + nbuf * MMA_N + half * 128,
+                                                       R[(c + 1) & 1]);
+                                        issued = true;
+                                    }
+                                }
+                            }
+                            fma_cw_v<CW>(acc, c * (CW / 2), R[c & 1], c * CW < 64 ? s2 : s2u);
+                            if (issued) tmem_wait_ld();
+                        }
+                        if (!ok) break;
+                    }
+                }
+            } else
+#endif
             for (int kb0 = 0; ok && kb0 < nkb; kb0 += SPF * P) {
 #pragma unroll
                 for (int i = 0; i < SPF; i++) {

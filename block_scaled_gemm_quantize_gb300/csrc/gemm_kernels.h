@@ -8,7 +8,8 @@
 namespace fp8bs {
 
 constexpr int kMaxGroups = 1024;
-constexpr int kStatusDeviceTimeout = -5;
+constexpr int kStatusDeviceTimeout = -5;   // FP8BS_ERR_DEVICE_TIMEOUT
+constexpr int kStatusBadOffsets = -1;      // FP8BS_ERR_INVALID_ARG: decreasing group offsets
 
 struct GemmParams {
     int64_t M, N, K;          // logical product size (M = rows of A as stored)

@@ -32,7 +32,8 @@
  *     (a zero dimension) are valid and launch nothing, except a product with
  *     K == 0, which writes zeros to Y.
  *   - Device-side waits are bounded; a kernel that gives up records it in a
- *     per-process status word read by fp8bs_device_status().
+ *     status word (one per process and device, shared by all streams) read
+ *     by fp8bs_device_status().
  */
 #ifndef FP8BS_H
 #define FP8BS_H
@@ -222,8 +223,12 @@ typedef struct {
  * A and B may use different formats (E5M2 gradients x E4M3 weights).
  * Partial products of each 128-long K block are accumulated in fp32 and
  * promoted with that block's two scales into an fp32 accumulator.
- *   mode = POW2 declares that every scale is an exact power of two in
- *   [2^-126, 2^127] (from the POW2 quantizers); the result is the same sum.
+ *   mode = POW2 declares that every BLOCK scale (GRAN_1x128, GRAN_128x128)
+ *   is an exact power of two in [2^-126, 2^127] (from the POW2 quantizers);
+ *   the result is the same sum.  The library cannot check this on the host;
+ *   other block scales under POW2 give a wrong result.  A per-tensor scale
+ *   (GRAN_TENSOR, e.g. a delayed-scaling scale) may be any fp32 value in
+ *   either mode.
  *   Y [M][ld_y], fp32 or bf16 (round to nearest even), written, not
  *   accumulated.
  * Errors: INVALID_ARG, UNSUPPORTED (K % 128, N % 8, GRAN_1x128 on a
@@ -241,7 +246,12 @@ int fp8_block_gemm(int64_t M, int64_t N, int64_t K,
  * mundo real"): for each group g the rows [row_offsets[g], row_offsets[g+1])
  * of A are multiplied by expert g's weights.
  *   row_offsets     device int32 [num_groups + 1], non-decreasing,
- *                   row_offsets[0] = 0, row_offsets[G] <= a_rows.
+ *                   row_offsets[0] = 0, row_offsets[G] <= a_rows.  Entries
+ *                   are clamped into [0, a_rows], so no tile writes outside
+ *                   Y; a table that decreases (after clamping) makes the
+ *                   kernel write nothing and record FP8BS_ERR_INVALID_ARG for
+ *                   fp8bs_device_status() -- it lives in device memory, so
+ *                   the host cannot check it before the launch.
  *   a_rows          rows of A as stored (its 1x128 scale table is
  *                   [K/128][a_rows]); sizes the launch on the host.
  *   A               [a_rows][K], transposed = 0, GRAN_1x128 or GRAN_TENSOR.
@@ -348,9 +358,14 @@ int fp8_attention_fwd(int64_t seq_q, int64_t seq_k, int32_t heads_q, int32_t hea
 /* Message for the last non-OK status returned on the calling host thread. */
 const char* fp8bs_last_error(void);
 
-/* Synchronizes `stream`, then returns FP8BS_ERR_DEVICE_TIMEOUT if any kernel
- * of this library gave up on a bounded wait since the last call (and clears
- * the record), FP8BS_ERR_CUDA on a CUDA error, else FP8BS_OK. */
+/* Synchronizes `stream`, then reads and clears the library's device status
+ * word: FP8BS_ERR_INVALID_ARG if a grouped product found its row_offsets
+ * decreasing (it then wrote nothing), FP8BS_ERR_DEVICE_TIMEOUT if a kernel
+ * gave up on a bounded wait, FP8BS_ERR_CUDA on a CUDA error, else FP8BS_OK.
+ * The status word is one per process and device, shared by every stream:
+ * it covers the kernels of all streams since the previous call, and it is
+ * only complete once every stream that ran this library's kernels has been
+ * synchronized (this call synchronizes `stream` alone). */
 int fp8bs_device_status(fp8bs_stream_t stream);
 
 /* Self-test of the device-side failure detection: launches one thread that

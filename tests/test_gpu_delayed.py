@@ -17,7 +17,7 @@ def _run(shape, steps, L, fmt, margin, scale_fn):
     for t in range(steps):
         x = inputs.student_t(shape, 3.0, scale_fn(t), seed=100 + t)
         q_ref, amax_ref = ref.step(x)
-        q = st.quantize(dev_bf16(x))
+        q = st.quantize(dev_bf16(x), update=True)
         assert np.array_equal(host(q), q_ref), t
         assert f32_bits(host(st.amax))[0] == f32_bits([amax_ref])[0], t
         assert np.array_equal(f32_bits(host(st.history)), f32_bits(ref.history)), t
@@ -43,9 +43,4 @@ def test_delayed_save_restore():
     st2.load_state_dict(sd)
     x = inputs.student_t((32, 512), 3.0, 1e-3, seed=999)
     q_ref, _ = ref.step(x)
-    assert np.array_equal(host(st2.quantize(dev_bf16(x))), q_ref)
-
-
-def test_delayed_full_size_dy():
-    """dY of the up-projection backward [8192, 14336], 3 steps."""
-    _run((8192, 14336), 3, 1024, fp8.E5M2, 0, lambda t: 1e-3)
+    assert np.array_equal(host(st2.quantize(dev_bf16(x), update=True)), q_ref)

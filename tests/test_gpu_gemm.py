@@ -235,3 +235,111 @@ def test_llama31_8b_linears_sampled(name, N, K):
     for out in (fp8.OUT_BF16, fp8.OUT_F32):
         y = fp8.fp8_block_gemm(A_d, B_d, M, N, K, out)
         _check(y, y_ref, yabs, out, rows, cols)
+
+
+# ------------------------------------- many tiles per CTA, many groups
+@pytest.mark.parametrize("a_t,b_t,a_gran,b_gran,fa", [
+    (False, True, orc.GRAN_1x128, orc.GRAN_128x128, orc.E4M3),   # dgrad, blockwise
+    (False, True, orc.GRAN_TENSOR, orc.GRAN_TENSOR, orc.E5M2),   # dgrad, per-tensor (whole K in TMEM)
+    (True, True, orc.GRAN_TENSOR, orc.GRAN_TENSOR, orc.E5M2),    # wgrad, per-tensor (whole K in TMEM)
+    (True, True, orc.GRAN_128x128, orc.GRAN_128x128, orc.E4M3),  # wgrad, 128x128
+    (True, False, orc.GRAN_TENSOR, orc.GRAN_128x128, orc.E5M2),
+    (False, False, orc.GRAN_TENSOR, orc.GRAN_TENSOR, orc.E5M2),  # K-major, whole K in TMEM
+])
+def test_transposed_operands_many_tiles_per_cta(a_t, b_t, a_gran, b_gran, fa):
+    """32 x 10 = 320 output tiles on 152 persistent CTAs: every CTA takes two or
+    three tiles, so the TMEM buffers and every barrier phase are reused across
+    tiles; every tile is sampled (two rows per 128-row block, two columns per
+    256-column block)."""
+    M, N, K = 4096, 2560, 512
+    A_o, B_o, A_d, B_d = _case(M, N, K, a_gran, b_gran, fa=fa, a_t=a_t, b_t=b_t, seed=17)
+    rng = np.random.default_rng(M + N)
+    rows = np.unique(np.concatenate([stratified(M, 128, rng), stratified(M, 128, rng)]))
+    cols = np.unique(np.concatenate([stratified(N, 256, rng), stratified(N, 256, rng)]))
+    y_ref, yabs = orc.gemm(M, N, K, A_o, B_o, rows=rows, cols=cols)
+    for out in (fp8.OUT_F32, fp8.OUT_BF16):
+        _check(fp8.fp8_block_gemm(A_d, B_d, M, N, K, out), y_ref, yabs, out, rows, cols)
+    fp8.device_status()
+
+
+def _grouped_operands(loads, N, K, seed, extra_rows=0):
+    G = loads.size
+    off = np.zeros(G + 1, np.int32)
+    off[1:] = np.cumsum(loads)
+    T = int(off[-1])
+    a_rows = T + extra_rows
+    x = inputs.activations(a_rows, K, seed=seed)
+    w = inputs.gaussian((G * N, K), 0.02, seed=seed + 1)
+    qa, sa = orc.quantize_1x128(x)
+    qw, sw = orc.quantize_128x128(w)
+    sw = sw.reshape(G, (N + 127) // 128, K // 128)
+    return off, T, a_rows, qa, sa, qw, sw
+
+
+def test_grouped_more_than_32_groups():
+    """40 groups (the device prefix of m-slots runs over two 32-group chunks):
+    empty, 1-row, exactly-128-row and multi-slot groups; 5 rows past the last
+    group stay untouched."""
+    import torch
+    rng = np.random.default_rng(41)
+    loads = rng.integers(0, 300, 40)
+    loads[[0, 7, 33]] = 0
+    loads[[3, 35]] = 1
+    loads[[12, 39]] = 128
+    N, K = 384, 256
+    off, T, a_rows, qa, sa, qw, sw = _grouped_operands(loads, N, K, seed=43, extra_rows=5)
+    A_o = orc.operand(qa, orc.E4M3, orc.GRAN_1x128, sa)
+    B_o = orc.operand(qw, orc.E4M3, orc.GRAN_128x128, sw)
+    y_ref, yabs = orc.grouped_gemm(off, a_rows, N, K, A_o, B_o, rows=np.arange(T))
+    y = torch.full((a_rows, N), float("nan"), device="cuda")
+    fp8.fp8_grouped_block_gemm(dev(off), fp8.operand(dev(qa), dev(sa)),
+                               fp8.operand(dev(qw), dev(sw), gran=fp8.GRAN_128x128),
+                               a_rows, N, K, fp8.OUT_F32, y=y)
+    fp8.device_status()
+    yh = host(y)
+    _check(y[:T], y_ref, yabs, fp8.OUT_F32)
+    assert np.all(np.isnan(yh[T:]))
+
+
+def test_grouped_decreasing_offsets_are_reported_and_nothing_is_written():
+    """A decreasing offset table would give overlapping groups (two tiles
+    writing the same rows).  The kernel writes nothing and the device status
+    reports an invalid argument; the next product runs normally."""
+    import torch
+    loads = np.array([200, 100, 150])
+    N, K = 256, 256
+    off, T, a_rows, qa, sa, qw, sw = _grouped_operands(loads, N, K, seed=47)
+    A_d = fp8.operand(dev(qa), dev(sa))
+    B_d = fp8.operand(dev(qw), dev(sw), gran=fp8.GRAN_128x128)
+    bad_off = np.array([0, 200, 120, 450], np.int32)      # group 1 ends before it starts
+    y = torch.full((a_rows, N), float("nan"), device="cuda")
+    fp8.fp8_grouped_block_gemm(dev(bad_off), A_d, B_d, a_rows, N, K, fp8.OUT_F32, y=y)
+    with pytest.raises(fp8.Fp8bsError) as e:
+        fp8.device_status()
+    assert e.value.code == -1
+    assert np.all(np.isnan(host(y)))
+    fp8.device_status()                                   # the record was cleared
+    y_ref, yabs = orc.grouped_gemm(off, a_rows, N, K, orc.operand(qa, orc.E4M3, orc.GRAN_1x128, sa),
+                                   orc.operand(qw, orc.E4M3, orc.GRAN_128x128, sw), rows=np.arange(T))
+    fp8.fp8_grouped_block_gemm(dev(off), A_d, B_d, a_rows, N, K, fp8.OUT_F32, y=y)
+    fp8.device_status()
+    _check(y[:T], y_ref, yabs, fp8.OUT_F32)
+
+
+def test_pow2_mode_with_per_tensor_scales_that_are_not_powers_of_two():
+    """Under POW2 the block scales are powers of two, but a per-tensor scale
+    (delayed scaling: amax_history / fmax) in general is not; such products
+    must still give the exact sum."""
+    M, N, K = 256, 512, 512
+    a = inputs.activations(M, K, seed=53)
+    b = inputs.gaussian((N, K), 0.02, seed=54)
+    amax = float(np.abs(inputs.bits_to_f32(a)).max())
+    s_t = np.float32([amax / 448.0 * 1.37])               # not a power of two
+    qa, _ = orc.quantize_tensor(a, orc.E4M3, float(s_t[0]))
+    qb, sb = orc.quantize_128x128(b, orc.E4M3, orc.SCALE_POW2)
+    y_ref, yabs = orc.gemm(M, N, K, orc.operand(qa, orc.E4M3, orc.GRAN_TENSOR, s_t),
+                           orc.operand(qb, orc.E4M3, orc.GRAN_128x128, sb))
+    y = fp8.fp8_block_gemm(fp8.operand(dev(qa), dev(s_t), gran=fp8.GRAN_TENSOR),
+                           fp8.operand(dev(qb), dev(sb), gran=fp8.GRAN_128x128), M, N, K, fp8.OUT_F32,
+                           fp8.SCALE_POW2)
+    _check(y, y_ref, yabs, fp8.OUT_F32)

@@ -241,7 +241,7 @@ class Fprop:
                            M * it["K"] * 3 + 4 * M * (it["K"] // 128) + it["N"] * it["K"] * 3
                            + 4 * ((it["N"] + 127) // 128) * (it["K"] // 128)) for it in self.items]
         self.flops = sum(u[1] for u in self.units)
-        self.launches = 3 * len(self.items)
+        self.launches = (3 if self.mx else 2) * len(self.items)
         self.config = self.static_config(cfg, only)
 
     @staticmethod
@@ -259,10 +259,9 @@ class Fprop:
                 _run(rec, "quant:" + it["name"], lambda it=it: (
                     fp8.fp8_quantize_mx(it["x"], fp8.E4M3, q=it["qx"], scales=it["sx"]),
                     fp8.fp8_quantize_mx(it["w"], fp8.E4M3, q=it["qw"], scales=it["sw"])))
-            else:
-                _run(rec, "quant:" + it["name"], lambda it=it: (
-                    fp8.fp8_quantize_1x128(it["x"], fp8.E4M3, mode, q=it["qx"], scales=it["sx"]),
-                    fp8.fp8_quantize_128x128(it["w"], fp8.E4M3, mode, q=it["qw"], scales=it["sw"])))
+            else:   # X (1x128) and W (128x128) in one launch
+                _run(rec, "quant:" + it["name"], lambda it=it: fp8.fp8_quantize_linear(
+                    it["x"], it["w"], fp8.E4M3, mode, qx=it["qx"], sx=it["sx"], qw=it["qw"], sw=it["sw"]))
             _run(rec, "gemm:" + it["name"], lambda it=it: fp8.fp8_block_gemm(
                 it["A"], it["B"], M, it["N"], it["K"], fp8.OUT_BF16, mode, y=it["y"]))
 
@@ -278,8 +277,8 @@ class Fprop:
                 fp8.fp8_quantize_mx(it["x"], fp8.E4M3, q=it["qx"], scales=it["sx"])
                 fp8.fp8_quantize_mx(it["w"], fp8.E4M3, q=it["qw"], scales=it["sw"])
             else:
-                fp8.fp8_quantize_1x128(it["x"], fp8.E4M3, mode, q=it["qx"], scales=it["sx"])
-                fp8.fp8_quantize_128x128(it["w"], fp8.E4M3, mode, q=it["qw"], scales=it["sw"])
+                fp8.fp8_quantize_linear(it["x"], it["w"], fp8.E4M3, mode, qx=it["qx"], sx=it["sx"], qw=it["qw"],
+                                        sw=it["sw"])
             fp8.fp8_block_gemm(it["A"], it["B"], M, it["N"], it["K"], fp8.OUT_BF16, mode, y=it["y"])
 
         return [([it["x"], it["w"]], [it["y"]], lambda it=it: unit(it)) for it in self.items]
@@ -460,7 +459,7 @@ class MoE:
         self.units = [(it["name"], 2.0 * T * it["N"] * it["K"],
                        3 * T * it["K"] + 3 * G * it["N"] * it["K"]) for it in self.items]
         self.flops = sum(u[1] for u in self.units)
-        self.launches = 3 * len(self.items)
+        self.launches = 2 * len(self.items)
         self.config = {"workload": cfg["name"] + (f" ({only} only)" if only else ""), "rows": T,
                        "experts": G, "max_rows": int(loads.max()), "min_rows": int(loads.min()),
                        "linears": [[it["name"], it["N"], it["K"]] for it in self.items],
@@ -470,9 +469,8 @@ class MoE:
         fp8, T = self.fp8, self.T
         for it in self.items:
             # the stacked [G*N][K] weights quantize per expert tile since N % 128 == 0
-            _run(rec, "quant:" + it["name"], lambda it=it: (
-                fp8.fp8_quantize_1x128(it["x"], q=it["qx"], scales=it["sx"]),
-                fp8.fp8_quantize_128x128(it["w"], q=it["qw"], scales=it["sw"])))
+            _run(rec, "quant:" + it["name"], lambda it=it: fp8.fp8_quantize_linear(
+                it["x"], it["w"], qx=it["qx"], sx=it["sx"], qw=it["qw"], sw=it["sw"]))
             _run(rec, "gemm:" + it["name"], lambda it=it: fp8.fp8_grouped_block_gemm(
                 self.off, it["A"], it["B"], T, it["N"], it["K"], fp8.OUT_BF16, y=it["y"]))
 

@@ -73,6 +73,7 @@ def lib() -> ctypes.CDLL:
             "fp8_quantize_128x128": [vp, i64, i64, i64, i32, i32, vp, i64, vp, vp],
             "fp8_quantize_tensor_delayed": [vp, i64, i32, vp, vp, vp, vp],
             "fp8_quantize_mx": [vp, i64, i64, i64, i32, vp, i64, vp, vp],
+            "fp8_quantize_linear": [vp, i64, i64, vp, i64, vp, vp, i64, i64, vp, i64, vp, i64, i32, i32, vp],
             "fp8_quantize_1x128_colwise": [vp, i64, i64, i64, i32, i32, vp, i64, vp, vp, i64, vp, vp],
             "fp8_amax_history_update": [vp, vp, i32, vp, i32, i32, vp, vp],
             "fp8_block_gemm": [i64, i64, i64, op, op, i32, vp, i64, i32, vp],
@@ -162,6 +163,34 @@ def fp8_quantize_128x128(w, fmt=E4M3, mode=SCALE_FP32, q=None, scales=None, stre
     _call("fp8_quantize_128x128", w.data_ptr(), rows, cols, w.stride(0), fmt, mode,
           q.data_ptr(), q.stride(0), scales.data_ptr(), _stream(stream))
     return q, scales
+
+
+def fp8_quantize_linear(x, w, fmt=E4M3, mode=SCALE_FP32, qx=None, sx=None, qw=None, sw=None, stream=None):
+    """Both operands of a linear layer in one launch: x [m, k] per 1x128 tile,
+    w [n, k] per 128x128 tile.  Returns (qx, sx, qw, sw) exactly as
+    fp8_quantize_1x128(x) and fp8_quantize_128x128(w) return them."""
+    torch = _torch()
+    _rowmajor(_dev(x, "x", torch.bfloat16), "x")
+    _rowmajor(_dev(w, "w", torch.bfloat16), "w")
+    m, k = x.shape
+    n, kw = w.shape
+    if kw != k:
+        raise ValueError(f"x has {k} columns, w has {kw}")
+    if qx is None:
+        qx = torch.empty((m, k), dtype=torch.uint8, device=x.device)
+    if sx is None:
+        sx = torch.empty((k // 128, m), dtype=torch.float32, device=x.device)
+    if qw is None:
+        qw = torch.empty((n, k), dtype=torch.uint8, device=w.device)
+    if sw is None:
+        sw = torch.empty(((n + 127) // 128, k // 128), dtype=torch.float32, device=w.device)
+    for t, nm in ((qx, "qx"), (qw, "qw")):
+        _rowmajor(_dev(t, nm, torch.uint8), nm)
+    _dev(sx, "sx", torch.float32)
+    _dev(sw, "sw", torch.float32)
+    _call("fp8_quantize_linear", x.data_ptr(), m, x.stride(0), qx.data_ptr(), qx.stride(0), sx.data_ptr(),
+          w.data_ptr(), n, w.stride(0), qw.data_ptr(), qw.stride(0), sw.data_ptr(), k, fmt, mode, _stream(stream))
+    return qx, sx, qw, sw
 
 
 def fp8_quantize_mx(x, fmt=E4M3, q=None, scales=None, stream=None):
@@ -366,8 +395,7 @@ def fp8_grouped_block_gemm_quant(offsets, A: Operand, B: Operand, a_rows: int, N
 def linear_fprop(x, w, mode=SCALE_FP32, out_dtype=OUT_BF16, stream=None):
     """FP8 linear layer forward: Y = X W^T with X quantized per 1x128 tile and
     W per 128x128 tile (E4M3), block-scaled FP8 GEMM, fp32 accumulation."""
-    qx, sx = fp8_quantize_1x128(x, E4M3, mode, stream=stream)
-    qw, sw = fp8_quantize_128x128(w, E4M3, mode, stream=stream)
+    qx, sx, qw, sw = fp8_quantize_linear(x, w, E4M3, mode, stream=stream)
     A = operand(qx, sx, E4M3, GRAN_1x128)
     B = operand(qw, sw, E4M3, GRAN_128x128)
     return fp8_block_gemm(A, B, x.shape[0], w.shape[0], x.shape[1], out_dtype, mode, stream=stream)

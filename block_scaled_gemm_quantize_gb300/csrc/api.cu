@@ -358,6 +358,23 @@ int fp8_quantize_128x128(const void* w, int64_t rows, int64_t cols, int64_t ld_w
     return e == cudaSuccess ? FP8BS_OK : cuda_fail(e, "fp8_quantize_128x128");
 }
 
+int fp8_quantize_linear(const void* x, int64_t m, int64_t ld_x, uint8_t* qx, int64_t ld_qx, float* sx,
+                        const void* w, int64_t n, int64_t ld_w, uint8_t* qw, int64_t ld_qw, float* sw,
+                        int64_t k, int32_t fmt, int32_t mode, fp8bs_stream_t stream) {
+    const char* fn = "fp8_quantize_linear";
+    if (m < 0 || n < 0 || k < 0) return fail(FP8BS_ERR_INVALID_ARG, "%s: negative size", fn);
+    // each operand is checked exactly as its own quantizer checks it
+    int rx = check_block_quant(fn, x, m, k, ld_x, fmt, mode, qx, ld_qx, sx);
+    if (rx < 0) return rx;
+    int rw = check_block_quant(fn, w, n, k, ld_w, fmt, mode, qw, ld_qw, sw);
+    if (rw < 0) return rw;
+    if (rx == 0 && rw == 0) return FP8BS_OK;
+    cudaError_t e = fp8bs::launch_quant_linear(
+        static_cast<const uint16_t*>(x), rx ? m : 0, ld_x, qx, ld_qx, sx, static_cast<const uint16_t*>(w),
+        rw ? n : 0, ld_w, qw, ld_qw, sw, k, fmt, mode, (cudaStream_t)stream);
+    return e == cudaSuccess ? FP8BS_OK : cuda_fail(e, fn);
+}
+
 int fp8_quantize_mx(const void* x, int64_t rows, int64_t cols, int64_t ld_x, int32_t fmt, uint8_t* q,
                     int64_t ld_q, uint8_t* scales, fp8bs_stream_t stream) {
     const char* fn = "fp8_quantize_mx";

@@ -67,6 +67,11 @@ constexpr int EPI_WARP0 = 4;
 constexpr int REGS_LOW = FP8BS_REGS_LOW, REGS_HIGH = (384 * 168 - 128 * REGS_LOW) / 256;
 static_assert(REGS_LOW % 8 == 0 && REGS_HIGH % 8 == 0 && 128 * REGS_LOW + 256 * REGS_HIGH == 384 * 168,
               "register split");
+// Block scales of the promotion staged in shared memory by the otherwise
+// idle warp 2 (no global load in the epilogue's K loop)
+#ifndef FP8BS_SCALES_SMEM
+#define FP8BS_SCALES_SMEM 0
+#endif
 #ifndef FP8BS_EPI_PIPE
 #define FP8BS_EPI_PIPE 0
 #endif
@@ -652,6 +657,71 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 }
             }
         }
+#if FP8BS_SCALES_SMEM
+      } else if (!B_COL && warp == 2) {
+        // ------------------------------------------- block-scale loader
+        // Per promotion group (P K blocks) of every tile, the 128 row scales
+        // of A and the column-block scales of B into a shared-memory ring
+        // slot: sa[row] at 4 row, sb[half] at 512 + 4 half, the up-rows'
+        // sb[half] at 520 + 4 half (SwiGLU).  The epilogue then issues no
+        // global load in its K loop.  Global loads of group i + 1 are in
+        // flight while group i waits for its slot.
+        const int ngroups = (nkb + P - 1) / P;
+        const int64_t nkb64 = nkb;
+        auto fetch = [&](int t, int g, float (&va)[4], float& vb) {
+            const Tile tl = decode_tile(t, total_slots, p.tiles_n, G, s_slot, s_off);
+            const int64_t kb = static_cast<int64_t>(g) * P;
+#pragma unroll
+            for (int i = 0; i < 4; i++) {
+                int64_t srow = static_cast<int64_t>(tl.row0) + 4 * lane + i;
+                srow = srow < p.a_rows ? srow : p.a_rows - 1;
+                const float* pa;
+                if (p.a_gran == 0) pa = p.sa + kb * p.a_rows + srow;
+                else if (p.a_gran == 1) pa = A_MN ? p.sa + kb * p.a_rblocks + srow / 128
+                                                  : p.sa + (srow / 128) * nkb64 + kb;
+                else pa = p.sa;
+                va[i] = ld_scale(pa);
+            }
+            vb = 0.0f;
+            if (lane < 4) {   // lanes 0, 1: sb of halves 0, 1; lanes 2, 3: the up rows' (SwiGLU)
+                const int half = lane & 1;
+                const int64_t col0 = static_cast<int64_t>(tl.nt) * BN + half * 128;
+                int64_t nb = SWIGLU ? (lane < 2 ? static_cast<int64_t>(tl.nt) : p.swiglu_i / 128 + tl.nt)
+                                    : min(col0, p.N - 1) / 128;
+                const float* pb;
+                if (p.b_gran == 1) pb = B_MN ? p.sb + kb * p.b_rblocks + nb
+                                             : p.sb + tl.g * p.b_scale_group_stride + nb * nkb64 + kb;
+                else pb = p.sb;
+                vb = ld_scale(pb);
+            }
+        };
+        int slot = 0;
+        uint32_t ph = 0;
+        bool ok = true;
+        int t = blockIdx.x, g = 0;
+        float va[4], vb;
+        if (t < total_tiles) fetch(t, g, va, vb);
+        while (ok && t < total_tiles) {
+            int tn = t, gn = g + 1;
+            if (gn == ngroups) { gn = 0; tn += gridDim.x; }
+            float na[4], nb2 = 0.0f;
+            if (tn < total_tiles) fetch(tn, gn, na, nb2);
+            ok = __all_sync(0xFFFFFFFFu, wait_or_flag(bsf_empty(slot), ph ^ 1u));
+            if (!ok) break;
+            const uint32_t dst = sbase + L::kBsfOff + slot * BSF_SLOT_BYTES;
+            st_shared_v4(dst + lane * 16, __float_as_uint(va[0]), __float_as_uint(va[1]),
+                         __float_as_uint(va[2]), __float_as_uint(va[3]));
+            if (lane < 4) st_shared_f32(dst + 512 + lane * 4, vb);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bsf_full(slot));
+            if (++slot == BSF_SLOTS) { slot = 0; ph ^= 1u; }
+#pragma unroll
+            for (int i = 0; i < 4; i++) va[i] = na[i];
+            vb = nb2;
+            t = tn;
+            g = gn;
+        }
+#endif
       }
     } else if (B_COL) {
         asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(REGS_HIGH));
@@ -752,6 +822,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         uint32_t chunk = 0, tile_i = 0;
         bool ok = true;
         const int64_t nkb64 = nkb;
+#if FP8BS_SCALES_SMEM
+        int sslot = 0;        // scale ring slot (the loader warp's order)
+        uint32_t sph = 0;
+#endif
         for (int t = blockIdx.x; ok && t < total_tiles; t += gridDim.x, tile_i++) {
             const Tile tl = decode_tile(t, total_slots, p.tiles_n, G, s_slot, s_off);
             const int64_t row = static_cast<int64_t>(tl.row0) + lrow;
@@ -785,6 +859,50 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             uint64_t acc[64];   // 128 fp32 accumulators as packed pairs
 #pragma unroll
             for (int i = 0; i < 64; i++) acc[i] = 0;
+#if FP8BS_SCALES_SMEM
+            (void)pa; (void)pb; (void)pbu; (void)sa_step; (void)sb_step;
+            if (H == 1) {
+                const int ngroups = (nkb + P - 1) / P;
+                for (int g = 0; ok && g < ngroups; g++) {
+                    // this group's two scales from the loader's ring slot
+                    ok = __all_sync(0xFFFFFFFFu, wait_or_flag(bsf_full(sslot), sph));
+                    if (!ok) break;
+                    const uint32_t src = sbase + L::kBsfOff + sslot * BSF_SLOT_BYTES;
+                    const float sa = ld_shared_f32(src + lrow * 4);
+                    const float sb = ld_shared_f32(src + 512 + half * 4);
+                    const float sbu = SWIGLU ? ld_shared_f32(src + 520 + half * 4) : sb;
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(bsf_empty(sslot));
+                    if (++sslot == BSF_SLOTS) { sslot = 0; sph ^= 1u; }
+                    const float s = sa * sb;
+                    const uint64_t s2 = pack_f32x2(__float_as_uint(s), __float_as_uint(s));
+                    const float su = sa * sbu;
+                    const uint64_t s2u = pack_f32x2(__float_as_uint(su), __float_as_uint(su));
+                    const uint32_t buf = chunk % TBUFS;
+                    ok = __all_sync(0xFFFFFFFFu, wait_or_flag(tfull_bar(buf), (chunk / TBUFS) & 1u));
+                    if (!ok) break;
+                    tc_fence_after();
+                    const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
+                                           buf * MMA_N + half * 128;
+#pragma unroll
+                    for (int j = 0; j < 4; j++) {
+                        uint32_t r[32];
+                        tmem_ld_32x32b_x32(taddr + j * 32, r);
+                        tmem_wait_ld();
+                        if (j == 3) {
+                            tc_fence_before();
+                            __syncwarp();
+                            if (lane == 0) mbar_arrive(tempty_bar(buf));
+                        }
+#pragma unroll
+                        for (int q = 0; q < 16; q++)
+                            fma_f32x2(acc[j * 16 + q], pack_f32x2(r[2 * q], r[2 * q + 1]), j < 2 ? s2 : s2u);
+                    }
+                    chunk++;
+                }
+            } else
+#endif
+            {
             // Scales: a ring of SPF register slots, slot i holding chunk
             // (kb0 + i); the K-block loop is unrolled by SPF so each slot is
             // refilled (SPF chunks ahead) right after use, with no register
@@ -919,6 +1037,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     }
                     chunk++;
                 }
+            }
             }
             if (!ok) break;
             ok = finish_tile<SWIGLU>(p, tmY, acc, tl, row, row_ok, col0, quarter, half, lane,

@@ -70,19 +70,15 @@ __device__ __forceinline__ void quant8(const float (&f)[8], float r, uint32_t& l
 // K block, x = group of 16*U rows; the 16 half-warps of a CTA take 16
 // consecutive rows, so each of the U rounds writes 16 consecutive scales, and
 // each thread keeps U loads in flight.
-#ifndef FP8BS_Q1_ALONG_K
-#define FP8BS_Q1_ALONG_K 1
-#endif
 template <int FMT, int MODE, int U>
-__global__ void __launch_bounds__(256) k_quant_1x128(const uint16_t* __restrict__ x, int64_t rows,
-                                                    int64_t ldx, int64_t nkb, uint8_t* __restrict__ q,
-                                                    int64_t ldq, float* __restrict__ scales) {
+__device__ __forceinline__ void quant_1x128_block(const uint16_t* __restrict__ x, int64_t rows, int64_t ldx,
+                                                  int64_t nkb, uint8_t* __restrict__ q, int64_t ldq,
+                                                  float* __restrict__ scales, int64_t bx, int64_t by) {
+    // a half-warp walks U consecutive K blocks of one row (U x 256 contiguous bytes)
     const int l16 = threadIdx.x & 15;
     const int hw = threadIdx.x >> 4;
-#if FP8BS_Q1_ALONG_K
-    // a half-warp walks U consecutive K blocks of one row (U x 256 contiguous bytes)
-    const int64_t r = static_cast<int64_t>(blockIdx.x) * 16 + hw;
-    const int64_t kb0 = static_cast<int64_t>(blockIdx.y) * U;
+    const int64_t r = bx * 16 + hw;
+    const int64_t kb0 = by * U;
     const bool rok = r < rows;
     const uint16_t* xr = x + r * ldx + kb0 * 128 + l16 * 8;
     uint4 v[U];
@@ -108,36 +104,13 @@ __global__ void __launch_bounds__(256) k_quant_1x128(const uint16_t* __restrict_
             if (l16 == 0) scales[kb * rows + r] = s;
         }
     }
-#else
-    const int64_t kb = blockIdx.y;
-    const int64_t r0 = static_cast<int64_t>(blockIdx.x) * (16 * U) + hw;
-    const uint16_t* xk = x + kb * 128 + l16 * 8;
-    uint4 v[U];
-#pragma unroll
-    for (int i = 0; i < U; i++) {
-        const int64_t r = r0 + 16 * i;
-        v[i] = make_uint4(0, 0, 0, 0);
-        if (r < rows) v[i] = ld_stream_v4(xk + r * ldx);
-    }
-#pragma unroll
-    for (int i = 0; i < U; i++) {
-        const int64_t r = r0 + 16 * i;
-        float f[8];
-        unpack8(v[i], f);
-        float m = amax8(f);
-#pragma unroll
-        for (int o = 8; o >= 1; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
-        if (r < rows) {
-            const float s = block_scale<FMT, MODE>(m);
-            const float rc = __frcp_rn(s);
-            uint32_t lo, hi;
-            quant8<FMT>(f, rc, lo, hi);
-            st_v2(q + r * ldq + kb * 128 + l16 * 8, lo, hi);
-            if (l16 == 0) scales[kb * rows + r] = s;
-        }
-    }
-    (void)nkb;
-#endif
+}
+
+template <int FMT, int MODE, int U>
+__global__ void __launch_bounds__(256) k_quant_1x128(const uint16_t* __restrict__ x, int64_t rows,
+                                                    int64_t ldx, int64_t nkb, uint8_t* __restrict__ q,
+                                                    int64_t ldq, float* __restrict__ scales) {
+    quant_1x128_block<FMT, MODE, U>(x, rows, ldx, nkb, q, ldq, scales, blockIdx.x, blockIdx.y);
 }
 
 // -------------------------------------------------------------- 128x128
@@ -149,13 +122,11 @@ __global__ void __launch_bounds__(256) k_quant_1x128(const uint16_t* __restrict_
 #define FP8BS_Q128_MINB 3
 #endif
 template <int FMT, int MODE>
-__global__ void __launch_bounds__(256, FP8BS_Q128_MINB) k_quant_128x128(const uint16_t* __restrict__ w, int64_t rows,
-                                                      int64_t ldw, int64_t nkb,
-                                                      uint8_t* __restrict__ q, int64_t ldq,
-                                                      float* __restrict__ scales) {
-    __shared__ float red[8];
-    const int64_t rb = blockIdx.x / nkb;
-    const int64_t kb = blockIdx.x - rb * nkb;
+__device__ __forceinline__ void quant_128x128_tile(const uint16_t* __restrict__ w, int64_t rows, int64_t ldw,
+                                                   int64_t nkb, uint8_t* __restrict__ q, int64_t ldq,
+                                                   float* __restrict__ scales, int64_t tile, float* red) {
+    const int64_t rb = tile / nkb;
+    const int64_t kb = tile - rb * nkb;
     const int c = threadIdx.x & 15;
     const int r0 = threadIdx.x >> 4;
     uint4 v[8];
@@ -193,6 +164,37 @@ __global__ void __launch_bounds__(256, FP8BS_Q128_MINB) k_quant_128x128(const ui
         }
     }
     if (threadIdx.x == 0) scales[rb * nkb + kb] = s;
+}
+
+template <int FMT, int MODE>
+__global__ void __launch_bounds__(256, FP8BS_Q128_MINB) k_quant_128x128(const uint16_t* __restrict__ w, int64_t rows,
+                                                      int64_t ldw, int64_t nkb,
+                                                      uint8_t* __restrict__ q, int64_t ldq,
+                                                      float* __restrict__ scales) {
+    __shared__ float red[8];
+    quant_128x128_tile<FMT, MODE>(w, rows, ldw, nkb, q, ldq, scales, blockIdx.x, red);
+}
+
+// ------------------------------------------------- one linear's two operands
+// X per 1x128 tile and W per 128x128 tile in one launch: the first nx_blocks
+// CTAs run the 1x128 work (a CTA = 16 rows x U K blocks), the rest one
+// 128x128 tile each.  One launch, one ramp and one tail instead of two.
+struct LinearQuantArgs {
+    const uint16_t* x; int64_t m, ldx; uint8_t* qx; int64_t ldqx; float* sx;
+    const uint16_t* w; int64_t n, ldw; uint8_t* qw; int64_t ldqw; float* sw;
+    int64_t nkb, gy, nx_blocks;
+};
+
+template <int FMT, int MODE, int U>
+__global__ void __launch_bounds__(256, FP8BS_Q128_MINB) k_quant_linear(const LinearQuantArgs a) {
+    __shared__ float red[8];
+    const int64_t b = blockIdx.x;
+    if (b < a.nx_blocks) {
+        const int64_t bx = b / a.gy;
+        quant_1x128_block<FMT, MODE, U>(a.x, a.m, a.ldx, a.nkb, a.qx, a.ldqx, a.sx, bx, b - bx * a.gy);
+    } else {
+        quant_128x128_tile<FMT, MODE>(a.w, a.n, a.ldw, a.nkb, a.qw, a.ldqw, a.sw, b - a.nx_blocks, red);
+    }
 }
 
 // ---------------------------------------------------------------- MXFP8
@@ -428,16 +430,30 @@ cudaError_t launch_quant_1x128(const uint16_t* x, int64_t rows, int64_t cols, in
                                int fmt, int mode, uint8_t* q, int64_t ldq, float* scales,
                                cudaStream_t st) {
     const int64_t nkb = cols / 128;
-#if FP8BS_Q1_ALONG_K
     const int64_t gx = (rows + 15) / 16, gy = (nkb + kU1 - 1) / kU1;
-#else
-    const int64_t gx = (rows + 16 * kU1 - 1) / (16 * kU1), gy = nkb;
-#endif
     if (gx > 0x7FFFFFFF || gy > 65535) return cudaErrorInvalidValue;
     auto k = fmt == 0 ? (mode == 0 ? k_quant_1x128<0, 0, kU1> : k_quant_1x128<0, 1, kU1>)
                       : (mode == 0 ? k_quant_1x128<1, 0, kU1> : k_quant_1x128<1, 1, kU1>);
     k<<<dim3(static_cast<unsigned>(gx), static_cast<unsigned>(gy)), 256, 0, st>>>(x, rows, ldx, nkb, q, ldq,
                                                                                  scales);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_quant_linear(const uint16_t* x, int64_t m, int64_t ldx, uint8_t* qx, int64_t ldqx, float* sx,
+                                const uint16_t* w, int64_t n, int64_t ldw, uint8_t* qw, int64_t ldqw, float* sw,
+                                int64_t k, int fmt, int mode, cudaStream_t st) {
+    LinearQuantArgs a;
+    a.x = x; a.m = m; a.ldx = ldx; a.qx = qx; a.ldqx = ldqx; a.sx = sx;
+    a.w = w; a.n = n; a.ldw = ldw; a.qw = qw; a.ldqw = ldqw; a.sw = sw;
+    a.nkb = k / 128;
+    a.gy = (a.nkb + kU1 - 1) / kU1;
+    a.nx_blocks = ((m + 15) / 16) * a.gy;
+    const int64_t grid = a.nx_blocks + ((n + 127) / 128) * a.nkb;
+    if (grid <= 0) return cudaSuccess;
+    if (grid > 0x7FFFFFFF) return cudaErrorInvalidValue;
+    auto kern = fmt == 0 ? (mode == 0 ? k_quant_linear<0, 0, kU1> : k_quant_linear<0, 1, kU1>)
+                         : (mode == 0 ? k_quant_linear<1, 0, kU1> : k_quant_linear<1, 1, kU1>);
+    kern<<<static_cast<unsigned>(grid), 256, 0, st>>>(a);
     return cudaGetLastError();
 }
 

@@ -98,6 +98,22 @@ int fp8_quantize_128x128(const void* w, int64_t rows, int64_t cols, int64_t ld_w
                          uint8_t* q, int64_t ld_q, float* scales, fp8bs_stream_t stream);
 
 /*
+ * Both FP8 operands of one linear layer in one launch: X [m][k] quantized
+ * exactly as fp8_quantize_1x128 does (codes qx [m][ld_qx], scales sx
+ * [k/128][m]) and W [n][k] exactly as fp8_quantize_128x128 does (codes qw
+ * [n][ld_qw], scales sw [ceil(n/128)][k/128]), with the same fmt and mode.
+ * The results equal the two separate calls bit for bit; the single launch
+ * saves the second launch's start-up and tail (the quantization overhead the
+ * NeMo RL page counts against the FP8 linear layer, hotbookzone.com
+ * "Ganancias de rendimiento en el mundo real").  Either operand may be
+ * empty (m or n == 0: its pointers are not read).
+ * Errors: those of fp8_quantize_1x128 for X and of fp8_quantize_128x128 for W.
+ */
+int fp8_quantize_linear(const void* x, int64_t m, int64_t ld_x, uint8_t* qx, int64_t ld_qx, float* sx,
+                        const void* w, int64_t n, int64_t ld_w, uint8_t* qw, int64_t ld_qw, float* sw,
+                        int64_t k, int32_t fmt, int32_t mode, fp8bs_stream_t stream);
+
+/*
  * MXFP8 (microscaling FP8) quantizer: one power-of-two scale per 32
  * consecutive elements of a row.  The introl page names MXFP8 as Blackwell's
  * hardware block scaling ("Requisitos de hardware para entrenamiento FP8";

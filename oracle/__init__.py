@@ -62,46 +62,44 @@ def _load():
 
 
 def _bind(lib):
-    if True:
-        if True:
-            i64, i32, vp, f32 = ctypes.c_int64, ctypes.c_int32, ctypes.c_void_p, ctypes.c_float
-            lib.fp8o_decode.argtypes = [ctypes.c_uint32, ctypes.c_int]
-            lib.fp8o_decode.restype = ctypes.c_double
-            lib.fp8o_fmax.argtypes = [ctypes.c_int]
-            lib.fp8o_fmax.restype = ctypes.c_double
-            lib.fp8o_encode.argtypes = [f32, ctypes.c_int]
-            lib.fp8o_encode.restype = ctypes.c_uint32
-            lib.fp8o_encode_array.argtypes = [vp, i64, ctypes.c_int, vp]
-            lib.fp8o_encode_array.restype = None
-            lib.fp8o_bf16_to_f32.argtypes = [ctypes.c_uint16]
-            lib.fp8o_bf16_to_f32.restype = f32
-            lib.fp8o_block_scale.argtypes = [f32, ctypes.c_int, ctypes.c_int]
-            lib.fp8o_block_scale.restype = f32
-            lib.fp8o_quantize_1x128.argtypes = [vp, i64, i64, i64, ctypes.c_int, ctypes.c_int, vp, i64, vp]
-            lib.fp8o_quantize_1x128.restype = None
-            lib.fp8o_quantize_1x128_f32.argtypes = [vp, i64, i64, i64, ctypes.c_int, ctypes.c_int, vp, i64,
-                                                    vp]
-            lib.fp8o_quantize_1x128_f32.restype = None
-            lib.fp8o_mx_scale_code.argtypes = [f32, ctypes.c_int]
-            lib.fp8o_mx_scale_code.restype = ctypes.c_uint8
-            lib.fp8o_quantize_mx.argtypes = [vp, i64, i64, i64, ctypes.c_int, vp, i64, vp]
-            lib.fp8o_quantize_mx.restype = None
-            lib.fp8o_quantize_128x128.argtypes = [vp, i64, i64, i64, ctypes.c_int, ctypes.c_int, vp, i64, vp]
-            lib.fp8o_quantize_128x128.restype = None
-            lib.fp8o_quantize_tensor.argtypes = [vp, i64, ctypes.c_int, f32, vp, vp]
-            lib.fp8o_quantize_tensor.restype = None
-            lib.fp8o_amax_history_update.argtypes = [vp, vp, i32, f32, ctypes.c_int, i32, vp]
-            lib.fp8o_amax_history_update.restype = None
-            lib.fp8o_gemm.argtypes = [i64, i64, i64, ctypes.POINTER(Operand), ctypes.POINTER(Operand),
-                                      i64, vp, i64, vp, vp, vp]
-            lib.fp8o_gemm.restype = ctypes.c_int
-            lib.fp8o_grouped_gemm.argtypes = [i32, vp, i64, i64, i64, ctypes.POINTER(Operand),
-                                              ctypes.POINTER(Operand), i64, vp, i64, vp, vp, vp]
-            lib.fp8o_grouped_gemm.restype = ctypes.c_int
-            lib.fp8o_attention.argtypes = [i64, i64, i32, i32, ctypes.c_int, ctypes.c_double,
-                                           vp, vp, ctypes.c_int, vp, vp, ctypes.c_int, vp, vp, ctypes.c_int,
-                                           i64, vp, vp, vp, vp, vp]
-            lib.fp8o_attention.restype = ctypes.c_int
+    i64, i32, vp, f32 = ctypes.c_int64, ctypes.c_int32, ctypes.c_void_p, ctypes.c_float
+    lib.fp8o_decode.argtypes = [ctypes.c_uint32, ctypes.c_int]
+    lib.fp8o_decode.restype = ctypes.c_double
+    lib.fp8o_fmax.argtypes = [ctypes.c_int]
+    lib.fp8o_fmax.restype = ctypes.c_double
+    lib.fp8o_encode.argtypes = [f32, ctypes.c_int]
+    lib.fp8o_encode.restype = ctypes.c_uint32
+    lib.fp8o_encode_array.argtypes = [vp, i64, ctypes.c_int, vp]
+    lib.fp8o_encode_array.restype = None
+    lib.fp8o_bf16_to_f32.argtypes = [ctypes.c_uint16]
+    lib.fp8o_bf16_to_f32.restype = f32
+    lib.fp8o_block_scale.argtypes = [f32, ctypes.c_int, ctypes.c_int]
+    lib.fp8o_block_scale.restype = f32
+    lib.fp8o_quantize_1x128.argtypes = [vp, i64, i64, i64, ctypes.c_int, ctypes.c_int, vp, i64, vp]
+    lib.fp8o_quantize_1x128.restype = None
+    lib.fp8o_quantize_1x128_f32.argtypes = [vp, i64, i64, i64, ctypes.c_int, ctypes.c_int, vp, i64,
+                                            vp]
+    lib.fp8o_quantize_1x128_f32.restype = None
+    lib.fp8o_mx_scale_code.argtypes = [f32, ctypes.c_int]
+    lib.fp8o_mx_scale_code.restype = ctypes.c_uint8
+    lib.fp8o_quantize_mx.argtypes = [vp, i64, i64, i64, ctypes.c_int, vp, i64, vp]
+    lib.fp8o_quantize_mx.restype = None
+    lib.fp8o_quantize_128x128.argtypes = [vp, i64, i64, i64, ctypes.c_int, ctypes.c_int, vp, i64, vp]
+    lib.fp8o_quantize_128x128.restype = None
+    lib.fp8o_quantize_tensor.argtypes = [vp, i64, ctypes.c_int, f32, vp, vp]
+    lib.fp8o_quantize_tensor.restype = None
+    lib.fp8o_amax_history_update.argtypes = [vp, vp, i32, f32, ctypes.c_int, i32, vp]
+    lib.fp8o_amax_history_update.restype = None
+    lib.fp8o_gemm.argtypes = [i64, i64, i64, ctypes.POINTER(Operand), ctypes.POINTER(Operand),
+                              i64, vp, i64, vp, vp, vp]
+    lib.fp8o_gemm.restype = ctypes.c_int
+    lib.fp8o_grouped_gemm.argtypes = [i32, vp, i64, i64, i64, ctypes.POINTER(Operand),
+                                      ctypes.POINTER(Operand), i64, vp, i64, vp, vp, vp]
+    lib.fp8o_grouped_gemm.restype = ctypes.c_int
+    lib.fp8o_attention.argtypes = [i64, i64, i32, i32, ctypes.c_int, ctypes.c_double,
+                                   vp, vp, ctypes.c_int, vp, vp, ctypes.c_int, vp, vp, ctypes.c_int,
+                                   i64, vp, vp, vp, vp, vp]
+    lib.fp8o_attention.restype = ctypes.c_int
     return lib
 
 

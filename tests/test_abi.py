@@ -156,3 +156,19 @@ def test_binding_refuses_cpu_tensors():
     x = torch.zeros(4, 128, dtype=torch.bfloat16)
     with pytest.raises(TypeError):
         fp8.fp8_quantize_1x128(x)
+
+
+def test_quantize_linear_validation(L):
+    f = L.fp8_quantize_linear
+    f.argtypes = [ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64, ctypes.c_void_p, ctypes.c_int64,
+                  ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64, ctypes.c_void_p,
+                  ctypes.c_int64, ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32, ctypes.c_int32,
+                  ctypes.c_void_p]
+    ok = (FAKE, 4, 256, FAKE, 256, FAKE)
+    assert f(None, 4, 256, FAKE, 256, FAKE, *ok, 256, 0, 0, None) == -1    # null x
+    assert f(*ok, FAKE, 4, 256, None, 256, FAKE, 256, 0, 0, None) == -1    # null qw
+    assert f(*ok, FAKE + 2, 4, 256, FAKE, 256, FAKE, 256, 0, 0, None) == -3  # misaligned w
+    assert f(*ok, *ok, 200, 0, 0, None) == -2                              # k % 128
+    assert f(*ok, *ok, 256, 0, 5, None) == -1                              # bad mode
+    assert f(*ok, *ok, -1, 0, 0, None) == -1                               # negative size
+    assert f(FAKE, 0, 256, FAKE, 256, FAKE, FAKE, 0, 256, FAKE, 256, FAKE, 256, 0, 0, None) == 0  # empty

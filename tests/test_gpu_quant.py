@@ -84,3 +84,24 @@ def test_pow2_scales_are_ue8m0_exact():
     x = inputs.activations(256, 1024, seed=4)
     _, s = fp8.fp8_quantize_1x128(dev_bf16(x), fp8.E4M3, fp8.SCALE_POW2)
     assert np.all((f32_bits(host(s)) & 0x7FFFFF) == 0)
+
+
+@pytest.mark.parametrize("M,N,K", [(300, 520, 640), (8192, 6144, 4096), (1, 128, 128), (0, 256, 256),
+                                   (256, 0, 256)])
+@pytest.mark.parametrize("fmt,mode", [(fp8.E4M3, fp8.SCALE_FP32), (fp8.E5M2, fp8.SCALE_POW2)])
+def test_quantize_linear_equals_the_two_quantizers(M, N, K, fmt, mode):
+    """One launch for a linear's X (1x128) and W (128x128): bit-exact with the
+    oracle (ragged rows of both, full Llama-3.1-8B QKV size, empty operands)."""
+    import torch
+    x = inputs.activations(M, K, seed=M + 1)
+    w = inputs.gaussian((N, K), 0.02, seed=N + 2)
+    qx, sx, qw, sw = fp8.fp8_quantize_linear(dev_bf16(x) if M else torch.empty((0, K), dtype=torch.bfloat16,
+                                                                               device="cuda"),
+                                             dev_bf16(w) if N else torch.empty((0, K), dtype=torch.bfloat16,
+                                                                               device="cuda"), fmt, mode)
+    if M:
+        rq, rs = orc.quantize_1x128(x, fmt, mode)
+        assert np.array_equal(host(qx), rq) and np.array_equal(f32_bits(host(sx)), f32_bits(rs))
+    if N:
+        rq, rs = orc.quantize_128x128(w, fmt, mode)
+        assert np.array_equal(host(qw), rq) and np.array_equal(f32_bits(host(sw)), f32_bits(rs))

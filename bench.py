@@ -241,7 +241,7 @@ class Fprop:
                            M * it["K"] * 3 + 4 * M * (it["K"] // 128) + it["N"] * it["K"] * 3
                            + 4 * ((it["N"] + 127) // 128) * (it["K"] // 128)) for it in self.items]
         self.flops = sum(u[1] for u in self.units)
-        self.launches = (3 if self.mx else 2) * len(self.items)
+        self.launches = 3 * len(self.items)   # X and W quantization, GEMM
         self.config = self.static_config(cfg, only)
 
     @staticmethod
@@ -459,7 +459,7 @@ class MoE:
         self.units = [(it["name"], 2.0 * T * it["N"] * it["K"],
                        3 * T * it["K"] + 3 * G * it["N"] * it["K"]) for it in self.items]
         self.flops = sum(u[1] for u in self.units)
-        self.launches = 2 * len(self.items)
+        self.launches = 3 * len(self.items)
         self.config = {"workload": cfg["name"] + (f" ({only} only)" if only else ""), "rows": T,
                        "experts": G, "max_rows": int(loads.max()), "min_rows": int(loads.min()),
                        "linears": [[it["name"], it["N"], it["K"]] for it in self.items],

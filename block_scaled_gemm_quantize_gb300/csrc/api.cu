@@ -278,6 +278,18 @@ int run_gemm(const char* fn, int32_t G, const int32_t* offsets, int64_t a_rows, 
     if (sms <= 0) return fail(FP8BS_ERR_CUDA, "%s: cannot query the device", fn);
     const int grid = static_cast<int>(tiles < sms ? tiles : sms);
     if (grid <= 0) return FP8BS_OK;
+    // (1x128 A scales reach the MX kernel by TMA: a row pitch of 16 bytes
+    // needed.)  Only block-scaled operands go there: a per-tensor scale
+    // (delayed scaling) is in general not a power of two, so those products
+    // keep the promotion kernel.
+    const bool sa_tma_ok = A->gran != FP8BS_GRAN_1x128 || (a_rows % 4 == 0 && aligned16(A->scales));
+    const bool blocks_only = A->gran != FP8BS_GRAN_TENSOR && B->gran != FP8BS_GRAN_TENSOR;
+#ifndef FP8BS_NO_MX
+    const bool use_mx = mx32 || (mode == FP8BS_SCALE_POW2 && !a_mn && !b_mn && !grouped && sa_tma_ok &&
+                                 blocks_only && B->gran != FP8BS_GRAN_1x128);
+#else
+    const bool use_mx = mx32;
+#endif
     // Power-of-two scales on K-major operands go to the block-scaled (MX)
     // kernel: the tensor core applies the UE8M0 scales, no promotion.
     cudaError_t e;
@@ -288,23 +300,16 @@ int run_gemm(const char* fn, int32_t G, const int32_t* offsets, int64_t a_rows, 
         e = fp8bs::launch_fp8_gemm_mx(tmA, tmB, tmY, tmSA, p, grid, stream);
         return e == cudaSuccess ? FP8BS_OK : cuda_fail(e, fn);
     }
-#ifndef FP8BS_NO_MX
-    // (1x128 A scales reach the kernel by TMA: a row pitch of 16 bytes needed).
-    // Only block-scaled operands: a per-tensor scale (delayed scaling) is in
-    // general not a power of two, so those products keep the promotion kernel.
-    const bool sa_tma_ok = A->gran != FP8BS_GRAN_1x128 || (a_rows % 4 == 0 && aligned16(A->scales));
-    const bool blocks_only = A->gran != FP8BS_GRAN_TENSOR && B->gran != FP8BS_GRAN_TENSOR;
-    if (mode == FP8BS_SCALE_POW2 && !a_mn && !b_mn && !grouped && sa_tma_ok && blocks_only &&
-        B->gran != FP8BS_GRAN_1x128) {
+    if (use_mx) {
         CUtensorMap tmSA;
         memset(&tmSA, 0, sizeof(tmSA));
         if (A->gran == FP8BS_GRAN_1x128 && (rc = make_scale_map(&tmSA, A->scales, a_rows, K / 128)) != FP8BS_OK)
             return rc;
         p.idesc = fp8bs::make_idesc_mx(A->fmt, B->fmt, BN);
         e = fp8bs::launch_fp8_gemm_mx(tmA, tmB, tmY, tmSA, p, grid, stream);
-    } else
-#endif
+    } else {
         e = fp8bs::launch_fp8_gemm(tmA, tmB, tmY, p, a_mn, b_mn, grid, stream);
+    }
     return e == cudaSuccess ? FP8BS_OK : cuda_fail(e, fn);
 }
 

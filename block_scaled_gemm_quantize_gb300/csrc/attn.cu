@@ -475,6 +475,393 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
     }
 }
 
+
+// ================================================================ two tiles
+// Version 2: a CTA takes TWO 128-query tiles (A: rows q0.., B: rows
+// q0 + 128..) of one head, which share every K/V tile, and keeps each
+// tile's O accumulating in tensor memory:
+//   TMEM columns   S_A 0-127, S_B 128-255, O_A 256-383, O_B 384-511.
+//   warp 0         TMA: Q_A and Q_B once, K/V 128-key tiles into 3 stages.
+//   warp 1         MMA: S_X(j) = Q_X K_j^T as soon as tile X's softmax has
+//                  read S_X(j-1); O_X += P_X(j) V_j once P_X(j) is written and
+//                  O_X has been rescaled for tile j.  A and B alternate, so the
+//                  tensor core works on one tile while the other is in softmax.
+//   warps 4-7      softmax of tile A, warps 8-11 of tile B: one thread per
+//                  query row holds the row's 128 scores (no exchange between
+//                  threads), the row max (reduced by the TMEM loads on fully
+//                  visible tiles), exp2, the row sum and the E4M3 codes of
+//                  448 P into a double-buffered, 128-byte-swizzled P buffer.
+//   warps 12-15    O correction, one thread per row of both tiles: before
+//                  O_X(j) accumulates, O_X *= alpha_j sv_{j-1} / sv_j (running-max
+//                  factor and the V tile scales: O_X then holds the sum scaled
+//                  by 1 / sv_j), read from and written back to TMEM; at the end
+//                  O = O_X sv_last / l in bf16.
+constexpr int A2_THREADS = 512;
+constexpr uint32_t A2_Q_OFF = 0;                                  // Q_A, Q_B
+constexpr uint32_t A2_KV_OFF = 2 * AT_TILE;                       // stage s: K +0, V +16 KiB
+constexpr uint32_t A2_P_OFF = A2_KV_OFF + AT_STAGES * 2 * AT_TILE;  // P[X][b]
+constexpr uint32_t A2_BAR_OFF = A2_P_OFF + 4 * AT_TILE;
+// q_full, kv_full[3], kv_empty[3], s_full[2], s_empty[2], p_full[2][2],
+// p_empty[2][2], o_done[2], corr_done[2], a_full[2][4], l_full[2], done
+constexpr int A2_NUM_BARS = 1 + 2 * AT_STAGES + 2 + 2 + 4 + 4 + 2 + 2 + 8 + 2 + 1;
+constexpr uint32_t A2_TMEMSLOT_OFF = A2_BAR_OFF + A2_NUM_BARS * 8;
+constexpr uint32_t A2_ALPHA_OFF = (A2_TMEMSLOT_OFF + 16 + 15) & ~15u;   // [X][4][128] fp32
+constexpr uint32_t A2_L_OFF = A2_ALPHA_OFF + 2 * 4 * 128 * 4;           // [X][128] fp32
+constexpr uint32_t A2_SMEM_BYTES = 1024 + A2_L_OFF + 2 * 128 * 4;
+static_assert(A2_SMEM_BYTES <= 232448, "shared memory budget (attention, two tiles)");
+// registers: 128 / thread at launch; control warps 48 and correction warps
+// 96 (both decreases), softmax 184 (an increase, 128 scores per row):
+// 128 * 48 + 256 * 184 + 128 * 96 == 512 * 128
+constexpr int A2_REGS_LOW = 48, A2_REGS_SM = 184, A2_REGS_CO = 96;
+static_assert(128 * A2_REGS_LOW + 256 * A2_REGS_SM + 128 * A2_REGS_CO == 512 * 128, "register split");
+static_assert(A2_REGS_LOW <= 128 && A2_REGS_CO <= 128 && A2_REGS_SM >= 128, "setmaxnreg directions");
+
+__global__ void __launch_bounds__(A2_THREADS, 1)
+    k_fp8_attn_fwd2(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                    const __grid_constant__ CUtensorMap tmV, const AttnParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    uint8_t* smem = smem_raw + ((1024u - (raw & 1023u)) & 1023u);
+    const uint32_t sbase = smem_u32(smem);
+    const uint32_t bars = sbase + A2_BAR_OFF;
+    const uint32_t q_full = bars;
+    auto kv_full = [&](int s) { return bars + 8u * (1 + s); };
+    auto kv_empty = [&](int s) { return bars + 8u * (1 + AT_STAGES + s); };
+    constexpr int B0 = 1 + 2 * AT_STAGES;
+    auto s_full = [&](int x) { return bars + 8u * (B0 + x); };
+    auto s_empty = [&](int x) { return bars + 8u * (B0 + 2 + x); };
+    auto p_full = [&](int x, int b) { return bars + 8u * (B0 + 4 + 2 * x + b); };
+    auto p_empty = [&](int x, int b) { return bars + 8u * (B0 + 8 + 2 * x + b); };
+    auto o_done = [&](int x) { return bars + 8u * (B0 + 12 + x); };
+    auto corr_done = [&](int x) { return bars + 8u * (B0 + 14 + x); };
+    auto a_full = [&](int x, int k) { return bars + 8u * (B0 + 16 + 4 * x + k); };
+    auto l_full = [&](int x) { return bars + 8u * (B0 + 24 + x); };
+    const uint32_t done_bar = bars + 8u * (B0 + 26);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + A2_TMEMSLOT_OFF);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int h = blockIdx.y;
+    const int g = h / (p.hq / p.hkv);
+    // causal: the last query tiles see the most keys, so they start first
+    const int64_t q0 = static_cast<int64_t>(p.causal ? gridDim.x - 1 - blockIdx.x : blockIdx.x) * (2 * AT_ROWS);
+    const int nA = q0 < p.seq_q ? kv_tiles(p, q0) : 0;
+    const int nB = q0 + AT_ROWS < p.seq_q ? kv_tiles(p, q0 + AT_ROWS) : 0;
+    const int n = max(nA, nB);
+
+    if (warp == 0 && lane == 0) {
+        tma_prefetch_desc(&tmQ);
+        tma_prefetch_desc(&tmK);
+        tma_prefetch_desc(&tmV);
+        mbar_init(q_full, 1);
+        for (int s = 0; s < AT_STAGES; s++) {
+            mbar_init(kv_full(s), 1);
+            mbar_init(kv_empty(s), 1);
+        }
+        for (int x = 0; x < 2; x++) {
+            mbar_init(s_full(x), 1);
+            mbar_init(s_empty(x), 4);            // the tile's four softmax warps
+            for (int b = 0; b < 2; b++) {
+                mbar_init(p_full(x, b), 4);
+                mbar_init(p_empty(x, b), 1);
+            }
+            mbar_init(o_done(x), 1);
+            mbar_init(corr_done(x), 4);          // the four correction warps
+            for (int k = 0; k < 4; k++) mbar_init(a_full(x, k), 4);
+            mbar_init(l_full(x), 4);
+        }
+        mbar_init(done_bar, 1);
+        fence_mbar_init();
+        fence_proxy_async_smem();
+    }
+    if (warp == 1) tmem_alloc(smem_u32(tmem_slot), 512);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp < 4) {
+        asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(A2_REGS_LOW));
+        if (warp == 0 && lane == 0 && n > 0) {
+            // ---------------------------------------------------------- TMA
+            bool ok = true;
+            int issued = 0;
+            mbar_arrive_expect_tx(q_full, 2 * AT_TILE);
+            tma_load_2d(sbase + A2_Q_OFF, &tmQ, h * AT_D, static_cast<int32_t>(q0), q_full);
+            tma_load_2d(sbase + A2_Q_OFF + AT_TILE, &tmQ, h * AT_D, static_cast<int32_t>(q0 + AT_ROWS), q_full);
+            for (int j = 0; j < n; j++) {
+                const int s = j % AT_STAGES;
+                if (!at_wait(kv_empty(s), ((j / AT_STAGES) & 1u) ^ 1u)) { ok = false; break; }
+                const uint32_t dst = sbase + A2_KV_OFF + s * 2 * AT_TILE;
+                mbar_arrive_expect_tx(kv_full(s), 2 * AT_TILE);
+                tma_load_2d(dst, &tmK, g * AT_D, j * AT_KEYS, kv_full(s));
+                tma_load_2d(dst + AT_TILE, &tmV, g * AT_D, j * AT_KEYS, kv_full(s));
+                issued++;
+            }
+            at_drain(q_full, 0);
+            if (!ok) {
+                for (int i = 0; i < AT_STAGES && i < issued; i++) {
+                    const int j = issued - 1 - i;
+                    at_drain(kv_full(j % AT_STAGES), (j / AT_STAGES) & 1u);
+                }
+            }
+        } else if (warp == 1 && lane == 0 && n > 0) {
+            // ---------------------------------------------------------- MMA
+            bool ok = at_wait(q_full, 0), issued_mma = false;
+            auto issue_s = [&](int x, int j) -> bool {
+                const int s = j % AT_STAGES;
+                if (!at_wait(kv_full(s), (j / AT_STAGES) & 1u)) return false;
+                if (j > 0 && !at_wait(s_empty(x), (j - 1) & 1u)) return false;   // S_X(j-1) was read
+                tc_fence_after();
+                const uint32_t kS = sbase + A2_KV_OFF + s * 2 * AT_TILE;
+                const uint32_t qS = sbase + A2_Q_OFF + x * AT_TILE;
+#pragma unroll
+                for (int k4 = 0; k4 < AT_D / 32; k4++)
+                    mma_f8f6f4(tmem + x * 128, smem_desc_sw128(qS + k4 * 32, 16, 1024),
+                               smem_desc_sw128(kS + k4 * 32, 16, 1024), p.idesc_s, k4 > 0 ? 1u : 0u);
+                issued_mma = true;
+                mma_commit(s_full(x));
+                return true;
+            };
+            auto issue_o = [&](int x, int j) -> bool {
+                const int s = j % AT_STAGES, b = j & 1;
+                if (!at_wait(p_full(x, b), (j >> 1) & 1u)) return false;
+                if (!at_wait(corr_done(x), j & 1u)) return false;                 // O_X rescaled for j
+                tc_fence_after();
+                const uint32_t vS = sbase + A2_KV_OFF + s * 2 * AT_TILE + AT_TILE;
+                const uint32_t pS = sbase + A2_P_OFF + (2 * x + b) * AT_TILE;
+#pragma unroll
+                for (int k4 = 0; k4 < AT_KEYS / 32; k4++)
+                    // P: K-major (keys contiguous in a row); V: MN-major, one
+                    // 128-wide atom, 32 keys x 128 B further per K step
+                    mma_f8f6f4(tmem + 256 + x * 128, smem_desc_sw128(pS + k4 * 32, 16, 1024),
+                               smem_desc_sw128(vS + k4 * 4096, 1024, 1024), p.idesc_o,
+                               (j > 0 || k4 > 0) ? 1u : 0u);
+                mma_commit(o_done(x));
+                mma_commit(p_empty(x, b));
+                return true;
+            };
+            if (ok && nA > 0) ok = issue_s(0, 0);
+            if (ok && nB > 0) ok = issue_s(1, 0);
+            for (int j = 0; ok && j < n; j++) {
+                if (j + 1 < nA && !issue_s(0, j + 1)) { ok = false; break; }
+                if (j < nA && !issue_o(0, j)) { ok = false; break; }
+                if (j + 1 < nB && !issue_s(1, j + 1)) { ok = false; break; }
+                if (j < nB && !issue_o(1, j)) { ok = false; break; }
+                mma_commit(kv_empty(j % AT_STAGES));
+            }
+            if (!ok && issued_mma) {
+                mma_commit(done_bar);
+                at_drain(done_bar, 0);
+            }
+        }
+    } else if (warp < 12) {
+        asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(A2_REGS_SM));
+        // -------------------------------------------------------- softmax
+        const int x = (warp - 4) >> 2;                  // query tile
+        const int quarter = warp & 3;
+        const int r = quarter * 32 + lane;              // TMEM lane = query row in the tile
+        const int64_t tq0 = q0 + x * AT_ROWS;
+        const int64_t row = tq0 + r;
+        const bool row_ok = row < p.seq_q;
+        const int64_t crow = row_ok ? row : p.seq_q - 1;
+        const int nx = x ? nB : nA;
+        const int64_t offs = p.seq_k - p.seq_q;
+        const int64_t last_key = p.causal ? min(crow + offs, p.seq_k - 1) : p.seq_k - 1;
+        // keys every row of this tile sees: a K/V tile below this needs no mask
+        const int64_t all_vis = p.causal ? min(tq0 + offs, p.seq_k - 1) : p.seq_k - 1;
+        const float qs = nx > 0 ? __ldg(p.sq + static_cast<int64_t>(h) * p.seq_q + crow) : 0.0f;
+        const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
+        float m = -INFINITY, l = 0.0f;   // l: the row's sum of 448 P
+        bool ok = true;
+        auto ksc = [&](int t) { return t < nx ? __ldg(p.sk + static_cast<int64_t>(t) * p.hkv + g) : 0.0f; };
+        float skw = 0.0f;   // K tile scales: lane i holds tile 32 w + i of window w
+        for (int j = 0; ok && j < nx; j++) {
+            const int b = j & 1;
+            if ((j & 31) == 0) skw = ksc(j + lane);
+            const float sk_j = __shfl_sync(0xFFFFFFFFu, skw, j & 31);
+            ok = __all_sync(0xFFFFFFFFu, at_wait(s_full(x), j & 1u));
+            if (!ok) break;
+            tc_fence_after();
+            const bool full = static_cast<int64_t>(j) * AT_KEYS + AT_KEYS - 1 <= all_vis;   // tile-uniform
+            uint32_t sr[4][32];
+            float lm[4];
+            if (full) {
+#pragma unroll
+                for (int u = 0; u < 4; u++) tmem_ld_max_32x32b_x32(tmem + lane_off + x * 128 + u * 32, sr[u], lm[u]);
+            } else {
+#pragma unroll
+                for (int u = 0; u < 4; u++) tmem_ld_32x32b_x32(tmem + lane_off + x * 128 + u * 32, sr[u]);
+            }
+            tmem_wait_ld();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(s_empty(x));   // S_X read: the next S_X may be computed
+            const float c = qs * sk_j * p.scale_log2;
+            float tm[4];
+            if (full) {
+#pragma unroll
+                for (int u = 0; u < 4; u++) tm[u] = lm[u];
+            } else {   // keys e <= lim are visible to this row
+                const int lim = static_cast<int>(max(min(last_key - static_cast<int64_t>(j) * AT_KEYS,
+                                                         static_cast<int64_t>(AT_KEYS)), static_cast<int64_t>(-1)));
+#pragma unroll
+                for (int u = 0; u < 4; u++) tm[u] = -INFINITY;
+#pragma unroll
+                for (int e = 0; e < AT_KEYS; e++) {
+                    const float v = e <= lim ? __uint_as_float(sr[e >> 5][e & 31]) : -INFINITY;
+                    sr[e >> 5][e & 31] = __float_as_uint(v);
+                    tm[e >> 5] = fmaxf(tm[e >> 5], v);
+                }
+            }
+            float tmax = fmaxf(fmaxf(tm[0], tm[1]), fmaxf(tm[2], tm[3]));
+            tmax = tmax == -INFINITY ? -INFINITY : tmax * c;
+            const float m_new = fmaxf(m, tmax);
+            const float alpha = m_new == -INFINITY ? 1.0f : ex2(m - m_new);
+            const float shift = AT_LOG2_448 - (m_new == -INFINITY ? 0.0f : m_new);
+            // P_X's buffer b is free once O_X(j - 2) has completed
+            ok = __all_sync(0xFFFFFFFFu, at_wait(p_empty(x, b), ((j >> 1) & 1u) ^ 1u));
+            if (!ok) break;
+            // the running-max factor for the correction warps, slot j % 4 (its
+            // previous value, tile j - 4, was read before O_X(j - 2) was issued)
+            st_shared_f32(sbase + A2_ALPHA_OFF + ((x * 4 + (j & 3)) * 128 + r) * 4, alpha);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(a_full(x, j & 3));
+            // 448 P = 2^(raw c - m_new + log2 448) (masked: 0), row sum, codes
+            const uint32_t prow = sbase + A2_P_OFF + (2 * x + b) * AT_TILE + r * 128;
+            float rs[8];
+#pragma unroll
+            for (int i = 0; i < 8; i++) rs[i] = 0.0f;
+#pragma unroll
+            for (int ch = 0; ch < AT_KEYS / 16; ch++) {          // 16 keys = one 16-byte chunk
+                float pv[16];
+#pragma unroll
+                for (int e = 0; e < 16; e++) {
+                    const int k = ch * 16 + e;
+                    pv[e] = ex2(fmaf(__uint_as_float(sr[k >> 5][k & 31]), c, shift));
+                    rs[e & 7] += pv[e];
+                }
+                uint32_t w[4];
+#pragma unroll
+                for (int i = 0; i < 4; i++) w[i] = cvt4_e4m3(pv[4 * i], pv[4 * i + 1], pv[4 * i + 2], pv[4 * i + 3]);
+                st_shared_v4(prow + ((static_cast<uint32_t>(ch) ^ (static_cast<uint32_t>(r) & 7u)) << 4), w[0], w[1],
+                             w[2], w[3]);
+            }
+            const float rsum = ((rs[0] + rs[1]) + (rs[2] + rs[3])) + ((rs[4] + rs[5]) + (rs[6] + rs[7]));
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(p_full(x, b));
+            l = l * alpha + rsum;
+            m = m_new;
+        }
+        // the row sum for the correction warps (always handed over, so that
+        // they never wait for it in vain; a timeout above is already recorded)
+        st_shared_f32(sbase + A2_L_OFF + (x * 128 + r) * 4, ok ? l : 0.0f);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(l_full(x));
+    } else {
+        // (96 is below the launch's 128: a decrease)
+        asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(A2_REGS_CO));
+        // ------------------------------------------------- O correction
+        const int quarter = warp & 3;
+        const int r = quarter * 32 + lane;
+        const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
+        bool ok = true;
+        auto vsc = [&](int t) { return t < n ? __ldg(p.sv + static_cast<int64_t>(t) * p.hkv + g) : 1.0f; };
+        float svw = 0.0f, sv_prev = 1.0f, sv_j = 1.0f;   // V tile scales (window of 32 across the lanes)
+        for (int j = 0; ok && j < n; j++) {
+            if ((j & 31) == 0) svw = vsc(j + lane);
+            sv_prev = sv_j;
+            sv_j = __shfl_sync(0xFFFFFFFFu, svw, j & 31);
+#pragma unroll
+            for (int x = 0; x < 2; x++) {
+                if (j >= (x ? nB : nA)) continue;
+                ok = __all_sync(0xFFFFFFFFu, at_wait(a_full(x, j & 3), (j >> 2) & 1u));
+                if (!ok) break;
+                const float alpha = ld_shared_f32(sbase + A2_ALPHA_OFF + ((x * 4 + (j & 3)) * 128 + r) * 4);
+                if (j > 0) {
+                    const float f = alpha * __fdiv_rn(sv_prev, sv_j);
+                    ok = __all_sync(0xFFFFFFFFu, at_wait(o_done(x), (j - 1) & 1u));   // O_X(j-1) complete
+                    if (!ok) break;
+                    tc_fence_after();
+                    if (__any_sync(0xFFFFFFFFu, f != 1.0f)) {
+                        const uint64_t f2 = pack_f32x2(__float_as_uint(f), __float_as_uint(f));
+                        const uint32_t ta = tmem + lane_off + 256 + x * 128;
+#pragma unroll
+                        for (int u = 0; u < 4; u++) {
+                            uint32_t rr[32];
+                            tmem_ld_32x32b_x32(ta + u * 32, rr);
+                            tmem_wait_ld();
+#pragma unroll
+                            for (int q = 0; q < 16; q++) {
+                                const uint64_t v = mul_f32x2(pack_f32x2(rr[2 * q], rr[2 * q + 1]), f2);
+                                const float2 fv = unpack_f32x2(v);
+                                rr[2 * q] = __float_as_uint(fv.x);
+                                rr[2 * q + 1] = __float_as_uint(fv.y);
+                            }
+                            tmem_st_32x32b_x32(ta + u * 32, rr);
+                        }
+                        tmem_wait_st();
+                    }
+                    tc_fence_before();
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(corr_done(x));
+            }
+        }
+        // O = O_X sv_last / l, bf16
+#pragma unroll
+        for (int x = 0; x < 2; x++) {
+            const int nx = x ? nB : nA;
+            const int64_t row = q0 + x * AT_ROWS + r;
+            const bool row_ok = row < p.seq_q;
+            float scale = 0.0f;
+            bool have = false;
+            if (ok && nx > 0) {
+                ok = __all_sync(0xFFFFFFFFu, at_wait(o_done(x), (nx - 1) & 1u)) &&
+                     __all_sync(0xFFFFFFFFu, at_wait(l_full(x), 0));
+                if (!ok) break;
+                tc_fence_after();
+                const float l = ld_shared_f32(sbase + A2_L_OFF + (x * 128 + r) * 4);
+                const float sv_last = __ldg(p.sv + static_cast<int64_t>(nx - 1) * p.hkv + g);
+                scale = l > 0.0f ? sv_last / l : 0.0f;
+                have = true;
+            }
+            if (!ok) break;
+            uint16_t* o = reinterpret_cast<uint16_t*>(p.o) + row * p.ldo + static_cast<int64_t>(h) * AT_D;
+#pragma unroll
+            for (int u = 0; u < 4; u++) {
+                uint32_t rr[32];
+                if (have) {
+                    tmem_ld_32x32b_x32(tmem + lane_off + 256 + x * 128 + u * 32, rr);
+                    tmem_wait_ld();
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 32; i++) rr[i] = 0u;
+                }
+                if (row_ok) {
+#pragma unroll
+                    for (int c8 = 0; c8 < 4; c8++) {
+                        uint32_t w[4];
+#pragma unroll
+                        for (int i = 0; i < 4; i++) {
+                            __nv_bfloat162 h2 = __floats2bfloat162_rn(__uint_as_float(rr[c8 * 8 + 2 * i]) * scale,
+                                                                      __uint_as_float(rr[c8 * 8 + 2 * i + 1]) * scale);
+                            w[i] = *reinterpret_cast<uint32_t*>(&h2);
+                        }
+                        *reinterpret_cast<uint4*>(o + u * 32 + c8 * 8) = make_uint4(w[0], w[1], w[2], w[3]);
+                    }
+                }
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, 512);
+    }
+}
+
 }  // namespace
 
 cudaError_t read_and_clear_attn_status(int* status) {
@@ -484,8 +871,21 @@ cudaError_t read_and_clear_attn_status(int* status) {
     return cudaMemcpyToSymbol(g_attn_status, &zero, sizeof(int));
 }
 
+#ifndef FP8BS_ATTN_V2
+#define FP8BS_ATTN_V2 1
+#endif
+
 cudaError_t launch_fp8_attn_fwd(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensorMap& tmV,
                                 const AttnParams& p, cudaStream_t st) {
+    if (FP8BS_ATTN_V2) {
+        auto k = k_fp8_attn_fwd2;
+        cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, A2_SMEM_BYTES);
+        if (e != cudaSuccess) return e;
+        const int64_t qt = (p.seq_q + 2 * AT_ROWS - 1) / (2 * AT_ROWS);
+        k<<<dim3(static_cast<unsigned>(qt), static_cast<unsigned>(p.hq)), A2_THREADS, A2_SMEM_BYTES, st>>>(
+            tmQ, tmK, tmV, p);
+        return cudaGetLastError();
+    }
     auto k = k_fp8_attn_fwd;
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, AT_SMEM_BYTES);
     if (e != cudaSuccess) return e;

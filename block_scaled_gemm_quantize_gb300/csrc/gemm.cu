@@ -59,26 +59,7 @@ constexpr uint32_t B_STAGE = BN * BK;   // 32 KiB
 constexpr uint32_t STAGE_BYTES = A_STAGE + B_STAGE;
 constexpr int NUM_THREADS = 384;
 constexpr int EPI_WARP0 = 4;
-#ifndef FP8BS_REGS_LOW
-#define FP8BS_REGS_LOW 72
-#endif
-// the two epilogue warpgroups share what the first warpgroup gives up:
-// 128 * REGS_LOW + 256 * REGS_HIGH == 384 * 168, the launch allocation
-constexpr int REGS_LOW = FP8BS_REGS_LOW, REGS_HIGH = (384 * 168 - 128 * REGS_LOW) / 256;
-static_assert(REGS_LOW % 8 == 0 && REGS_HIGH % 8 == 0 && 128 * REGS_LOW + 256 * REGS_HIGH == 384 * 168,
-              "register split");
-// Block scales of the promotion staged in shared memory by the otherwise
-// idle warp 2 (no global load in the epilogue's K loop)
-#ifndef FP8BS_SCALES_SMEM
-#define FP8BS_SCALES_SMEM 0
-#endif
-#ifndef FP8BS_EPI_PIPE
-#define FP8BS_EPI_PIPE 0
-#endif
-#ifndef FP8BS_EPI_CW
-#define FP8BS_EPI_CW 16
-#endif
-constexpr int CW = FP8BS_EPI_CW;             // columns per pipelined TMEM load
+constexpr int REGS_LOW = 72, REGS_HIGH = 216;   // 128*72 + 256*216 == 384*168
 constexpr int NUM_EPI_WARPS = 8;
 constexpr uint32_t TMEM_COLS = 512;
 #ifndef FP8BS_RASTER_M
@@ -201,23 +182,6 @@ __device__ __forceinline__ Tile decode_tile(int t, int total_slots, int tiles_n,
 
 __device__ __forceinline__ float ld_scale(const float* p) { return __ldg(p); }
 
-// acc[a0 .. a0 + CW/2) += r (CW fp32, as pairs) * s2, as volatile packed
-// FMAs so that they stay between the TMEM load they overlap and its wait.
-template <int CW>
-__device__ __forceinline__ void fma_cw_v(uint64_t (&acc)[64], int a0, const uint32_t (&r)[CW], uint64_t s2) {
-#pragma unroll
-    for (int q = 0; q < CW / 2; q++)
-        asm volatile("fma.rn.f32x2 %0, %1, %2, %0;"
-                     : "+l"(acc[a0 + q])
-                     : "l"(pack_f32x2(r[2 * q], r[2 * q + 1])), "l"(s2));
-}
-
-template <int CW>
-__device__ __forceinline__ void tmem_ld_cw(uint32_t taddr, uint32_t (&r)[CW]) {
-    if constexpr (CW == 32) tmem_ld_32x32b_x32(taddr, r);
-    else tmem_ld_32x32b_x16(taddr, r);
-}
-
 // Store one warp's 32 rows x 128 columns of a finished tile (acc = 128 fp32
 // as packed pairs): TMA bulk stores of 32 x 64-byte boxes staged in the warp's
 // `subs` 2 KiB sub-slabs when the warp's 32 rows all belong to the tile's
@@ -227,7 +191,37 @@ __device__ __forceinline__ void store_tile(const GemmParams& p, const CUtensorMa
                                            bool row_ok, int64_t col0, int quarter, int lane,
                                            uint32_t slab, int subs) {
     const int64_t wrow0 = static_cast<int64_t>(tl.row0) + quarter * 32;
-    if (p.tma_store && (p.offsets == nullptr || wrow0 + 32 <= tl.row_end)) {
+    if (p.tma_store && (p.offsets == nullptr || wrow0 + 32 <= tl.row_end) && p.out_bf16 && subs == 4) {
+        // bf16 with four sub-slabs: the whole 32 x 128 block at once -- the
+        // four slabs written, one proxy fence, four stores issued together
+        const uint32_t sw = (lane >> 1) & 3;          // 64-B swizzle: chunk ^= (row/2)%4
+        if (lane == 0) bulk_wait_group_read0();       // this warp's earlier stores have read their slabs
+        __syncwarp();
+#pragma unroll
+        for (int ps = 0; ps < 4; ps++) {
+            const uint32_t rbase = slab + static_cast<uint32_t>(ps) * OUT_SUB + lane * 64;
+#pragma unroll
+            for (int c = 0; c < 4; c++) {
+                uint32_t w[4];
+#pragma unroll
+                for (int i = 0; i < 4; i++) {
+                    const float2 f = unpack_f32x2(acc[ps * 16 + c * 4 + i]);
+                    __nv_bfloat162 h = __floats2bfloat162_rn(f.x, f.y);
+                    w[i] = *reinterpret_cast<uint32_t*>(&h);
+                }
+                st_shared_v4(rbase + ((c ^ sw) << 4), w[0], w[1], w[2], w[3]);
+            }
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+#pragma unroll
+            for (int ps = 0; ps < 4; ps++)
+                tma_store_2d(&tmY, slab + static_cast<uint32_t>(ps) * OUT_SUB, static_cast<int32_t>(col0 + ps * 32),
+                             static_cast<int32_t>(wrow0));
+            bulk_commit_group();
+        }
+    } else if (p.tma_store && (p.offsets == nullptr || wrow0 + 32 <= tl.row_end)) {
         const uint32_t sw = (lane >> 1) & 3;          // 64-B swizzle: chunk ^= (row/2)%4
         const int passes = p.out_bf16 ? 4 : 8;        // 32 bf16 or 16 fp32 columns each
 #pragma unroll
@@ -657,71 +651,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 }
             }
         }
-#if FP8BS_SCALES_SMEM
-      } else if (!B_COL && warp == 2) {
-        // ------------------------------------------- block-scale loader
-        // Per promotion group (P K blocks) of every tile, the 128 row scales
-        // of A and the column-block scales of B into a shared-memory ring
-        // slot: sa[row] at 4 row, sb[half] at 512 + 4 half, the up-rows'
-        // sb[half] at 520 + 4 half (SwiGLU).  The epilogue then issues no
-        // global load in its K loop.  Global loads of group i + 1 are in
-        // flight while group i waits for its slot.
-        const int ngroups = (nkb + P - 1) / P;
-        const int64_t nkb64 = nkb;
-        auto fetch = [&](int t, int g, float (&va)[4], float& vb) {
-            const Tile tl = decode_tile(t, total_slots, p.tiles_n, G, s_slot, s_off);
-            const int64_t kb = static_cast<int64_t>(g) * P;
-#pragma unroll
-            for (int i = 0; i < 4; i++) {
-                int64_t srow = static_cast<int64_t>(tl.row0) + 4 * lane + i;
-                srow = srow < p.a_rows ? srow : p.a_rows - 1;
-                const float* pa;
-                if (p.a_gran == 0) pa = p.sa + kb * p.a_rows + srow;
-                else if (p.a_gran == 1) pa = A_MN ? p.sa + kb * p.a_rblocks + srow / 128
-                                                  : p.sa + (srow / 128) * nkb64 + kb;
-                else pa = p.sa;
-                va[i] = ld_scale(pa);
-            }
-            vb = 0.0f;
-            if (lane < 4) {   // lanes 0, 1: sb of halves 0, 1; lanes 2, 3: the up rows' (SwiGLU)
-                const int half = lane & 1;
-                const int64_t col0 = static_cast<int64_t>(tl.nt) * BN + half * 128;
-                int64_t nb = SWIGLU ? (lane < 2 ? static_cast<int64_t>(tl.nt) : p.swiglu_i / 128 + tl.nt)
-                                    : min(col0, p.N - 1) / 128;
-                const float* pb;
-                if (p.b_gran == 1) pb = B_MN ? p.sb + kb * p.b_rblocks + nb
-                                             : p.sb + tl.g * p.b_scale_group_stride + nb * nkb64 + kb;
-                else pb = p.sb;
-                vb = ld_scale(pb);
-            }
-        };
-        int slot = 0;
-        uint32_t ph = 0;
-        bool ok = true;
-        int t = blockIdx.x, g = 0;
-        float va[4], vb;
-        if (t < total_tiles) fetch(t, g, va, vb);
-        while (ok && t < total_tiles) {
-            int tn = t, gn = g + 1;
-            if (gn == ngroups) { gn = 0; tn += gridDim.x; }
-            float na[4], nb2 = 0.0f;
-            if (tn < total_tiles) fetch(tn, gn, na, nb2);
-            ok = __all_sync(0xFFFFFFFFu, wait_or_flag(bsf_empty(slot), ph ^ 1u));
-            if (!ok) break;
-            const uint32_t dst = sbase + L::kBsfOff + slot * BSF_SLOT_BYTES;
-            st_shared_v4(dst + lane * 16, __float_as_uint(va[0]), __float_as_uint(va[1]),
-                         __float_as_uint(va[2]), __float_as_uint(va[3]));
-            if (lane < 4) st_shared_f32(dst + 512 + lane * 4, vb);
-            __syncwarp();
-            if (lane == 0) mbar_arrive(bsf_full(slot));
-            if (++slot == BSF_SLOTS) { slot = 0; ph ^= 1u; }
-#pragma unroll
-            for (int i = 0; i < 4; i++) va[i] = na[i];
-            vb = nb2;
-            t = tn;
-            g = gn;
-        }
-#endif
       }
     } else if (B_COL) {
         asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(REGS_HIGH));
@@ -822,10 +751,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         uint32_t chunk = 0, tile_i = 0;
         bool ok = true;
         const int64_t nkb64 = nkb;
-#if FP8BS_SCALES_SMEM
-        int sslot = 0;        // scale ring slot (the loader warp's order)
-        uint32_t sph = 0;
-#endif
         for (int t = blockIdx.x; ok && t < total_tiles; t += gridDim.x, tile_i++) {
             const Tile tl = decode_tile(t, total_slots, p.tiles_n, G, s_slot, s_off);
             const int64_t row = static_cast<int64_t>(tl.row0) + lrow;
@@ -859,50 +784,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             uint64_t acc[64];   // 128 fp32 accumulators as packed pairs
 #pragma unroll
             for (int i = 0; i < 64; i++) acc[i] = 0;
-#if FP8BS_SCALES_SMEM
-            (void)pa; (void)pb; (void)pbu; (void)sa_step; (void)sb_step;
-            if (H == 1) {
-                const int ngroups = (nkb + P - 1) / P;
-                for (int g = 0; ok && g < ngroups; g++) {
-                    // this group's two scales from the loader's ring slot
-                    ok = __all_sync(0xFFFFFFFFu, wait_or_flag(bsf_full(sslot), sph));
-                    if (!ok) break;
-                    const uint32_t src = sbase + L::kBsfOff + sslot * BSF_SLOT_BYTES;
-                    const float sa = ld_shared_f32(src + lrow * 4);
-                    const float sb = ld_shared_f32(src + 512 + half * 4);
-                    const float sbu = SWIGLU ? ld_shared_f32(src + 520 + half * 4) : sb;
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(bsf_empty(sslot));
-                    if (++sslot == BSF_SLOTS) { sslot = 0; sph ^= 1u; }
-                    const float s = sa * sb;
-                    const uint64_t s2 = pack_f32x2(__float_as_uint(s), __float_as_uint(s));
-                    const float su = sa * sbu;
-                    const uint64_t s2u = pack_f32x2(__float_as_uint(su), __float_as_uint(su));
-                    const uint32_t buf = chunk % TBUFS;
-                    ok = __all_sync(0xFFFFFFFFu, wait_or_flag(tfull_bar(buf), (chunk / TBUFS) & 1u));
-                    if (!ok) break;
-                    tc_fence_after();
-                    const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
-                                           buf * MMA_N + half * 128;
-#pragma unroll
-                    for (int j = 0; j < 4; j++) {
-                        uint32_t r[32];
-                        tmem_ld_32x32b_x32(taddr + j * 32, r);
-                        tmem_wait_ld();
-                        if (j == 3) {
-                            tc_fence_before();
-                            __syncwarp();
-                            if (lane == 0) mbar_arrive(tempty_bar(buf));
-                        }
-#pragma unroll
-                        for (int q = 0; q < 16; q++)
-                            fma_f32x2(acc[j * 16 + q], pack_f32x2(r[2 * q], r[2 * q + 1]), j < 2 ? s2 : s2u);
-                    }
-                    chunk++;
-                }
-            } else
-#endif
-            {
             // Scales: a ring of SPF register slots, slot i holding chunk
             // (kb0 + i); the K-block loop is unrolled by SPF so each slot is
             // refilled (SPF chunks ahead) right after use, with no register
@@ -915,76 +796,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 sb_r[i] = ld_scale(pb + kbi * sb_step);
                 sbu_r[i] = SWIGLU ? ld_scale(pbu + kbi * sb_step) : sb_r[i];
             }
-#if FP8BS_EPI_PIPE
-            if (H == 1) {
-                // Software-pipelined promotion: the TMEM load of the next CW
-                // columns (across K blocks too) is in flight while the FMAs of
-                // the current CW issue; R[0] / R[1] alternate.  A buffer goes
-                // back to the MMA once its last load has completed.
-                constexpr int NCH = 128 / CW;
-                const int ngroups = (nkb + P - 1) / P;
-                const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
-                uint32_t R[2][CW];
-                {
-                    const uint32_t buf = chunk % TBUFS;
-                    ok = __all_sync(0xFFFFFFFFu, wait_or_flag(tfull_bar(buf), (chunk / TBUFS) & 1u));
-                    if (ok) {
-                        tc_fence_after();
-                        tmem_ld_cw<CW>(tmem_base + lane_off + buf * MMA_N + half * 128, R[0]);
-                        tmem_wait_ld();
-                    }
-                }
-                for (int g0 = 0; ok && g0 < ngroups; g0 += SPF) {
-#pragma unroll
-                    for (int i = 0; i < SPF; i++) {
-                        const int g = g0 + i;
-                        if (g >= ngroups) break;
-                        const int kb = g * P;
-                        const float s = sa_r[i] * sb_r[i];
-                        const uint64_t s2 = pack_f32x2(__float_as_uint(s), __float_as_uint(s));
-                        const float su = sa_r[i] * sbu_r[i];
-                        const uint64_t s2u = pack_f32x2(__float_as_uint(su), __float_as_uint(su));
-                        if (kb + SPF * P < nkb) {
-                            sa_r[i] = ld_scale(pa + (kb + SPF * P) * sa_step);
-                            sb_r[i] = ld_scale(pb + (kb + SPF * P) * sb_step);
-                            sbu_r[i] = SWIGLU ? ld_scale(pbu + (kb + SPF * P) * sb_step) : sb_r[i];
-                        }
-                        const uint32_t buf = chunk % TBUFS;
-                        const uint32_t ta = tmem_base + lane_off + buf * MMA_N + half * 128;
-                        const bool more = g + 1 < ngroups;
-#pragma unroll
-                        for (int c = 0; c < NCH; c++) {
-                            bool issued = true;
-                            if (c + 1 < NCH) {
-                                tmem_ld_cw<CW>(ta + (c + 1) * CW, R[(c + 1) & 1]);
-                            } else {
-                                // every load of this buffer has completed: hand it back,
-                                // then start on the next K block's buffer
-                                tc_fence_before();
-                                __syncwarp();
-                                if (lane == 0) mbar_arrive(tempty_bar(buf));
-                                chunk++;
-                                issued = false;
-                                if (more) {
-                                    const uint32_t nbuf = chunk % TBUFS;
-                                    ok = __all_sync(0xFFFFFFFFu,
-                                                    wait_or_flag(tfull_bar(nbuf), (chunk / TBUFS) & 1u));
-                                    if (ok) {
-                                        tc_fence_after();
-                                        tmem_ld_cw<CW>(tmem_base + lane_off + nbuf * MMA_N + half * 128,
-                                                       R[(c + 1) & 1]);
-                                        issued = true;
-                                    }
-                                }
-                            }
-                            fma_cw_v<CW>(acc, c * (CW / 2), R[c & 1], c * CW < 64 ? s2 : s2u);
-                            if (issued) tmem_wait_ld();
-                        }
-                        if (!ok) break;
-                    }
-                }
-            } else
-#endif
             for (int kb0 = 0; ok && kb0 < nkb; kb0 += SPF * P) {
 #pragma unroll
                 for (int i = 0; i < SPF; i++) {
@@ -1037,7 +848,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     }
                     chunk++;
                 }
-            }
             }
             if (!ok) break;
             ok = finish_tile<SWIGLU>(p, tmY, acc, tl, row, row_ok, col0, quarter, half, lane,

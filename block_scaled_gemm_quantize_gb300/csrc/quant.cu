@@ -106,10 +106,23 @@ __device__ __forceinline__ void quant_1x128_block(const uint16_t* __restrict__ x
     }
 }
 
+// A kernel launched after this one with programmatic stream serialization
+// (the weight half of fp8_quantize_linear) may start as soon as every CTA
+// of this grid has started; for any other launch the trigger has no effect.
+__device__ __forceinline__ void allow_dependent_launch() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+// Wait until the grid this one depends on programmatically has completed and
+// its memory operations are visible (returns at once for a normal launch).
+__device__ __forceinline__ void wait_prerequisite_grid() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
 template <int FMT, int MODE, int U>
 __global__ void __launch_bounds__(256) k_quant_1x128(const uint16_t* __restrict__ x, int64_t rows,
                                                     int64_t ldx, int64_t nkb, uint8_t* __restrict__ q,
                                                     int64_t ldq, float* __restrict__ scales) {
+    allow_dependent_launch();
     quant_1x128_block<FMT, MODE, U>(x, rows, ldx, nkb, q, ldq, scales, blockIdx.x, blockIdx.y);
 }
 
@@ -166,35 +179,18 @@ __device__ __forceinline__ void quant_128x128_tile(const uint16_t* __restrict__ 
     if (threadIdx.x == 0) scales[rb * nkb + kb] = s;
 }
 
-template <int FMT, int MODE>
+// JOIN: launched as the programmatic dependent of the 1x128 kernel of the
+// same linear layer (independent data): it runs alongside that grid's last
+// wave and waits for it only before exiting, so that its own completion
+// still implies the other grid's for the work queued after it.
+template <int FMT, int MODE, bool JOIN>
 __global__ void __launch_bounds__(256, FP8BS_Q128_MINB) k_quant_128x128(const uint16_t* __restrict__ w, int64_t rows,
                                                       int64_t ldw, int64_t nkb,
                                                       uint8_t* __restrict__ q, int64_t ldq,
                                                       float* __restrict__ scales) {
     __shared__ float red[8];
     quant_128x128_tile<FMT, MODE>(w, rows, ldw, nkb, q, ldq, scales, blockIdx.x, red);
-}
-
-// ------------------------------------------------- one linear's two operands
-// X per 1x128 tile and W per 128x128 tile in one launch: the first nx_blocks
-// CTAs run the 1x128 work (a CTA = 16 rows x U K blocks), the rest one
-// 128x128 tile each.  One launch, one ramp and one tail instead of two.
-struct LinearQuantArgs {
-    const uint16_t* x; int64_t m, ldx; uint8_t* qx; int64_t ldqx; float* sx;
-    const uint16_t* w; int64_t n, ldw; uint8_t* qw; int64_t ldqw; float* sw;
-    int64_t nkb, gy, nx_blocks;
-};
-
-template <int FMT, int MODE, int U>
-__global__ void __launch_bounds__(256, FP8BS_Q128_MINB) k_quant_linear(const LinearQuantArgs a) {
-    __shared__ float red[8];
-    const int64_t b = blockIdx.x;
-    if (b < a.nx_blocks) {
-        const int64_t bx = b / a.gy;
-        quant_1x128_block<FMT, MODE, U>(a.x, a.m, a.ldx, a.nkb, a.qx, a.ldqx, a.sx, bx, b - bx * a.gy);
-    } else {
-        quant_128x128_tile<FMT, MODE>(a.w, a.n, a.ldw, a.nkb, a.qw, a.ldqw, a.sw, b - a.nx_blocks, red);
-    }
+    if (JOIN) wait_prerequisite_grid();
 }
 
 // ---------------------------------------------------------------- MXFP8
@@ -442,19 +438,27 @@ cudaError_t launch_quant_1x128(const uint16_t* x, int64_t rows, int64_t cols, in
 cudaError_t launch_quant_linear(const uint16_t* x, int64_t m, int64_t ldx, uint8_t* qx, int64_t ldqx, float* sx,
                                 const uint16_t* w, int64_t n, int64_t ldw, uint8_t* qw, int64_t ldqw, float* sw,
                                 int64_t k, int fmt, int mode, cudaStream_t st) {
-    LinearQuantArgs a;
-    a.x = x; a.m = m; a.ldx = ldx; a.qx = qx; a.ldqx = ldqx; a.sx = sx;
-    a.w = w; a.n = n; a.ldw = ldw; a.qw = qw; a.ldqw = ldqw; a.sw = sw;
-    a.nkb = k / 128;
-    a.gy = (a.nkb + kU1 - 1) / kU1;
-    a.nx_blocks = ((m + 15) / 16) * a.gy;
-    const int64_t grid = a.nx_blocks + ((n + 127) / 128) * a.nkb;
-    if (grid <= 0) return cudaSuccess;
+    // X first (a normal launch: after all earlier work on the stream), then
+    // W as its programmatic dependent, overlapping X's last wave
+    if (m == 0) return launch_quant_128x128(w, n, k, ldw, fmt, mode, qw, ldqw, sw, st);
+    cudaError_t e = launch_quant_1x128(x, m, k, ldx, fmt, mode, qx, ldqx, sx, st);
+    if (e != cudaSuccess || n == 0) return e;
+    const int64_t nkb = k / 128, nrb = (n + 127) / 128;
+    const int64_t grid = nkb * nrb;
     if (grid > 0x7FFFFFFF) return cudaErrorInvalidValue;
-    auto kern = fmt == 0 ? (mode == 0 ? k_quant_linear<0, 0, kU1> : k_quant_linear<0, 1, kU1>)
-                         : (mode == 0 ? k_quant_linear<1, 0, kU1> : k_quant_linear<1, 1, kU1>);
-    kern<<<static_cast<unsigned>(grid), 256, 0, st>>>(a);
-    return cudaGetLastError();
+    auto kern = fmt == 0 ? (mode == 0 ? k_quant_128x128<0, 0, true> : k_quant_128x128<0, 1, true>)
+                         : (mode == 0 ? k_quant_128x128<1, 0, true> : k_quant_128x128<1, 1, true>);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(grid));
+    cfg.blockDim = dim3(256);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, w, n, ldw, nkb, qw, ldqw, sw);
 }
 
 cudaError_t launch_quant_128x128(const uint16_t* w, int64_t rows, int64_t cols, int64_t ldw,
@@ -463,8 +467,8 @@ cudaError_t launch_quant_128x128(const uint16_t* w, int64_t rows, int64_t cols, 
     const int64_t nkb = cols / 128, nrb = (rows + 127) / 128;
     const int64_t grid = nkb * nrb;
     if (grid > 0x7FFFFFFF) return cudaErrorInvalidValue;
-    auto k = fmt == 0 ? (mode == 0 ? k_quant_128x128<0, 0> : k_quant_128x128<0, 1>)
-                      : (mode == 0 ? k_quant_128x128<1, 0> : k_quant_128x128<1, 1>);
+    auto k = fmt == 0 ? (mode == 0 ? k_quant_128x128<0, 0, false> : k_quant_128x128<0, 1, false>)
+                      : (mode == 0 ? k_quant_128x128<1, 0, false> : k_quant_128x128<1, 1, false>);
     k<<<static_cast<unsigned>(grid), 256, 0, st>>>(w, rows, ldw, nkb, q, ldq, scales);
     return cudaGetLastError();
 }

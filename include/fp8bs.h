@@ -98,15 +98,18 @@ int fp8_quantize_128x128(const void* w, int64_t rows, int64_t cols, int64_t ld_w
                          uint8_t* q, int64_t ld_q, float* scales, fp8bs_stream_t stream);
 
 /*
- * Both FP8 operands of one linear layer in one launch: X [m][k] quantized
+ * Both FP8 operands of one linear layer in one call: X [m][k] quantized
  * exactly as fp8_quantize_1x128 does (codes qx [m][ld_qx], scales sx
  * [k/128][m]) and W [n][k] exactly as fp8_quantize_128x128 does (codes qw
  * [n][ld_qw], scales sw [ceil(n/128)][k/128]), with the same fmt and mode.
- * The results equal the two separate calls bit for bit; the single launch
- * saves the second launch's start-up and tail (the quantization overhead the
- * NeMo RL page counts against the FP8 linear layer, hotbookzone.com
- * "Ganancias de rendimiento en el mundo real").  Either operand may be
- * empty (m or n == 0: its pointers are not read).
+ * The results equal the two separate calls bit for bit.  The weight half is
+ * launched as a programmatic dependent of the activation half, so it runs
+ * alongside that grid's last wave instead of after it (part of the
+ * quantization overhead the NeMo RL page counts against the FP8 linear
+ * layer, hotbookzone.com "Ganancias de rendimiento en el mundo real"); work
+ * queued after this call on the stream still starts only once both are done.
+ * The outputs must not overlap the inputs.  Either operand may be empty (m
+ * or n == 0: its pointers are not read).
  * Errors: those of fp8_quantize_1x128 for X and of fp8_quantize_128x128 for W.
  */
 int fp8_quantize_linear(const void* x, int64_t m, int64_t ld_x, uint8_t* qx, int64_t ld_qx, float* sx,

@@ -482,10 +482,11 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
 // tile's O accumulating in tensor memory:
 //   TMEM columns   S_A 0-127, S_B 128-255, O_A 256-383, O_B 384-511.
 //   warp 0         TMA: Q_A and Q_B once, K/V 128-key tiles into 3 stages.
-//   warp 1         MMA: S_X(j) = Q_X K_j^T as soon as tile X's softmax has
-//                  read S_X(j-1); O_X += P_X(j) V_j once P_X(j) is written and
-//                  O_X has been rescaled for tile j.  A and B alternate, so the
-//                  tensor core works on one tile while the other is in softmax.
+//   warps 1, 2     MMA, one issuer per query tile: S_X(j) = Q_X K_j^T as soon
+//                  as tile X's softmax has read S_X(j-1); O_X += P_X(j) V_j once
+//                  P_X(j) is written and O_X has been rescaled for tile j.  The
+//                  two tiles progress independently, so the tensor core works
+//                  on one while the other is in softmax.
 //   warps 4-7      softmax of tile A, warps 8-11 of tile B: one thread per
 //                  query row holds the row's 128 scores (no exchange between
 //                  threads), the row max (reduced by the TMEM loads on fully
@@ -502,8 +503,8 @@ constexpr uint32_t A2_KV_OFF = 2 * AT_TILE;                       // stage s: K 
 constexpr uint32_t A2_P_OFF = A2_KV_OFF + AT_STAGES * 2 * AT_TILE;  // P[X][b]
 constexpr uint32_t A2_BAR_OFF = A2_P_OFF + 4 * AT_TILE;
 // q_full, kv_full[3], kv_empty[3], s_full[2], s_empty[2], p_full[2][2],
-// p_empty[2][2], o_done[2], corr_done[2], a_full[2][4], l_full[2], done
-constexpr int A2_NUM_BARS = 1 + 2 * AT_STAGES + 2 + 2 + 4 + 4 + 2 + 2 + 8 + 2 + 1;
+// p_empty[2][2], o_done[2], corr_done[2], a_full[2][4], l_full[2], done[2]
+constexpr int A2_NUM_BARS = 1 + 2 * AT_STAGES + 2 + 2 + 4 + 4 + 2 + 2 + 8 + 2 + 2;
 constexpr uint32_t A2_TMEMSLOT_OFF = A2_BAR_OFF + A2_NUM_BARS * 8;
 constexpr uint32_t A2_ALPHA_OFF = (A2_TMEMSLOT_OFF + 16 + 15) & ~15u;   // [X][4][128] fp32
 constexpr uint32_t A2_L_OFF = A2_ALPHA_OFF + 2 * 4 * 128 * 4;           // [X][128] fp32
@@ -536,7 +537,7 @@ __global__ void __launch_bounds__(A2_THREADS, 1)
     auto corr_done = [&](int x) { return bars + 8u * (B0 + 14 + x); };
     auto a_full = [&](int x, int k) { return bars + 8u * (B0 + 16 + 4 * x + k); };
     auto l_full = [&](int x) { return bars + 8u * (B0 + 24 + x); };
-    const uint32_t done_bar = bars + 8u * (B0 + 26);
+    auto done_bar = [&](int x) { return bars + 8u * (B0 + 26 + x); };
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + A2_TMEMSLOT_OFF);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -555,7 +556,7 @@ __global__ void __launch_bounds__(A2_THREADS, 1)
         mbar_init(q_full, 1);
         for (int s = 0; s < AT_STAGES; s++) {
             mbar_init(kv_full(s), 1);
-            mbar_init(kv_empty(s), 1);
+            mbar_init(kv_empty(s), 2);            // both MMA issuers
         }
         for (int x = 0; x < 2; x++) {
             mbar_init(s_full(x), 1);
@@ -568,8 +569,8 @@ __global__ void __launch_bounds__(A2_THREADS, 1)
             mbar_init(corr_done(x), 4);          // the four correction warps
             for (int k = 0; k < 4; k++) mbar_init(a_full(x, k), 4);
             mbar_init(l_full(x), 4);
+            mbar_init(done_bar(x), 1);
         }
-        mbar_init(done_bar, 1);
         fence_mbar_init();
         fence_proxy_async_smem();
     }
@@ -604,10 +605,18 @@ __global__ void __launch_bounds__(A2_THREADS, 1)
                     at_drain(kv_full(j % AT_STAGES), (j / AT_STAGES) & 1u);
                 }
             }
-        } else if (warp == 1 && lane == 0 && n > 0) {
-            // ---------------------------------------------------------- MMA
+        } else if ((warp == 1 || warp == 2) && lane == 0 && n > 0) {
+            // ------------------------------------------ MMA, one issuer per tile
+            // warp 1 issues tile A's products, warp 2 tile B's, so that one
+            // tile's softmax never waits behind the other's: S_X(j + 1) as soon
+            // as the softmax has read S_X(j), O_X += P_X(j) V_j once P_X(j) is
+            // written and O_X rescaled.  Both release each K/V stage; for the
+            // key tiles past its own the issuer waits for the stage to fill
+            // first, so that its release counts for that tile.
+            const int x = warp - 1;
+            const int nx = x ? nB : nA;
             bool ok = at_wait(q_full, 0), issued_mma = false;
-            auto issue_s = [&](int x, int j) -> bool {
+            auto issue_s = [&](int j) -> bool {
                 const int s = j % AT_STAGES;
                 if (!at_wait(kv_full(s), (j / AT_STAGES) & 1u)) return false;
                 if (j > 0 && !at_wait(s_empty(x), (j - 1) & 1u)) return false;   // S_X(j-1) was read
@@ -622,7 +631,7 @@ __global__ void __launch_bounds__(A2_THREADS, 1)
                 mma_commit(s_full(x));
                 return true;
             };
-            auto issue_o = [&](int x, int j) -> bool {
+            auto issue_o = [&](int j) -> bool {
                 const int s = j % AT_STAGES, b = j & 1;
                 if (!at_wait(p_full(x, b), (j >> 1) & 1u)) return false;
                 if (!at_wait(corr_done(x), j & 1u)) return false;                 // O_X rescaled for j
@@ -640,18 +649,20 @@ __global__ void __launch_bounds__(A2_THREADS, 1)
                 mma_commit(p_empty(x, b));
                 return true;
             };
-            if (ok && nA > 0) ok = issue_s(0, 0);
-            if (ok && nB > 0) ok = issue_s(1, 0);
+            if (ok && nx > 0) ok = issue_s(0);
             for (int j = 0; ok && j < n; j++) {
-                if (j + 1 < nA && !issue_s(0, j + 1)) { ok = false; break; }
-                if (j < nA && !issue_o(0, j)) { ok = false; break; }
-                if (j + 1 < nB && !issue_s(1, j + 1)) { ok = false; break; }
-                if (j < nB && !issue_o(1, j)) { ok = false; break; }
+                if (j < nx) {
+                    if (j + 1 < nx && !issue_s(j + 1)) { ok = false; break; }
+                    if (!issue_o(j)) { ok = false; break; }
+                } else if (!at_wait(kv_full(j % AT_STAGES), (j / AT_STAGES) & 1u)) {
+                    ok = false;
+                    break;
+                }
                 mma_commit(kv_empty(j % AT_STAGES));
             }
             if (!ok && issued_mma) {
-                mma_commit(done_bar);
-                at_drain(done_bar, 0);
+                mma_commit(done_bar(x));
+                at_drain(done_bar(x), 0);
             }
         }
     } else if (warp < 12) {

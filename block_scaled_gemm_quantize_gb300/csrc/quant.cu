@@ -443,6 +443,10 @@ cudaError_t launch_quant_linear(const uint16_t* x, int64_t m, int64_t ldx, uint8
     if (m == 0) return launch_quant_128x128(w, n, k, ldw, fmt, mode, qw, ldqw, sw, st);
     cudaError_t e = launch_quant_1x128(x, m, k, ldx, fmt, mode, qx, ldqx, sx, st);
     if (e != cudaSuccess || n == 0) return e;
+#ifndef FP8BS_QUANT_PDL
+#define FP8BS_QUANT_PDL 1
+#endif
+    if (!FP8BS_QUANT_PDL) return launch_quant_128x128(w, n, k, ldw, fmt, mode, qw, ldqw, sw, st);
     const int64_t nkb = k / 128, nrb = (n + 127) / 128;
     const int64_t grid = nkb * nrb;
     if (grid > 0x7FFFFFFF) return cudaErrorInvalidValue;

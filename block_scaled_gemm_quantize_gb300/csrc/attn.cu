@@ -114,6 +114,10 @@ __device__ __forceinline__ bool at_drain(uint32_t bar, uint32_t parity) {
     return true;
 }
 
+__device__ __forceinline__ void add_f32x2(uint64_t& acc, uint64_t b) {   // two fp32 adds, one instruction
+    asm("add.rn.f32x2 %0, %0, %1;" : "+l"(acc) : "l"(b));
+}
+
 __device__ __forceinline__ float ex2(float x) {
     float y;
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
@@ -737,19 +741,26 @@ __global__ void __launch_bounds__(A2_THREADS, 1)
             st_shared_f32(sbase + A2_ALPHA_OFF + ((x * 4 + (j & 3)) * 128 + r) * 4, alpha);
             __syncwarp();
             if (lane == 0) mbar_arrive(a_full(x, j & 3));
-            // 448 P = 2^(raw c - m_new + log2 448) (masked: 0), row sum, codes
+            // 448 P = 2^(raw c - m_new + log2 448) (masked: 0), row sum, codes;
+            // the argument and the row sum in packed pairs (f32x2)
             const uint32_t prow = sbase + A2_P_OFF + (2 * x + b) * AT_TILE + r * 128;
-            float rs[8];
+            const uint64_t c2 = pack_f32x2(__float_as_uint(c), __float_as_uint(c));
+            const uint64_t sh2 = pack_f32x2(__float_as_uint(shift), __float_as_uint(shift));
+            uint64_t rs[4];
 #pragma unroll
-            for (int i = 0; i < 8; i++) rs[i] = 0.0f;
+            for (int i = 0; i < 4; i++) rs[i] = 0;
 #pragma unroll
             for (int ch = 0; ch < AT_KEYS / 16; ch++) {          // 16 keys = one 16-byte chunk
                 float pv[16];
 #pragma unroll
-                for (int e = 0; e < 16; e++) {
+                for (int e = 0; e < 16; e += 2) {
                     const int k = ch * 16 + e;
-                    pv[e] = ex2(fmaf(__uint_as_float(sr[k >> 5][k & 31]), c, shift));
-                    rs[e & 7] += pv[e];
+                    uint64_t a2 = sh2;
+                    fma_f32x2(a2, pack_f32x2(sr[k >> 5][k & 31], sr[k >> 5][(k & 31) + 1]), c2);
+                    const float2 a = unpack_f32x2(a2);
+                    pv[e] = ex2(a.x);
+                    pv[e + 1] = ex2(a.y);
+                    add_f32x2(rs[(e >> 1) & 3], pack_f32x2(__float_as_uint(pv[e]), __float_as_uint(pv[e + 1])));
                 }
                 uint32_t w[4];
 #pragma unroll
@@ -757,7 +768,8 @@ __global__ void __launch_bounds__(A2_THREADS, 1)
                 st_shared_v4(prow + ((static_cast<uint32_t>(ch) ^ (static_cast<uint32_t>(r) & 7u)) << 4), w[0], w[1],
                              w[2], w[3]);
             }
-            const float rsum = ((rs[0] + rs[1]) + (rs[2] + rs[3])) + ((rs[4] + rs[5]) + (rs[6] + rs[7]));
+            float2 q0 = unpack_f32x2(rs[0]), q1 = unpack_f32x2(rs[1]), q2 = unpack_f32x2(rs[2]), q3 = unpack_f32x2(rs[3]);
+            const float rsum = ((q0.x + q1.x) + (q2.x + q3.x)) + ((q0.y + q1.y) + (q2.y + q3.y));
             fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) mbar_arrive(p_full(x, b));

@@ -751,51 +751,70 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         uint32_t chunk = 0, tile_i = 0;
         bool ok = true;
         const int64_t nkb64 = nkb;
-        for (int t = blockIdx.x; ok && t < total_tiles; t += gridDim.x, tile_i++) {
-            const Tile tl = decode_tile(t, total_slots, p.tiles_n, G, s_slot, s_off);
-            const int64_t row = static_cast<int64_t>(tl.row0) + lrow;
-            const bool row_ok = row < tl.row_end;
-            const int64_t srow = row < p.a_rows ? row : p.a_rows - 1;   // clamp for scale reads
-            const int64_t col0 = static_cast<int64_t>(tl.nt) * BN + half * 128;
+        // A tile's row, columns and scale pointers (advanced per K block).
+        struct TileCtx {
+            Tile tl;
+            int64_t row, col0;
+            bool row_ok;
+            const float *pa, *pb, *pbu;
+            int64_t sa_step, sb_step;
+        };
+        auto setup = [&](int t) {
+            TileCtx c;
+            c.tl = decode_tile(t, total_slots, p.tiles_n, G, s_slot, s_off);
+            c.row = static_cast<int64_t>(c.tl.row0) + lrow;
+            c.row_ok = c.row < c.tl.row_end;
+            const int64_t srow = c.row < p.a_rows ? c.row : p.a_rows - 1;   // clamp for scale reads
+            c.col0 = static_cast<int64_t>(c.tl.nt) * BN + half * 128;
             // weight row-blocks of this thread's columns 0-63 (nb) and 64-127
             // (nbu); they differ only with SwiGLU (gate and up rows)
-            const int64_t nb = SWIGLU ? tl.nt : min(col0, p.N - 1) / 128;
-            const int64_t nbu = SWIGLU ? p.swiglu_i / 128 + tl.nt : nb;
-            // scale pointers for this (row, column block); advanced per K block
-            const float* pa;
-            int64_t sa_step;
-            if (p.a_gran == 0) { pa = p.sa + srow; sa_step = p.a_rows; }
+            const int64_t nb = SWIGLU ? c.tl.nt : min(c.col0, p.N - 1) / 128;
+            const int64_t nbu = SWIGLU ? p.swiglu_i / 128 + c.tl.nt : nb;
+            if (p.a_gran == 0) { c.pa = p.sa + srow; c.sa_step = p.a_rows; }
             else if (p.a_gran == 1) {
-                if (A_MN) { pa = p.sa + srow / 128; sa_step = p.a_rblocks; }
-                else { pa = p.sa + (srow / 128) * nkb64; sa_step = 1; }
-            } else { pa = p.sa; sa_step = 0; }
-            const float* pb;
-            const float* pbu;
-            int64_t sb_step;
+                if (A_MN) { c.pa = p.sa + srow / 128; c.sa_step = p.a_rblocks; }
+                else { c.pa = p.sa + (srow / 128) * nkb64; c.sa_step = 1; }
+            } else { c.pa = p.sa; c.sa_step = 0; }
             if (p.b_gran == 1) {
-                if (B_MN) { pb = p.sb + nb; pbu = pb; sb_step = p.b_rblocks; }
+                if (B_MN) { c.pb = p.sb + nb; c.pbu = c.pb; c.sb_step = p.b_rblocks; }
                 else {
-                    pb = p.sb + tl.g * p.b_scale_group_stride + nb * nkb64;
-                    pbu = p.sb + tl.g * p.b_scale_group_stride + nbu * nkb64;
-                    sb_step = 1;
+                    c.pb = p.sb + c.tl.g * p.b_scale_group_stride + nb * nkb64;
+                    c.pbu = p.sb + c.tl.g * p.b_scale_group_stride + nbu * nkb64;
+                    c.sb_step = 1;
                 }
-            } else { pb = p.sb; pbu = pb; sb_step = 0; }
+            } else { c.pb = p.sb; c.pbu = c.pb; c.sb_step = 0; }
+            return c;
+        };
+        // Scales: a ring of SPF register slots, slot i holding chunk
+        // (kb0 + i); the K-block loop is unrolled by SPF so each slot is
+        // refilled (SPF chunks ahead) right after use, with no register
+        // copies that would wait on the load early.  A tile's first SPF
+        // scales are loaded before the previous tile is stored, so the
+        // store hides their latency.
+        float sa_r[SPF], sb_r[SPF], sbu_r[SPF];
+        auto fill = [&](const TileCtx& c) {
+#pragma unroll
+            for (int i = 0; i < SPF; i++) {
+                const int kbi = min(i * P, nkb - 1);
+                sa_r[i] = ld_scale(c.pa + kbi * c.sa_step);
+                sb_r[i] = ld_scale(c.pb + kbi * c.sb_step);
+                sbu_r[i] = SWIGLU ? ld_scale(c.pbu + kbi * c.sb_step) : sb_r[i];
+            }
+        };
+        TileCtx cur;
+        if (static_cast<int>(blockIdx.x) < total_tiles) {
+            cur = setup(blockIdx.x);
+            fill(cur);
+        }
+        for (int t = blockIdx.x; ok && t < total_tiles; t += gridDim.x, tile_i++) {
+            const float* pa = cur.pa;
+            const float* pb = cur.pb;
+            const float* pbu = cur.pbu;
+            const int64_t sa_step = cur.sa_step, sb_step = cur.sb_step;
 
             uint64_t acc[64];   // 128 fp32 accumulators as packed pairs
 #pragma unroll
             for (int i = 0; i < 64; i++) acc[i] = 0;
-            // Scales: a ring of SPF register slots, slot i holding chunk
-            // (kb0 + i); the K-block loop is unrolled by SPF so each slot is
-            // refilled (SPF chunks ahead) right after use, with no register
-            // copies that would wait on the load early.
-            float sa_r[SPF], sb_r[SPF], sbu_r[SPF];
-#pragma unroll
-            for (int i = 0; i < SPF; i++) {
-                const int kbi = min(i * P, nkb - 1);
-                sa_r[i] = ld_scale(pa + kbi * sa_step);
-                sb_r[i] = ld_scale(pb + kbi * sb_step);
-                sbu_r[i] = SWIGLU ? ld_scale(pbu + kbi * sb_step) : sb_r[i];
-            }
             for (int kb0 = 0; ok && kb0 < nkb; kb0 += SPF * P) {
 #pragma unroll
                 for (int i = 0; i < SPF; i++) {
@@ -850,7 +869,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 }
             }
             if (!ok) break;
-            ok = finish_tile<SWIGLU>(p, tmY, acc, tl, row, row_ok, col0, quarter, half, lane,
+            const TileCtx done = cur;
+            if (t + static_cast<int>(gridDim.x) < total_tiles) {
+                cur = setup(t + gridDim.x);
+                fill(cur);
+            }
+            ok = finish_tile<SWIGLU>(p, tmY, acc, done.tl, done.row, done.row_ok, done.col0, quarter, half, lane,
                              sbase + L::kOutOff + (warp - EPI_WARP0) * L::kSlab, sbase + L::kXchgOff,
                              xchg_bar(quarter), tile_i & 1u, L::kSubs);
         }

@@ -256,6 +256,7 @@ int run_gemm(const char* fn, int32_t G, const int32_t* offsets, int64_t a_rows, 
     p.b_rows_per_group = grouped ? static_cast<int32_t>(N) : 0;
     p.a_gran = A->gran;
     p.b_gran = B->gran;
+    p.sa_bulk = A->gran == FP8BS_GRAN_1x128 && a_rows % 4 == 0 && aligned16(A->scales);
     p.tiles_n = static_cast<int32_t>(swiglu ? n_out / 128 : (N + BN - 1) / BN);
     p.promote = (A->gran == FP8BS_GRAN_TENSOR && B->gran == FP8BS_GRAN_TENSOR) ? 0 : 1;
     p.out_bf16 = !o.quant && o.dtype == FP8BS_OUT_BF16;

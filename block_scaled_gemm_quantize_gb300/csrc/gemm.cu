@@ -14,18 +14,23 @@
 //               tcgen05.mma.kind::f8f6f4 (M=128, K=32) over the 256 columns,
 //               as one N=256 slice (H = 1: a ring of two 256-column TMEM
 //               buffers) or two N=128 slices (H = 2: four 128-column buffers).
-//   warp 2      idle; warp 3 loads per-column B scales (1x128 B) into a
-//               shared-memory ring when the product has them.
+//   warp 2      idle.
+//   warp 3      scales: per K block, the products sA(row) * sB(column block)
+//               for the tile's 128 rows into a shared-memory slot of the
+//               block's TMEM buffer (loaded a few blocks ahead), its lanes
+//               then joining that buffer's "full" barrier with the MMA
+//               commit; with per-column B scales (1x128 B) it instead loads
+//               the raw scale rows into a shared-memory ring.
 //   warps 4..11 epilogue ("promotion"): each thread owns one output row (its
-//               TMEM lane) and 128 columns; per K block it loads the fp32
-//               partial from TMEM and folds it into fp32 registers with that
-//               block's scales: acc = fma(partial, sA * sB, acc), two columns
-//               per packed f32x2 FMA.  At the end of a tile it stores bf16 or
-//               fp32, or quantizes (optionally after SwiGLU) to the next
-//               linear's FP8 operand.
+//               TMEM lane) and 128 columns; per K block it waits once for
+//               the partial and its scale, loads the fp32 partial from TMEM
+//               and folds it into fp32 registers: acc = fma(partial, sA * sB,
+//               acc), two columns per packed f32x2 FMA.  At the end of a tile
+//               it stores bf16 or fp32, or quantizes (optionally after
+//               SwiGLU) to the next linear's FP8 operand.
 // Register split (setmaxnreg): the block launches with 168 registers per
-// thread (384 x 168 = 64512); the first warpgroup releases down to 72 and the
-// two epilogue warpgroups grow to 216: 128 x 72 + 256 x 216 = 64512.
+// thread (384 x 168 = 64512); the first warpgroup releases down to 104 and the
+// two epilogue warpgroups grow to 200: 128 x 104 + 256 x 200 = 64512.
 // A TMEM buffer goes back to the MMA right after the epilogue's last load of
 // it, so the MMAs of the next block(s) overlap the promotion arithmetic.
 // When both operands have one scale per tensor the whole K accumulates in
@@ -59,24 +64,13 @@ constexpr uint32_t B_STAGE = BN * BK;   // 32 KiB
 constexpr uint32_t STAGE_BYTES = A_STAGE + B_STAGE;
 constexpr int NUM_THREADS = 384;
 constexpr int EPI_WARP0 = 4;
-constexpr int REGS_LOW = 72, REGS_HIGH = 216;   // 128*72 + 256*216 == 384*168
+constexpr int REGS_LOW = 56, REGS_HIGH = 224;   // 128*56 + 256*224 == 384*168
 constexpr int NUM_EPI_WARPS = 8;
 constexpr uint32_t TMEM_COLS = 512;
 #ifndef FP8BS_RASTER_M
 #define FP8BS_RASTER_M 16
 #endif
 constexpr int RASTER_M = FP8BS_RASTER_M;   // m-slots per rasterization group
-#ifndef FP8BS_EPI_LOADS
-#define FP8BS_EPI_LOADS 1
-#endif
-constexpr int EPI_LOADS = FP8BS_EPI_LOADS;   // TMEM loads (x32 columns) per wait
-#ifndef FP8BS_SPF
-#define FP8BS_SPF 8
-#endif
-constexpr int SPF = FP8BS_SPF;               // scale prefetch distance (chunks)
-#ifndef FP8BS_FFMA2
-#define FP8BS_FFMA2 1                        // packed f32x2 promotion FMAs
-#endif
 constexpr uint64_t WAIT_LIMIT_NS = 4000000000ull;
 constexpr uint64_t DRAIN_LIMIT_NS = 200000000ull;
 
@@ -99,6 +93,18 @@ constexpr int MAX_TBUFS = 4;
 // tile's 256 B column scales (1 KiB) and, for a 1x128 A, its 128 row scales
 constexpr int BSF_SLOTS = 4;
 constexpr uint32_t BSF_SLOT_BYTES = 1536;
+// promotion products (in the B-scale ring's space, unused by those kernels):
+// per TMEM buffer a slot of the scale products of its 128 rows for two
+// column parts (the two 128-column halves, or SwiGLU's gate and up blocks);
+// then, with a 1x128 A scale table, a ring of SR_SLOTS slots, slot i %
+// SR_SLOTS holding the A scales of K block i of this CTA for the tile's rows
+// [r0, r0 + 132), r0 = its first row rounded down to a multiple of 4: the
+// producer copies them (one bulk copy) along with the block's operand tiles
+constexpr uint32_t SC_SLOT_BYTES = 2 * 128 * 4;
+constexpr int SR_SLOTS = BSF_SLOTS;   // barriers: bsf_full = ready, bsf_empty = free
+constexpr uint32_t SR_SLOT_BYTES = 132 * 4;
+static_assert(2 * SC_SLOT_BYTES + SR_SLOTS * SR_SLOT_BYTES <= BSF_SLOTS * BSF_SLOT_BYTES,
+              "scale slots fit the B-scale ring");
 // output staging: 2 KiB sub-slabs (32 rows x 64 B, 64-B swizzle), one or four
 // per epilogue warp
 constexpr uint32_t OUT_SUB = 2048;
@@ -132,8 +138,7 @@ struct GemmLayout {
     static_assert(kSmemBytes <= 232448, "shared memory budget");
 };
 template <bool A_MN, bool B_MN, bool SWIGLU, bool B_COL>
-using GemmLayoutFor = GemmLayout<(A_MN || B_MN || SWIGLU || B_COL) ? STAGES : STAGES - 1,
-                                 (A_MN || B_MN || SWIGLU || B_COL) ? 1 : 4>;
+using GemmLayoutFor = GemmLayout<STAGES, 1>;
 
 __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
     if (mbar_try_wait(bar, parity)) return true;
@@ -181,6 +186,13 @@ __device__ __forceinline__ Tile decode_tile(int t, int total_slots, int tiles_n,
 }
 
 __device__ __forceinline__ float ld_scale(const float* p) { return __ldg(p); }
+// a scale load kept in program order with the surrounding shared-memory
+// accesses (bounds how many are in flight)
+__device__ __forceinline__ float ld_scale_ordered(const float* p) {
+    float v;
+    asm volatile("ld.global.nc.f32 %0, [%1];" : "=f"(v) : "l"(p) : "memory");
+    return v;
+}
 
 // Store one warp's 32 rows x 128 columns of a finished tile (acc = 128 fp32
 // as packed pairs): TMA bulk stores of 32 x 64-byte boxes staged in the warp's
@@ -430,6 +442,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     auto xchg_bar = [&](int q) { return bars + 8u * (2 * STAGES + 2 * MAX_TBUFS + 1 + q); };
     auto bsf_full = [&](int q) { return bars + 8u * (2 * STAGES + 2 * MAX_TBUFS + 5 + q); };
     auto bsf_empty = [&](int q) { return bars + 8u * (2 * STAGES + 2 * MAX_TBUFS + 5 + BSF_SLOTS + q); };
+    auto sr_ready = [&](int q) { return bsf_full(q); };   // (promotion products) a scale-ring
+    auto sr_free = [&](int q) { return bsf_empty(q); };   // slot landed / was read
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kTmemSlotOff);
     int* s_off = reinterpret_cast<int*>(smem + L::kTableOff);
     int* s_slot = s_off + (kMaxGroups + 1);
@@ -446,14 +460,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             mbar_init(empty_bar(s), 1);
         }
         for (int b = 0; b < TBUFS; b++) {
-            mbar_init(tfull_bar(b), 1);
+            // the MMA commit, plus the scale warp's 32 lanes (promotion products)
+            mbar_init(tfull_bar(b), B_COL ? 1 : 33);
             mbar_init(tempty_bar(b), NUM_EPI_WARPS / H);   // the warps reading it
         }
         mbar_init(done_bar, 1);
         for (int q = 0; q < 4; q++) mbar_init(xchg_bar(q), 64);
         for (int q = 0; q < BSF_SLOTS; q++) {
-            mbar_init(bsf_full(q), 1);                    // the loader's expect_tx arrival
-            mbar_init(bsf_empty(q), NUM_EPI_WARPS);       // one arrival per epilogue warp
+            mbar_init(bsf_full(q), 1);   // the loader's (promotion: the producer's) expect_tx arrival
+            // one arrival per epilogue warp (promotion: per scale-warp lane)
+            mbar_init(bsf_empty(q), B_COL ? NUM_EPI_WARPS : 32);
         }
         fence_mbar_init();
         fence_proxy_async_smem();
@@ -517,8 +533,23 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 const Tile tl = decode_tile(t, total_slots, p.tiles_n, G, s_slot, s_off);
                 const int a_row = tl.row0;
                 const int b_row = tl.g * p.b_rows_per_group + tl.nt * BN;
+                // this tile's A scale rows for the scale ring
+                const int64_t sr0 = tl.row0 & ~3;
+                const uint32_t sr_bytes = static_cast<uint32_t>(
+                    ((min(static_cast<int64_t>(tl.row0) + BM, p.a_rows) + 3) & ~3ll) - sr0) * 4u;
                 for (int kb = 0; kb < nkb; kb++) {
                     if (!wait_or_flag(empty_bar(stage), phase ^ 1u)) { ok = false; break; }
+                    if (!B_COL && p.sa_bulk) {
+                        // the block's A scales, into the scale ring (their own barrier)
+                        const int q = issued % SR_SLOTS;
+                        if (!wait_or_flag(sr_free(q), ((static_cast<uint32_t>(issued) / SR_SLOTS) & 1u) ^ 1u)) {
+                            ok = false;
+                            break;
+                        }
+                        mbar_arrive_expect_tx(sr_ready(q), sr_bytes);
+                        bulk_load_g2s(sbase + L::kBsfOff + TBUFS * SC_SLOT_BYTES + q * SR_SLOT_BYTES,
+                                      p.sa + static_cast<int64_t>(kb) * p.a_rows + sr0, sr_bytes, sr_ready(q));
+                    }
                     mbar_arrive_expect_tx(full_bar(stage), STAGE_BYTES);
                     const int kc = kb * BK;
                     const uint32_t dA = sA + stage * A_STAGE, dB = sB + stage * B_STAGE;
@@ -651,6 +682,83 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 }
             }
         }
+      } else if (!B_COL && warp == 3) {
+        // ------------------------------------- scale warp (promotion products)
+        // Chunk c of this CTA (P K blocks of one tile, in the MMA's order)
+        // goes to TMEM buffer c % TBUFS.  For its first K block the lanes
+        // take the A scales of rows l + 32 e (lane l) -- from the scale ring
+        // once its copy has landed, or else from global memory -- and the
+        // two B scales; once the epilogue has released the
+        // buffer (it read the slot's previous products before), they write
+        // the products sA(row) * sB(part) into the buffer's slot and arrive
+        // on its full barrier, so the epilogue waits once per chunk.
+        static_assert(B_COL || H == 1, "one TMEM buffer per K block");
+        const int cpt = nkb / P;
+        const bool bulk = p.sa_bulk != 0;
+        const uint32_t ring0 = sbase + L::kBsfOff + TBUFS * SC_SLOT_BYTES;
+        uint32_t c = 0;
+        bool ok = true;
+        for (int t = blockIdx.x; ok && t < total_tiles; t += gridDim.x) {
+            const Tile tl = decode_tile(t, total_slots, p.tiles_n, G, s_slot, s_off);
+            const int r0 = tl.row0 & ~3;
+            uint32_t ro[4];   // rows l + 32 e (clamped) relative to r0
+#pragma unroll
+            for (int e = 0; e < 4; e++)
+                ro[e] = static_cast<uint32_t>(min(static_cast<int64_t>(tl.row0) + lane + 32 * e, p.a_rows - 1) - r0);
+            // the parts' weight row-blocks: columns 0-127 and 128-255 of the
+            // tile, or SwiGLU's gate and up rows
+            const int64_t n0 = static_cast<int64_t>(tl.nt) * BN;
+            const int64_t nb0 = SWIGLU ? tl.nt : min(n0, p.N - 1) / 128;
+            const int64_t nb1 = SWIGLU ? p.swiglu_i / 128 + tl.nt : min(n0 + 128, p.N - 1) / 128;
+            const float* pb0 = p.sb;
+            int64_t db = 0, sb_step = 0;   // part 1 at pb0 + db; per K block + sb_step
+            if (p.b_gran == 1) {
+                pb0 = B_MN ? p.sb + nb0 : p.sb + tl.g * p.b_scale_group_stride + nb0 * nkb;
+                db = B_MN ? nb1 - nb0 : (nb1 - nb0) * nkb;
+                sb_step = B_MN ? p.b_rblocks : 1;
+            }
+            for (int ci = 0; ci < cpt; ci++, c++) {
+                const int64_t kb = static_cast<int64_t>(ci) * P;
+                const float* pbk = pb0 + kb * sb_step;
+                const float b0 = ld_scale(pbk), b1 = ld_scale(pbk + db);
+                const uint32_t q = c % SR_SLOTS;
+                const uint32_t ring = ring0 + q * SR_SLOT_BYTES;
+                if (bulk) {
+                    ok = __all_sync(0xFFFFFFFFu, wait_or_flag(sr_ready(q), (c / SR_SLOTS) & 1u));
+                    if (!ok) break;
+                } else {
+                    // no ring copy: this lane stages its rows' A scales itself,
+                    // row r's at sa + kb * ks + (r or its 128-row block) * rs,
+                    // two loads in flight
+                    const int64_t ks = p.a_gran == 0 ? p.a_rows : p.a_gran == 1 ? (A_MN ? p.a_rblocks : 1) : 0;
+                    const int64_t rs = p.a_gran == 1 && !A_MN ? nkb : p.a_gran == 2 ? 0 : 1;
+                    const int sh = p.a_gran == 1 ? 7 : 0;
+                    const float* pak = p.sa + kb * ks;
+                    const float v0 = ld_scale_ordered(pak + ((r0 + static_cast<int>(ro[0])) >> sh) * rs);
+                    const float v1 = ld_scale_ordered(pak + ((r0 + static_cast<int>(ro[1])) >> sh) * rs);
+                    st_shared_f32(ring + ro[0] * 4, v0);
+                    st_shared_f32(ring + ro[1] * 4, v1);
+                    const float v2 = ld_scale_ordered(pak + ((r0 + static_cast<int>(ro[2])) >> sh) * rs);
+                    const float v3 = ld_scale_ordered(pak + ((r0 + static_cast<int>(ro[3])) >> sh) * rs);
+                    st_shared_f32(ring + ro[2] * 4, v2);
+                    st_shared_f32(ring + ro[3] * 4, v3);
+                }
+                float a[4];
+#pragma unroll
+                for (int e = 0; e < 4; e++) a[e] = ld_shared_f32(ring + ro[e] * 4);
+                if (bulk) mbar_arrive(sr_free(q));   // each lane: its reads are done
+                const uint32_t buf = c % TBUFS;
+                ok = __all_sync(0xFFFFFFFFu, wait_or_flag(tempty_bar(buf), ((c / TBUFS) & 1u) ^ 1u));
+                if (!ok) break;
+                const uint32_t slot = sbase + L::kBsfOff + buf * SC_SLOT_BYTES;
+#pragma unroll
+                for (int e = 0; e < 4; e++) {
+                    st_shared_f32(slot + (lane + 32 * e) * 4, a[e] * b0);
+                    st_shared_f32(slot + (128 + lane + 32 * e) * 4, a[e] * b1);
+                }
+                mbar_arrive(tfull_bar(buf));
+            }
+        }
       }
     } else if (B_COL) {
         asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(REGS_HIGH));
@@ -748,133 +856,54 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const int quarter = warp & 3;           // TMEM lanes 32*quarter ..
         const int half = (warp - EPI_WARP0) >> 2;  // columns 128*half ..
         const int lrow = quarter * 32 + lane;
+        const int cpt = nkb / P;                // TMEM chunks per tile
+        // this thread's scale products in a slot: its half's part (SwiGLU:
+        // the gate part for columns 0-63, the up part for 64-127)
+        const uint32_t s_off0 = (SWIGLU ? 0u : static_cast<uint32_t>(half) * 512u) + lrow * 4;
+        const uint32_t s_off1 = SWIGLU ? 512u + lrow * 4 : s_off0;
         uint32_t chunk = 0, tile_i = 0;
         bool ok = true;
-        const int64_t nkb64 = nkb;
-        // A tile's row, columns and scale pointers (advanced per K block).
-        struct TileCtx {
-            Tile tl;
-            int64_t row, col0;
-            bool row_ok;
-            const float *pa, *pb, *pbu;
-            int64_t sa_step, sb_step;
-        };
-        auto setup = [&](int t) {
-            TileCtx c;
-            c.tl = decode_tile(t, total_slots, p.tiles_n, G, s_slot, s_off);
-            c.row = static_cast<int64_t>(c.tl.row0) + lrow;
-            c.row_ok = c.row < c.tl.row_end;
-            const int64_t srow = c.row < p.a_rows ? c.row : p.a_rows - 1;   // clamp for scale reads
-            c.col0 = static_cast<int64_t>(c.tl.nt) * BN + half * 128;
-            // weight row-blocks of this thread's columns 0-63 (nb) and 64-127
-            // (nbu); they differ only with SwiGLU (gate and up rows)
-            const int64_t nb = SWIGLU ? c.tl.nt : min(c.col0, p.N - 1) / 128;
-            const int64_t nbu = SWIGLU ? p.swiglu_i / 128 + c.tl.nt : nb;
-            if (p.a_gran == 0) { c.pa = p.sa + srow; c.sa_step = p.a_rows; }
-            else if (p.a_gran == 1) {
-                if (A_MN) { c.pa = p.sa + srow / 128; c.sa_step = p.a_rblocks; }
-                else { c.pa = p.sa + (srow / 128) * nkb64; c.sa_step = 1; }
-            } else { c.pa = p.sa; c.sa_step = 0; }
-            if (p.b_gran == 1) {
-                if (B_MN) { c.pb = p.sb + nb; c.pbu = c.pb; c.sb_step = p.b_rblocks; }
-                else {
-                    c.pb = p.sb + c.tl.g * p.b_scale_group_stride + nb * nkb64;
-                    c.pbu = p.sb + c.tl.g * p.b_scale_group_stride + nbu * nkb64;
-                    c.sb_step = 1;
-                }
-            } else { c.pb = p.sb; c.pbu = c.pb; c.sb_step = 0; }
-            return c;
-        };
-        // Scales: a ring of SPF register slots, slot i holding chunk
-        // (kb0 + i); the K-block loop is unrolled by SPF so each slot is
-        // refilled (SPF chunks ahead) right after use, with no register
-        // copies that would wait on the load early.  A tile's first SPF
-        // scales are loaded before the previous tile is stored, so the
-        // store hides their latency.
-        float sa_r[SPF], sb_r[SPF], sbu_r[SPF];
-        auto fill = [&](const TileCtx& c) {
-#pragma unroll
-            for (int i = 0; i < SPF; i++) {
-                const int kbi = min(i * P, nkb - 1);
-                sa_r[i] = ld_scale(c.pa + kbi * c.sa_step);
-                sb_r[i] = ld_scale(c.pb + kbi * c.sb_step);
-                sbu_r[i] = SWIGLU ? ld_scale(c.pbu + kbi * c.sb_step) : sb_r[i];
-            }
-        };
-        TileCtx cur;
-        if (static_cast<int>(blockIdx.x) < total_tiles) {
-            cur = setup(blockIdx.x);
-            fill(cur);
-        }
         for (int t = blockIdx.x; ok && t < total_tiles; t += gridDim.x, tile_i++) {
-            const float* pa = cur.pa;
-            const float* pb = cur.pb;
-            const float* pbu = cur.pbu;
-            const int64_t sa_step = cur.sa_step, sb_step = cur.sb_step;
+            const Tile tl = decode_tile(t, total_slots, p.tiles_n, G, s_slot, s_off);
+            const int64_t row = static_cast<int64_t>(tl.row0) + lrow;
+            const bool row_ok = row < tl.row_end;
+            const int64_t col0 = static_cast<int64_t>(tl.nt) * BN + half * 128;
 
             uint64_t acc[64];   // 128 fp32 accumulators as packed pairs
 #pragma unroll
             for (int i = 0; i < 64; i++) acc[i] = 0;
-            for (int kb0 = 0; ok && kb0 < nkb; kb0 += SPF * P) {
+#pragma unroll 1
+            for (int ci = 0; ci < cpt; ci++, chunk++) {
+                const uint32_t buf = chunk % TBUFS;
+                // one wait: the partial (MMA commit) and its scale products
+                ok = __all_sync(0xFFFFFFFFu, wait_or_flag(tfull_bar(buf), (chunk / TBUFS) & 1u));
+                if (!ok) break;
+                tc_fence_after();
+                const uint32_t slot = sbase + L::kBsfOff + buf * SC_SLOT_BYTES;
+                const float s = ld_shared_f32(slot + s_off0);
+                const float su = SWIGLU ? ld_shared_f32(slot + s_off1) : s;
+                const uint64_t s2 = pack_f32x2(__float_as_uint(s), __float_as_uint(s));
+                const uint64_t s2u = pack_f32x2(__float_as_uint(su), __float_as_uint(su));
+                const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + buf * MMA_N + half * 128;
+                // 32 columns per TMEM round trip; the buffer is handed back
+                // right after the last load
 #pragma unroll
-                for (int i = 0; i < SPF; i++) {
-                    const int kb = kb0 + i * P;
-                    if (kb >= nkb) break;
-                    const float s = sa_r[i] * sb_r[i];
-                    const uint64_t s2 = pack_f32x2(__float_as_uint(s), __float_as_uint(s));
-                    const float su = sa_r[i] * sbu_r[i];
-                    const uint64_t s2u = pack_f32x2(__float_as_uint(su), __float_as_uint(su));
-                    if (kb + SPF * P < nkb) {
-                        sa_r[i] = ld_scale(pa + (kb + SPF * P) * sa_step);
-                        sb_r[i] = ld_scale(pb + (kb + SPF * P) * sb_step);
-                        sbu_r[i] = SWIGLU ? ld_scale(pbu + (kb + SPF * P) * sb_step) : sb_r[i];
+                for (int j = 0; j < 4; j++) {
+                    uint32_t r[32];
+                    tmem_ld_32x32b_x32(taddr + j * 32, r);
+                    tmem_wait_ld();
+                    if (j == 3) {
+                        tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(tempty_bar(buf));
                     }
-                    const uint32_t c = H * chunk + (H == 2 ? half : 0), buf = c % TBUFS;
-                    ok = __all_sync(0xFFFFFFFFu, wait_or_flag(tfull_bar(buf), (c / TBUFS) & 1u));
-                    if (!ok) break;
-                    tc_fence_after();
-                    const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
-                                           buf * MMA_N + (H == 1 ? half * 128 : 0);
-                    // EPI_LOADS x 32 columns in flight per wait (one TMEM round
-                    // trip); the buffer is handed back right after the last load
 #pragma unroll
-                    for (int j = 0; j < 4; j += EPI_LOADS) {
-                        uint32_t r[EPI_LOADS][32];
-#pragma unroll
-                        for (int u = 0; u < EPI_LOADS; u++) tmem_ld_32x32b_x32(taddr + (j + u) * 32, r[u]);
-                        tmem_wait_ld();
-                        if (j + EPI_LOADS >= 4) {
-                            tc_fence_before();
-                            __syncwarp();
-                            if (lane == 0) mbar_arrive(tempty_bar(buf));
-                        }
-#pragma unroll
-                        for (int u = 0; u < EPI_LOADS; u++) {
-#pragma unroll
-                            for (int q = 0; q < 16; q++) {
-#if FP8BS_FFMA2
-                                fma_f32x2(acc[(j + u) * 16 + q], pack_f32x2(r[u][2 * q], r[u][2 * q + 1]),
-                                          j + u < 2 ? s2 : s2u);
-#else
-                                const float sc = j + u < 2 ? s : su;
-                                float2 a = unpack_f32x2(acc[(j + u) * 16 + q]);
-                                a.x = __fmaf_rn(__uint_as_float(r[u][2 * q]), sc, a.x);
-                                a.y = __fmaf_rn(__uint_as_float(r[u][2 * q + 1]), sc, a.y);
-                                acc[(j + u) * 16 + q] = pack_f32x2(__float_as_uint(a.x), __float_as_uint(a.y));
-#endif
-                            }
-                        }
-                    }
-                    chunk++;
+                    for (int q = 0; q < 16; q++)
+                        fma_f32x2(acc[j * 16 + q], pack_f32x2(r[2 * q], r[2 * q + 1]), j < 2 ? s2 : s2u);
                 }
             }
             if (!ok) break;
-            const TileCtx done = cur;
-            if (t + static_cast<int>(gridDim.x) < total_tiles) {
-                cur = setup(t + gridDim.x);
-                fill(cur);
-            }
-            ok = finish_tile<SWIGLU>(p, tmY, acc, done.tl, done.row, done.row_ok, done.col0, quarter, half, lane,
+            ok = finish_tile<SWIGLU>(p, tmY, acc, tl, row, row_ok, col0, quarter, half, lane,
                              sbase + L::kOutOff + (warp - EPI_WARP0) * L::kSlab, sbase + L::kXchgOff,
                              xchg_bar(quarter), tile_i & 1u, L::kSubs);
         }

@@ -29,6 +29,8 @@ struct GemmParams {
     int32_t promote;          // 1: scale per 128-K block; 0: one scale per tensor pair
     int32_t out_bf16;
     int32_t tma_store;        // 1: tmY describes Y (box 32 rows x 64 B, 64-B swizzle)
+    int32_t sa_bulk;          // 1: 1x128 A scale table 16-byte aligned with a_rows % 4 == 0
+                              //    (copied by bulk copies, a K block's rows at once)
     uint32_t idesc;
     // Quantized output: Y holds 8-bit codes [rows][n_out] and sq its 1x128
     // scales [n_out/128][a_rows] (the next linear's activation operand).

@@ -343,3 +343,74 @@ def test_pow2_mode_with_per_tensor_scales_that_are_not_powers_of_two():
                            fp8.operand(dev(qb), dev(sb), gran=fp8.GRAN_128x128), M, N, K, fp8.OUT_F32,
                            fp8.SCALE_POW2)
     _check(y, y_ref, yabs, fp8.OUT_F32)
+
+
+def _block_varying(x_bits, K, seed):
+    """Activations whose magnitude changes by up to 2^4 from one 128-column
+    block to the next (and between rows), so that a scale applied to the
+    wrong K block or row moves the result far outside the tolerance."""
+    x = inputs.bits_to_f32(x_bits).astype(np.float64)
+    rng = np.random.default_rng(seed)
+    blk = 2.0 ** rng.integers(-2, 3, size=(x.shape[0] // 64 + 1, K // 128))
+    f = np.repeat(np.repeat(blk, 64, axis=0)[:x.shape[0]], 128, axis=1)
+    return inputs.bf16_bits((x * f).astype(np.float32))
+
+
+def test_repeated_grouped_runs_are_identical_and_match_the_oracle():
+    """Many tiles per CTA with a short K (the scale ring and the two TMEM
+    buffers wrap many times per tile sequence) on 64 experts with ragged
+    group starts: eight launches give bit-identical outputs, and every row of
+    the first is checked against the oracle on sampled columns."""
+    import torch
+    from helpers import par_grouped_gemm
+    rng = np.random.default_rng(77)
+    G, N, K = 64, 1024, 768
+    loads = rng.integers(1, 1500, G)
+    off = np.concatenate([[0], np.cumsum(loads)]).astype(np.int32)
+    T = int(off[-1])
+    x = _block_varying(inputs.activations(T, K, seed=78), K, seed=79)
+    w = inputs.gaussian((G * N, K), 0.02, seed=80)
+    qa, sa = orc.quantize_1x128(x)
+    qw, sw = orc.quantize_128x128(w)
+    sw = sw.reshape(G, N // 128, K // 128)
+    A_o = orc.operand(qa, orc.E4M3, orc.GRAN_1x128, sa)
+    B_o = orc.operand(qw, orc.E4M3, orc.GRAN_128x128, sw)
+    A_d = fp8.operand(dev(qa), dev(sa))
+    B_d = fp8.operand(dev(qw), dev(sw), gran=fp8.GRAN_128x128)
+    offd = dev(off)
+    ys = [fp8.fp8_grouped_block_gemm(offd, A_d, B_d, T, N, K, fp8.OUT_BF16) for _ in range(8)]
+    fp8.device_status()
+    for i in range(1, 8):
+        assert torch.equal(ys[i], ys[0]), f"launch {i} differs from launch 0"
+    cols = stratified(N, 128, rng, extra=(N - 1,))
+    rows = np.arange(T)
+    y_ref, yabs = par_grouped_gemm(orc, off, T, N, K, A_o, B_o, rows, cols)
+    _check(ys[0], y_ref, yabs, fp8.OUT_BF16, rows=rows, cols=cols)
+
+
+@pytest.mark.parametrize("M", [4096, 4093])
+def test_repeated_dense_runs_are_identical_and_match_the_oracle(M):
+    """A dense product with several tiles per CTA and 48 K blocks, with the
+    1x128 scale table aligned (copied by the producer) and, for M = 4093,
+    not (staged by the scale warp's own loads): eight launches give
+    bit-identical outputs; sampled rows and columns match the oracle."""
+    import torch
+    from helpers import par_gemm
+    rng = np.random.default_rng(M)
+    N, K = 2048, 6144
+    x = _block_varying(inputs.activations(M, K, seed=81), K, seed=82)
+    w = inputs.gaussian((N, K), 0.02, seed=83)
+    qa, sa = orc.quantize_1x128(x)
+    qw, sw = orc.quantize_128x128(w)
+    A_o = orc.operand(qa, orc.E4M3, orc.GRAN_1x128, sa)
+    B_o = orc.operand(qw, orc.E4M3, orc.GRAN_128x128, sw)
+    A_d = fp8.operand(dev(qa), dev(sa))
+    B_d = fp8.operand(dev(qw), dev(sw), gran=fp8.GRAN_128x128)
+    ys = [fp8.fp8_block_gemm(A_d, B_d, M, N, K, fp8.OUT_BF16) for _ in range(8)]
+    fp8.device_status()
+    for i in range(1, 8):
+        assert torch.equal(ys[i], ys[0]), f"launch {i} differs from launch 0"
+    rows = stratified(M, 128, rng, extra=(M - 1,))
+    cols = stratified(N, 128, rng, extra=(N - 1,))
+    y_ref, yabs = par_gemm(orc, M, N, K, A_o, B_o, rows, cols)
+    _check(ys[0], y_ref, yabs, fp8.OUT_BF16, rows=rows, cols=cols)

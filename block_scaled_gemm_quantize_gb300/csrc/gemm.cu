@@ -114,13 +114,13 @@ constexpr uint32_t XCHG_BYTES = 2 * 2 * 128 * 4;
 
 // Shared memory of k_fp8_gemm: [align pad][A ring][B ring][barriers][tmem
 // addr][group tables][output slabs][SwiGLU exchange][B-scale ring], for S
-// operand stages and SUBS output sub-slabs per epilogue warp.  With four
-// sub-slabs a tile's four store passes never wait for an earlier pass's
-// store to finish reading its slab; the plain K-major kernel (the promotion
-// products) gives up one operand stage for them, as its K blocks are paced by
-// the promotion rather than by the loads.  The kernels that accumulate the
-// whole K in TMEM (MN-major, per-tensor scales) and the SwiGLU / per-column-B
-// epilogues keep four stages.
+// operand stages and SUBS output sub-slabs per epilogue warp.  A K block
+// waits for its operand tiles about four blocks' time (their copy latency),
+// so four stages keep the MMA fed; with one sub-slab a tile's store passes
+// wait in turn for the previous pass's store to read the slab.  Products
+// with few K blocks per tile (at most SHORT_K_BLOCKS) store a tile every few
+// blocks: their kernel keeps three stages and four sub-slabs, so a tile's
+// four store passes never wait.
 template <int S, int SUBS>
 struct GemmLayout {
     static constexpr int kStages = S;
@@ -137,8 +137,9 @@ struct GemmLayout {
     static constexpr uint32_t kSmemBytes = 1024 + kBsfOff + BSF_SLOTS * BSF_SLOT_BYTES;
     static_assert(kSmemBytes <= 232448, "shared memory budget");
 };
-template <bool A_MN, bool B_MN, bool SWIGLU, bool B_COL>
-using GemmLayoutFor = GemmLayout<STAGES, 1>;
+constexpr int SHORT_K_BLOCKS = 16;
+template <bool SHORT_K>
+using GemmLayoutFor = GemmLayout<SHORT_K ? STAGES - 1 : STAGES, SHORT_K ? 4 : 1>;
 
 __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
     if (mbar_try_wait(bar, parity)) return true;
@@ -419,7 +420,7 @@ __device__ __forceinline__ bool finish_tile(const GemmParams& p, const CUtensorM
     return true;
 }
 
-template <bool A_MN, bool B_MN, bool SWIGLU, bool B_COL, int H>
+template <bool A_MN, bool B_MN, bool SWIGLU, bool B_COL, int H, bool SHORT_K = false>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     k_fp8_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                const __grid_constant__ CUtensorMap tmY, const GemmParams p) {
@@ -430,7 +431,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     uint8_t* smem = smem_raw + ((1024u - (raw & 1023u)) & 1023u);
     const uint32_t sbase = smem_u32(smem);
     const uint32_t sA = sbase;
-    using L = GemmLayoutFor<A_MN, B_MN, SWIGLU, B_COL>;
+    using L = GemmLayoutFor<SHORT_K>;
     constexpr int STAGES = L::kStages;
     const uint32_t sB = sbase + STAGES * A_STAGE;
     const uint32_t bars = sbase + L::kBarOff;
@@ -1326,13 +1327,15 @@ cudaError_t launch_fp8_gemm(const CUtensorMap& tmA, const CUtensorMap& tmB, cons
     // SwiGLU and per-column B scales run only on K-major operands (the host
     // checks it); the latter with BCOL_HALVES MMA slices per K block
     constexpr int h1 = HALVES, hb = BCOL_HALVES;
+    // (the plain K-major product with few K blocks per tile: three stages,
+    // four output sub-slabs)
+    const bool short_k = !p.swiglu && p.b_gran != 0 && !a_mn && !b_mn && p.K / BK <= SHORT_K_BLOCKS;
     auto k = p.swiglu ? k_fp8_gemm<false, false, true, false, h1>
              : p.b_gran == 0 ? k_fp8_gemm<false, false, false, true, hb>
              : a_mn ? (b_mn ? k_fp8_gemm<true, true, false, false, h1> : k_fp8_gemm<true, false, false, false, h1>)
-                    : (b_mn ? k_fp8_gemm<false, true, false, false, h1> : k_fp8_gemm<false, false, false, false, h1>);
-    const uint32_t smem = p.swiglu || p.b_gran == 0 || a_mn || b_mn
-                              ? GemmLayoutFor<true, false, false, false>::kSmemBytes
-                              : GemmLayoutFor<false, false, false, false>::kSmemBytes;
+             : b_mn ? k_fp8_gemm<false, true, false, false, h1>
+             : short_k ? k_fp8_gemm<false, false, false, false, h1, true> : k_fp8_gemm<false, false, false, false, h1>;
+    const uint32_t smem = short_k ? GemmLayoutFor<true>::kSmemBytes : GemmLayoutFor<false>::kSmemBytes;
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     k<<<grid, NUM_THREADS, smem, st>>>(tmA, tmB, tmY, p);

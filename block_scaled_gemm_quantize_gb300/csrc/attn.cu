@@ -124,6 +124,24 @@ __device__ __forceinline__ float ex2(float x) {
     return y;
 }
 
+__device__ __forceinline__ float lg2(float x) {
+    float y;
+    asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+// Largest V tile scale of kv head g (over all its key tiles), reduced across
+// the warp: P is scaled by sv_j / this maximum (at most 1) before it is
+// quantized, so the products of every key tile accumulate in one unit.
+__device__ __forceinline__ float head_max_sv(const float* sv, int64_t seq_k, int32_t hkv, int g, int lane) {
+    const int64_t nt = (seq_k + 127) / 128;
+    float m = 0.0f;
+    for (int64_t t = lane; t < nt; t += 32) m = fmaxf(m, __ldg(sv + t * hkv + g));
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
+    return m;
+}
+
 // number of 128-key tiles a CTA visits (0: no visible key for any of its rows)
 __device__ __forceinline__ int kv_tiles(const AttnParams& p, int64_t q0) {
     const int64_t n_all = (p.seq_k + AT_KEYS - 1) / AT_KEYS;
@@ -495,12 +513,16 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
 //                  query row holds the row's 128 scores (no exchange between
 //                  threads), the row max (reduced by the TMEM loads on fully
 //                  visible tiles), exp2, the row sum and the E4M3 codes of
-//                  448 P into a double-buffered, 128-byte-swizzled P buffer.
+//                  448 P (sv_j / svm) into a double-buffered, 128-byte-swizzled
+//                  P buffer, svm the head's largest V tile scale: the factor
+//                  is a shift of the exponent, so every tile's P V product
+//                  lands in O_X in the unit of svm, and the row sum takes P
+//                  unscaled.
 //   warps 12-15    O correction, one thread per row of both tiles: before
-//                  O_X(j) accumulates, O_X *= alpha_j sv_{j-1} / sv_j (running-max
-//                  factor and the V tile scales: O_X then holds the sum scaled
-//                  by 1 / sv_j), read from and written back to TMEM; at the end
-//                  O = O_X sv_last / l in bf16.
+//                  O_X(j) accumulates, O_X *= alpha_j (the running-max factor),
+//                  read from and written back to TMEM -- only when a row of
+//                  the warp changed its maximum; at the end O = O_X svm / l in
+//                  bf16.
 constexpr int A2_THREADS = 512;
 constexpr uint32_t A2_Q_OFF = 0;                                  // Q_A, Q_B
 constexpr uint32_t A2_KV_OFF = 2 * AT_TILE;                       // stage s: K +0, V +16 KiB
@@ -515,9 +537,9 @@ constexpr uint32_t A2_L_OFF = A2_ALPHA_OFF + 2 * 4 * 128 * 4;           // [X][1
 constexpr uint32_t A2_SMEM_BYTES = 1024 + A2_L_OFF + 2 * 128 * 4;
 static_assert(A2_SMEM_BYTES <= 232448, "shared memory budget (attention, two tiles)");
 // registers: 128 / thread at launch; control warps 48 and correction warps
-// 96 (both decreases), softmax 184 (an increase, 128 scores per row):
-// 128 * 48 + 256 * 184 + 128 * 96 == 512 * 128
-constexpr int A2_REGS_LOW = 48, A2_REGS_SM = 184, A2_REGS_CO = 96;
+// 80 (both decreases), softmax 192 (an increase, 128 scores per row):
+// 128 * 48 + 256 * 192 + 128 * 80 == 512 * 128
+constexpr int A2_REGS_LOW = 48, A2_REGS_SM = 192, A2_REGS_CO = 80;
 static_assert(128 * A2_REGS_LOW + 256 * A2_REGS_SM + 128 * A2_REGS_CO == 512 * 128, "register split");
 static_assert(A2_REGS_LOW <= 128 && A2_REGS_CO <= 128 && A2_REGS_SM >= 128, "setmaxnreg directions");
 
@@ -689,11 +711,24 @@ __global__ void __launch_bounds__(A2_THREADS, 1)
         float m = -INFINITY, l = 0.0f;   // l: the row's sum of 448 P
         bool ok = true;
         auto ksc = [&](int t) { return t < nx ? __ldg(p.sk + static_cast<int64_t>(t) * p.hkv + g) : 0.0f; };
-        float skw = 0.0f;   // K tile scales: lane i holds tile 32 w + i of window w
+        auto vsc = [&](int t) { return t < nx ? __ldg(p.sv + static_cast<int64_t>(t) * p.hkv + g) : 0.0f; };
+        const float svm = head_max_sv(p.sv, p.seq_k, p.hkv, g, lane);
+        const float lg_svm = svm > 0.0f ? lg2(svm) : 0.0f;
+        float skw = 0.0f, svw = 0.0f;   // K / V tile scales: lane i holds tile 32 w + i of window w
         for (int j = 0; ok && j < nx; j++) {
             const int b = j & 1;
-            if ((j & 31) == 0) skw = ksc(j + lane);
+            if ((j & 31) == 0) {
+                skw = ksc(j + lane);
+                svw = vsc(j + lane);
+            }
             const float sk_j = __shfl_sync(0xFFFFFFFFu, skw, j & 31);
+            const float sv_j = __shfl_sync(0xFFFFFFFFu, svw, j & 31);
+            // P of this tile scaled by sv_j / svm = 2^lv (a shift of the
+            // exponent); its row sum is taken back by 2^-lv.  lv >= -60: a
+            // zero (or smaller) scale still gives zero codes (448 P 2^-60 is
+            // below half the least E4M3 subnormal) and an exact fp32 row sum.
+            const float lv = fmaxf(lg2(sv_j) - lg_svm, -60.0f);
+            const float inv_lv = ex2(-lv);
             ok = __all_sync(0xFFFFFFFFu, at_wait(s_full(x), j & 1u));
             if (!ok) break;
             tc_fence_after();
@@ -731,8 +766,8 @@ __global__ void __launch_bounds__(A2_THREADS, 1)
             float tmax = fmaxf(fmaxf(tm[0], tm[1]), fmaxf(tm[2], tm[3]));
             tmax = tmax == -INFINITY ? -INFINITY : tmax * c;
             const float m_new = fmaxf(m, tmax);
-            const float alpha = m_new == -INFINITY ? 1.0f : ex2(m - m_new);
-            const float shift = AT_LOG2_448 - (m_new == -INFINITY ? 0.0f : m_new);
+            const float alpha = (m_new == -INFINITY || m_new == m) ? 1.0f : ex2(m - m_new);
+            const float shift = AT_LOG2_448 + lv - (m_new == -INFINITY ? 0.0f : m_new);
             // P_X's buffer b is free once O_X(j - 2) has completed
             ok = __all_sync(0xFFFFFFFFu, at_wait(p_empty(x, b), ((j >> 1) & 1u) ^ 1u));
             if (!ok) break;
@@ -769,7 +804,7 @@ __global__ void __launch_bounds__(A2_THREADS, 1)
                              w[2], w[3]);
             }
             float2 q0 = unpack_f32x2(rs[0]), q1 = unpack_f32x2(rs[1]), q2 = unpack_f32x2(rs[2]), q3 = unpack_f32x2(rs[3]);
-            const float rsum = ((q0.x + q1.x) + (q2.x + q3.x)) + ((q0.y + q1.y) + (q2.y + q3.y));
+            const float rsum = (((q0.x + q1.x) + (q2.x + q3.x)) + ((q0.y + q1.y) + (q2.y + q3.y))) * inv_lv;
             fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) mbar_arrive(p_full(x, b));
@@ -782,56 +817,53 @@ __global__ void __launch_bounds__(A2_THREADS, 1)
         __syncwarp();
         if (lane == 0) mbar_arrive(l_full(x));
     } else {
-        // (96 is below the launch's 128: a decrease)
+        // (80 is below the launch's 128: a decrease)
         asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(A2_REGS_CO));
         // ------------------------------------------------- O correction
         const int quarter = warp & 3;
         const int r = quarter * 32 + lane;
         const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
         bool ok = true;
-        auto vsc = [&](int t) { return t < n ? __ldg(p.sv + static_cast<int64_t>(t) * p.hkv + g) : 1.0f; };
-        float svw = 0.0f, sv_prev = 1.0f, sv_j = 1.0f;   // V tile scales (window of 32 across the lanes)
+        const float svm = head_max_sv(p.sv, p.seq_k, p.hkv, g, lane);
         for (int j = 0; ok && j < n; j++) {
-            if ((j & 31) == 0) svw = vsc(j + lane);
-            sv_prev = sv_j;
-            sv_j = __shfl_sync(0xFFFFFFFFu, svw, j & 31);
 #pragma unroll
             for (int x = 0; x < 2; x++) {
                 if (j >= (x ? nB : nA)) continue;
                 ok = __all_sync(0xFFFFFFFFu, at_wait(a_full(x, j & 3), (j >> 2) & 1u));
                 if (!ok) break;
-                const float alpha = ld_shared_f32(sbase + A2_ALPHA_OFF + ((x * 4 + (j & 3)) * 128 + r) * 4);
-                if (j > 0) {
-                    const float f = alpha * __fdiv_rn(sv_prev, sv_j);
+                // O_X holds its sum in the unit of the largest V scale, so only
+                // the running-max factor rescales it; while no row of this warp
+                // changed its maximum, O_X(j) may follow O_X(j - 1) unwaited (the
+                // products of one accumulator run in order)
+                const float f = ld_shared_f32(sbase + A2_ALPHA_OFF + ((x * 4 + (j & 3)) * 128 + r) * 4);
+                if (j > 0 && __any_sync(0xFFFFFFFFu, f != 1.0f)) {
                     ok = __all_sync(0xFFFFFFFFu, at_wait(o_done(x), (j - 1) & 1u));   // O_X(j-1) complete
                     if (!ok) break;
                     tc_fence_after();
-                    if (__any_sync(0xFFFFFFFFu, f != 1.0f)) {
-                        const uint64_t f2 = pack_f32x2(__float_as_uint(f), __float_as_uint(f));
-                        const uint32_t ta = tmem + lane_off + 256 + x * 128;
+                    const uint64_t f2 = pack_f32x2(__float_as_uint(f), __float_as_uint(f));
+                    const uint32_t ta = tmem + lane_off + 256 + x * 128;
 #pragma unroll
-                        for (int u = 0; u < 4; u++) {
-                            uint32_t rr[32];
-                            tmem_ld_32x32b_x32(ta + u * 32, rr);
-                            tmem_wait_ld();
+                    for (int u = 0; u < 4; u++) {
+                        uint32_t rr[32];
+                        tmem_ld_32x32b_x32(ta + u * 32, rr);
+                        tmem_wait_ld();
 #pragma unroll
-                            for (int q = 0; q < 16; q++) {
-                                const uint64_t v = mul_f32x2(pack_f32x2(rr[2 * q], rr[2 * q + 1]), f2);
-                                const float2 fv = unpack_f32x2(v);
-                                rr[2 * q] = __float_as_uint(fv.x);
-                                rr[2 * q + 1] = __float_as_uint(fv.y);
-                            }
-                            tmem_st_32x32b_x32(ta + u * 32, rr);
+                        for (int q = 0; q < 16; q++) {
+                            const uint64_t v = mul_f32x2(pack_f32x2(rr[2 * q], rr[2 * q + 1]), f2);
+                            const float2 fv = unpack_f32x2(v);
+                            rr[2 * q] = __float_as_uint(fv.x);
+                            rr[2 * q + 1] = __float_as_uint(fv.y);
                         }
-                        tmem_wait_st();
+                        tmem_st_32x32b_x32(ta + u * 32, rr);
                     }
+                    tmem_wait_st();
                     tc_fence_before();
                 }
                 __syncwarp();
                 if (lane == 0) mbar_arrive(corr_done(x));
             }
         }
-        // O = O_X sv_last / l, bf16
+        // O = O_X svm / l, bf16
 #pragma unroll
         for (int x = 0; x < 2; x++) {
             const int nx = x ? nB : nA;
@@ -845,8 +877,7 @@ __global__ void __launch_bounds__(A2_THREADS, 1)
                 if (!ok) break;
                 tc_fence_after();
                 const float l = ld_shared_f32(sbase + A2_L_OFF + (x * 128 + r) * 4);
-                const float sv_last = __ldg(p.sv + static_cast<int64_t>(nx - 1) * p.hkv + g);
-                scale = l > 0.0f ? sv_last / l : 0.0f;
+                scale = l > 0.0f ? svm / l : 0.0f;
                 have = true;
             }
             if (!ok) break;

@@ -473,7 +473,8 @@ def attention(seq_q: int, seq_k: int, hq: int, hkv: int, causal: bool, scale: fl
     q: [seq_q, hq*128] codes, sq: [hq, seq_q] (1x128 scales); k, v: [seq_k, hkv*128]
     codes, sk, sv: [ceil(seq_k/128), hkv] (128x128 scales).  rows/heads select
     (row, head) pairs (default: all).  Returns (o, oap, oav) of shape [n, 128]:
-    the output, sum_j P|V|/l and sum_j |V|/l."""
+    the output, sum_j P|V|/l and sum_j |V code| svm / l (svm: the head's
+    largest V tile scale; see the acceptance rule below)."""
     q = np.ascontiguousarray(q, dtype=np.uint8)
     k = np.ascontiguousarray(k, dtype=np.uint8)
     v = np.ascontiguousarray(v, dtype=np.uint8)
@@ -498,13 +499,17 @@ def attention(seq_q: int, seq_k: int, hq: int, hkv: int, causal: bool, scale: fl
 
 
 # Acceptance rule of the FP8 attention output.  The kernel quantizes the
-# softmax numerators P (in [0, 1] after the running-max subtraction) to E4M3
-# with the scale 1/448 (amax 1 by construction), so each P carries a rounding
-# error of at most 2^-4 P (normal range) or 2^-10 / 448 (subnormal range);
-# the row sum l uses the unrounded values.  Hence per output element
-#   |o - o_ref| <= (2^-4 + 1e-4) sum_j P_j |V_j| / l + (2^-10 / 448) sum_j |V_j| / l
+# softmax numerators P (in [0, 1] after the running-max subtraction), each
+# times sv_t / svm (its key tile's V scale over the head's largest, at most
+# 1), to E4M3 with the scale 1/448, so each carries a rounding error of at
+# most 2^-4 P (normal range) or 2^-10 / 448 * svm / sv_t in P units
+# (subnormal range); the row sum l uses the unrounded values.  Hence per
+# output element
+#   |o - o_ref| <= (2^-4 + 1e-4) sum_j P_j |V_j| / l
+#                  + (2^-10 / 448) sum_j |V_j| (svm / sv_t(j)) / l
 #                  + 1e-5 |o_ref|   (fp32 scores, exp2, accumulation)
-# plus half a bf16 unit of the stored value.
+# plus half a bf16 unit of the stored value; the attention oracle returns the
+# second sum as oav.
 ATTN_P_REL = 2.0 ** -4 + 1e-4
 ATTN_P_ABS = 2.0 ** -10 / 448.0
 

@@ -460,7 +460,11 @@ int fp8o_grouped_gemm(int32_t G, const int32_t* off, int64_t a_rows, int64_t N, 
  *   P_ij = exp(S_ij - max_j S_ij), l_i = sum_j P_ij
  *   O[i][h][d] = sum_j P_ij deqV[j][g][d] / l_i
  * and, for the tolerance, oap[i][h][d] = sum_j P_ij |deqV| / l_i and
- * oav[i][h][d] = sum_j |deqV| / l_i, all in fp64.
+ * oav[i][h][d] = sum_j |deqV| (svm_g / sv_t(j)) / l_i = sum_j |V code| svm_g
+ * / l_i, all in fp64, where sv_t(j) is key j's V tile scale and svm_g the
+ * largest V tile scale of kv head g (the kernel quantizes P times sv_t / svm_g,
+ * so the absolute error of a subnormal P code, read back in P units, grows by
+ * svm_g / sv_t).
  * q: [seq_q][hq][128] codes, sq: [hq][seq_q] (1x128 table of the [seq_q][hq*128]
  * matrix); k, v: [seq_k][hkv][128] codes, sk, sv: [ceil(seq_k/128)][hkv].
  * Selected (row, head) pairs: rows[n], heads[n].  Output [n][128]. */
@@ -483,6 +487,9 @@ int fp8o_attention(int64_t seq_q, int64_t seq_k, int32_t hq, int32_t hkv, int ca
         if (i < 0 || i >= seq_q || h < 0 || h >= hq) { free(sc); return -1; }
         int32_t g = h / (hq / hkv);
         double qs = sq[(int64_t)h * seq_q + i];
+        double svm = 0.0;
+        for (int64_t tt = 0; tt < (seq_k + 127) / 128; tt++)
+            if (sv[tt * hkv + g] > svm) svm = sv[tt * hkv + g];
         int64_t jend = causal ? i + (seq_k - seq_q) + 1 : seq_k;
         if (jend > seq_k) jend = seq_k;
         double m = -INFINITY;
@@ -501,7 +508,7 @@ int fp8o_attention(int64_t seq_q, int64_t seq_k, int32_t hq, int32_t hkv, int ca
                 double vv = lv[v[(j * hkv + g) * D + d]] * sv[(j / 128) * hkv + g];
                 a += sc[j] * vv;
                 ap += sc[j] * fabs(vv);
-                av += fabs(vv);
+                av += fabs(lv[v[(j * hkv + g) * D + d]]) * svm;
             }
             o[t * D + d] = jend > 0 ? a / l : 0.0;
             oap[t * D + d] = jend > 0 ? ap / l : 0.0;

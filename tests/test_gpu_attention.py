@@ -15,10 +15,20 @@ pytestmark = pytest.mark.gpu
 SCALE = 128 ** -0.5
 
 
-def _inputs(S_q, S_k, hq, hkv, seed, zero_k=False):
+def _inputs(S_q, S_k, hq, hkv, seed, zero_k=False, v_tile_gain=None):
+    """v_tile_gain: per 128-key tile factors applied to V (0 = a tile of
+    zeros), or "equal": each tile's first key set to 8 in every element, so
+    every V tile of a head gets the same scale."""
     q = inputs.gaussian((S_q, hq * 128), 1.0, seed=seed)
     k = inputs.gaussian((max(S_k, 1), hkv * 128), 1.0, seed=seed + 1)[:S_k]
     v = inputs.gaussian((max(S_k, 1), hkv * 128), 1.0, seed=seed + 2)[:S_k]
+    if v_tile_gain is not None and S_k:
+        vf = inputs.bits_to_f32(v).astype(np.float64)
+        if isinstance(v_tile_gain, str):
+            vf[::128] = 8.0
+        else:
+            vf *= np.repeat(np.asarray(v_tile_gain, np.float64), 128)[:S_k, None]
+        v = inputs.bf16_bits(vf.astype(np.float32))
     qq, sq = orc.quantize_1x128(q)
     kq, sk = orc.quantize_128x128(k) if S_k else (np.zeros((0, hkv * 128), np.uint8), np.ones((1, hkv), np.float32))
     vq, sv = orc.quantize_128x128(v) if S_k else (np.zeros((0, hkv * 128), np.uint8), np.ones((1, hkv), np.float32))
@@ -65,9 +75,13 @@ def test_attention_more_than_32_key_tiles(causal):
 
 
 def test_attention_equal_scores_give_the_mean_of_the_visible_values():
+    """All keys equal and every V tile of the head at the same scale: each
+    visible P is exactly 448 in E4M3 (P is scaled by its tile's V scale over
+    the head's largest, here 1), so the output is the plain mean."""
     import torch
     S, hq, hkv = 384, 2, 1
-    arrs = _inputs(S, S, hq, hkv, seed=7, zero_k=True)
+    arrs = _inputs(S, S, hq, hkv, seed=7, zero_k=True, v_tile_gain="equal")
+    assert np.all(arrs[5] == arrs[5][0])
     o_bits = _run(S, S, hq, hkv, True, arrs)
     o = torch.from_numpy(o_bits.view(np.int16)).view(torch.bfloat16).to(torch.float64).numpy()
     ref, _, _ = orc.attention(S, S, hq, hkv, True, SCALE, *arrs)
@@ -92,3 +106,21 @@ def test_attention_llama31_8b_prefill_sampled():
     heads = rng.integers(0, hq, rows.size)
     ref = orc.attention(S, S, hq, hkv, True, SCALE, *arrs, rows=rows, heads=heads)
     _check(o_bits[rows * hq + heads], ref)
+
+
+@pytest.mark.parametrize("zero_scale", [False, True])
+@pytest.mark.parametrize("causal", [False, True])
+def test_attention_v_tiles_with_very_different_scales_and_a_zero_tile(causal, zero_scale):
+    """V tiles scaled by 1 .. 2^-12 and one tile of zeros (its scale as the
+    quantizer gives it, 1, which then is the head's largest; or 0): P is
+    quantized after the factor sv_t / (largest V scale of the head), so
+    small-scale tiles lose precision only in the subnormal range the bound
+    allows; the zero tile contributes nothing (its keys still count in the
+    row sum)."""
+    S_q, S_k, hq, hkv = 256, 896, 2, 2
+    gains = [1.0, 2.0 ** -4, 0.0, 2.0 ** -12, 0.5, 2.0 ** -8, 1.0]
+    arrs = _inputs(S_q, S_k, hq, hkv, seed=91, v_tile_gain=gains)
+    if zero_scale:
+        arrs[5][2] = 0.0
+    o_bits = _run(S_q, S_k, hq, hkv, causal, arrs)
+    _check(o_bits, orc.attention(S_q, S_k, hq, hkv, causal, SCALE, *arrs))

@@ -142,12 +142,16 @@ __device__ __forceinline__ void quant_128x128_tile(const uint16_t* __restrict__ 
     const int64_t kb = tile - rb * nkb;
     const int c = threadIdx.x & 15;
     const int r0 = threadIdx.x >> 4;
+    // rows r0 + 16 i of the tile that exist (the last row-tile may be ragged)
+    const int64_t left = rows - (rb * 128 + r0);
+    const int nrow = left <= 0 ? 0 : (left >= 113 ? 8 : static_cast<int>((left + 15) / 16));
+    const uint16_t* src = w + (rb * 128 + r0) * ldw + kb * 128 + c * 8;
+    const int64_t step = 16 * ldw;
     uint4 v[8];
 #pragma unroll
     for (int i = 0; i < 8; i++) {
-        const int64_t row = rb * 128 + r0 + 16 * i;
         v[i] = make_uint4(0, 0, 0, 0);
-        if (row < rows) v[i] = ld_stream_v4(w + row * ldw + kb * 128 + c * 8);
+        if (i < nrow) v[i] = ld_stream_v4(src + i * step);
     }
     float m = 0.0f;
 #pragma unroll
@@ -165,15 +169,16 @@ __device__ __forceinline__ void quant_128x128_tile(const uint16_t* __restrict__ 
     for (int i = 1; i < 8; i++) m = fmaxf(m, red[i]);
     const float s = block_scale<FMT, MODE>(m);
     const float r = __frcp_rn(s);
+    uint8_t* dst = q + (rb * 128 + r0) * ldq + kb * 128 + c * 8;
+    const int64_t qstep = 16 * ldq;
 #pragma unroll
     for (int i = 0; i < 8; i++) {
-        const int64_t row = rb * 128 + r0 + 16 * i;
-        if (row < rows) {
+        if (i < nrow) {
             float f[8];
             unpack8(v[i], f);
             uint32_t lo, hi;
             quant8<FMT>(f, r, lo, hi);
-            st_v2(q + row * ldq + kb * 128 + c * 8, lo, hi);
+            st_v2(dst + i * qstep, lo, hi);
         }
     }
     if (threadIdx.x == 0) scales[rb * nkb + kb] = s;

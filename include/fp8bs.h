@@ -353,9 +353,11 @@ typedef struct {
  * attention operations).  Both products run on the FP8 tensor cores:
  *   S = scale * deq(Q_h) deq(K_g)^T, masked (causal: key j visible to query
  *       i iff j <= i + seq_k - seq_q), g = h / (heads_q / heads_kv);
- *   P = exp(S - running row max) in fp32, quantized to E4M3 with the scale
- *       1/448 (its maximum is 1), row sums l from the unrounded values;
- *   O = (P deq(V_g)) / l, accumulated in fp32, stored as bf16.
+ *   P = exp(S - running row max) in fp32; P times (its key tile's V scale /
+ *       the largest V tile scale of head g), at most 1, quantized to E4M3
+ *       with the scale 1/448; row sums l from the unrounded, unscaled values;
+ *   O = (P deq(V_g)) / l, accumulated in fp32 in the unit of that largest V
+ *       scale, stored as bf16.
  * Scales (readings; the pages give none): Q one per token and head, as the
  * 1x128 activation tiles -- fp8_quantize_1x128 of the [seq_q][heads_q * 128]
  * matrix, table [heads_q][seq_q]; K and V (the KV cache) one per 128 tokens

@@ -84,17 +84,6 @@ __device__ __forceinline__ void tma_store_2d(const void* tmap, uint32_t src, int
         "r"(x), "r"(y), "r"(src)
         : "memory");
 }
-// 4-byte asynchronous copy global -> shared; a thread's copies complete in
-// the order of its commit groups (cp_async_wait<N>: all but the last N).
-__device__ __forceinline__ void cp_async_4(uint32_t dst, const void* src) {
-    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(dst), "l"(reinterpret_cast<uint64_t>(src))
-                 : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-template <int N>
-__device__ __forceinline__ void cp_async_wait() {
-    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
-}
 
 __device__ __forceinline__ void bulk_commit_group() {
     asm volatile("cp.async.bulk.commit_group;" ::: "memory");

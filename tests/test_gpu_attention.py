@@ -57,11 +57,16 @@ def _check(o_bits, ref):
 
 
 @pytest.mark.parametrize("causal", [False, True])
-@pytest.mark.parametrize("S_q,S_k,hq,hkv", [(300, 384, 4, 2), (256, 256, 4, 1), (200, 456, 2, 2), (130, 130, 8, 8)])
+@pytest.mark.parametrize("S_q,S_k,hq,hkv", [(300, 384, 4, 2), (256, 256, 4, 1), (200, 456, 2, 2), (130, 130, 8, 8),
+                                             # more queries than keys: causal rows below
+                                             # seq_q - seq_k see no key (whole tiles of them)
+                                             (400, 200, 2, 1), (300, 130, 4, 2)])
 def test_attention_small(causal, S_q, S_k, hq, hkv):
     arrs = _inputs(S_q, S_k, hq, hkv, seed=S_q + S_k)
     o_bits = _run(S_q, S_k, hq, hkv, causal, arrs)
     _check(o_bits, orc.attention(S_q, S_k, hq, hkv, causal, SCALE, *arrs))
+    if causal and S_q > S_k:   # rows that see no key are 0
+        assert np.all(o_bits[: (S_q - S_k) * hq] == 0)
 
 
 @pytest.mark.parametrize("causal", [False, True])

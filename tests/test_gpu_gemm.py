@@ -301,6 +301,46 @@ def test_grouped_more_than_32_groups():
     assert np.all(np.isnan(yh[T:]))
 
 
+def test_grouped_maximum_group_count():
+    """1024 groups, the most one call takes (empty, 1-row and multi-slot groups;
+    the device prefix of m-slots spans 32 chunks), sampled rows of every group
+    and all columns; rows past the last group stay untouched."""
+    import torch
+    from helpers import par_grouped_gemm
+    rng = np.random.default_rng(51)
+    loads = rng.integers(0, 200, 1024)
+    loads[rng.choice(1024, 100, replace=False)] = 0
+    loads[rng.choice(1024, 50, replace=False)] = 1
+    N, K = 256, 256
+    off, T, a_rows, qa, sa, qw, sw = _grouped_operands(loads, N, K, seed=53, extra_rows=3)
+    rows = np.unique(np.concatenate([off[:-1][loads > 0], off[1:][loads > 0] - 1,
+                                     rng.integers(0, T, 2000)]))
+    A_o = orc.operand(qa, orc.E4M3, orc.GRAN_1x128, sa)
+    B_o = orc.operand(qw, orc.E4M3, orc.GRAN_128x128, sw)
+    y_ref, yabs = par_grouped_gemm(orc, off, a_rows, N, K, A_o, B_o, rows, np.arange(N))
+    y = torch.full((a_rows, N), float("nan"), device="cuda")
+    fp8.fp8_grouped_block_gemm(dev(off), fp8.operand(dev(qa), dev(sa)),
+                               fp8.operand(dev(qw), dev(sw), gran=fp8.GRAN_128x128),
+                               a_rows, N, K, fp8.OUT_F32, y=y)
+    fp8.device_status()
+    yh = host(y)
+    _check(y, y_ref, yabs, fp8.OUT_F32, rows, np.arange(N))
+    assert np.all(np.isnan(yh[T:]))
+
+
+def test_grouped_all_groups_empty_writes_nothing():
+    import torch
+    loads = np.zeros(5, np.int64)
+    N, K = 256, 128
+    off, T, a_rows, qa, sa, qw, sw = _grouped_operands(loads, N, K, seed=57, extra_rows=7)
+    y = torch.full((a_rows, N), float("nan"), device="cuda")
+    fp8.fp8_grouped_block_gemm(dev(off), fp8.operand(dev(qa), dev(sa)),
+                               fp8.operand(dev(qw), dev(sw), gran=fp8.GRAN_128x128),
+                               a_rows, N, K, fp8.OUT_F32, y=y)
+    fp8.device_status()
+    assert T == 0 and np.all(np.isnan(host(y)))
+
+
 def test_grouped_decreasing_offsets_are_reported_and_nothing_is_written():
     """A decreasing offset table would give overlapping groups (two tiles
     writing the same rows).  The kernel writes nothing and the device status

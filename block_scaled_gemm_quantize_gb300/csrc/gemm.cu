@@ -126,8 +126,9 @@ struct GemmLayout {
     static constexpr int kStages = S;
     static constexpr int kSubs = SUBS;
     static constexpr uint32_t kBarOff = S * STAGE_BYTES;
-    // full, empty, tfull, tempty, done, xchg[4], bsf_full, bsf_empty
-    static constexpr int kNumBars = 2 * S + 2 * MAX_TBUFS + 1 + 4 + 2 * BSF_SLOTS;
+    // full, empty, tfull, tempty, done, xchg[4], bsf_full, bsf_empty,
+    // st_full[8], st_free[8]
+    static constexpr int kNumBars = 2 * S + 2 * MAX_TBUFS + 1 + 4 + 2 * BSF_SLOTS + 2 * NUM_EPI_WARPS;
     static constexpr uint32_t kTmemSlotOff = kBarOff + kNumBars * 8;
     static constexpr uint32_t kTableOff = (kTmemSlotOff + 16 + 15) & ~15u;
     static constexpr uint32_t kSlab = SUBS * OUT_SUB;
@@ -193,6 +194,28 @@ __device__ __forceinline__ float ld_scale_ordered(const float* p) {
     float v;
     asm volatile("ld.global.nc.f32 %0, [%1];" : "=f"(v) : "l"(p) : "memory");
     return v;
+}
+
+// One warp's 32 rows x 128 columns of a finished tile as bf16 into its four
+// 2 KiB sub-slabs (32 rows x 64 B each, 64-B swizzle: 16-B chunk c of row r
+// at chunk c ^ (r/2)%4), the layout the output tensor map's TMA store reads.
+__device__ __forceinline__ void stage_tile_bf16(const uint64_t (&acc)[64], uint32_t slab, int lane) {
+    const uint32_t sw = (lane >> 1) & 3;
+#pragma unroll
+    for (int ps = 0; ps < 4; ps++) {
+        const uint32_t rbase = slab + static_cast<uint32_t>(ps) * OUT_SUB + lane * 64;
+#pragma unroll
+        for (int c = 0; c < 4; c++) {
+            uint32_t w[4];
+#pragma unroll
+            for (int i = 0; i < 4; i++) {
+                const float2 f = unpack_f32x2(acc[ps * 16 + c * 4 + i]);
+                __nv_bfloat162 h = __floats2bfloat162_rn(f.x, f.y);
+                w[i] = *reinterpret_cast<uint32_t*>(&h);
+            }
+            st_shared_v4(rbase + ((c ^ sw) << 4), w[0], w[1], w[2], w[3]);
+        }
+    }
 }
 
 // Store one warp's 32 rows x 128 columns of a finished tile (acc = 128 fp32
@@ -445,6 +468,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     auto bsf_empty = [&](int q) { return bars + 8u * (2 * STAGES + 2 * MAX_TBUFS + 5 + BSF_SLOTS + q); };
     auto sr_ready = [&](int q) { return bsf_full(q); };   // (promotion products) a scale-ring
     auto sr_free = [&](int q) { return bsf_empty(q); };   // slot landed / was read
+    // a bf16 block staged by epilogue warp w for the store warp / read out again
+    auto st_full = [&](int w) { return bars + 8u * (2 * STAGES + 2 * MAX_TBUFS + 5 + 2 * BSF_SLOTS + w); };
+    auto st_free = [&](int w) {
+        return bars + 8u * (2 * STAGES + 2 * MAX_TBUFS + 5 + 2 * BSF_SLOTS + NUM_EPI_WARPS + w);
+    };
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kTmemSlotOff);
     int* s_off = reinterpret_cast<int*>(smem + L::kTableOff);
     int* s_slot = s_off + (kMaxGroups + 1);
@@ -471,6 +499,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             mbar_init(bsf_full(q), 1);   // the loader's (promotion: the producer's) expect_tx arrival
             // one arrival per epilogue warp (promotion: per scale-warp lane)
             mbar_init(bsf_empty(q), B_COL ? NUM_EPI_WARPS : 32);
+        }
+        for (int w = 0; w < NUM_EPI_WARPS; w++) {
+            mbar_init(st_full(w), 1);
+            mbar_init(st_free(w), 1);
         }
         fence_mbar_init();
         fence_proxy_async_smem();
@@ -520,6 +552,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const int total_tiles = total_slots * p.tiles_n;
     const int nkb = static_cast<int>(p.K / BK);
     const int P = p.promote ? 1 : nkb;  // K blocks per TMEM partial
+    // Products with few K blocks per tile (four output sub-slabs per warp)
+    // and a plain bf16 output hand each finished block to warp 2, which
+    // issues its TMA stores: issuing them takes ~1000 cycles behind the
+    // operand copies in the TMA unit, time the epilogue warp now spends on
+    // the next tile.
+    const bool store_warp = !SWIGLU && !B_COL && L::kSubs == 4 && p.out_bf16 && !p.out_q && p.tma_store;
 
     if (warp < EPI_WARP0) {
       asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(REGS_LOW));
@@ -682,6 +720,46 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     wait_bounded(bsf_full(slot), ph, DRAIN_LIMIT_NS);
                 }
             }
+        }
+      } else if (warp == 2 && store_warp) {
+        // ------------------------------------------------- tile store issuer
+        // For every tile of this CTA and every epilogue warp whose 32 rows
+        // lie inside the tile's group (the others store directly): wait for
+        // the warp's staged block, issue its four TMA stores; once all of the
+        // tile's stores have read their slabs, hand the slabs back.
+        if (lane == 0) {
+            uint32_t cnt[NUM_EPI_WARPS];
+#pragma unroll
+            for (int w = 0; w < NUM_EPI_WARPS; w++) cnt[w] = 0;
+            bool ok = true;
+            for (int t = blockIdx.x; ok && t < total_tiles; t += gridDim.x) {
+                const Tile tl = decode_tile(t, total_slots, p.tiles_n, G, s_slot, s_off);
+                uint32_t used = 0;
+#pragma unroll
+                for (int w = 0; w < NUM_EPI_WARPS; w++) {
+                    const int64_t wrow0 = static_cast<int64_t>(tl.row0) + (w & 3) * 32;
+                    if (!ok || !(p.offsets == nullptr || wrow0 + 32 <= tl.row_end)) continue;
+                    if (!wait_or_flag(st_full(w), cnt[w] & 1u)) { ok = false; continue; }
+                    const uint32_t slab = sbase + L::kOutOff + w * L::kSlab;
+                    const int64_t col0 = static_cast<int64_t>(tl.nt) * BN + (w >> 2) * 128;
+#pragma unroll
+                    for (int ps = 0; ps < 4; ps++)
+                        tma_store_2d(&tmY, slab + static_cast<uint32_t>(ps) * OUT_SUB, static_cast<int32_t>(col0 + ps * 32),
+                                     static_cast<int32_t>(wrow0));
+                    bulk_commit_group();
+                    used |= 1u << w;
+                }
+                if (used) {
+                    bulk_wait_group_read0();   // the slabs have been read
+#pragma unroll
+                    for (int w = 0; w < NUM_EPI_WARPS; w++)
+                        if (used & (1u << w)) {
+                            mbar_arrive(st_free(w));
+                            cnt[w]++;
+                        }
+                }
+            }
+            bulk_wait_group0();   // every store has landed
         }
       } else if (!B_COL && warp == 3) {
         // ------------------------------------- scale warp (promotion products)
@@ -868,7 +946,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         // the gate part for columns 0-63, the up part for 64-127)
         const uint32_t s_off0 = (SWIGLU ? 0u : static_cast<uint32_t>(half) * 512u) + lrow * 4;
         const uint32_t s_off1 = SWIGLU ? 512u + lrow * 4 : s_off0;
-        uint32_t chunk = 0, tile_i = 0;
+        uint32_t chunk = 0, tile_i = 0, ntma = 0;
         bool ok = true;
         for (int t = blockIdx.x; ok && t < total_tiles; t += gridDim.x, tile_i++) {
             const Tile tl = decode_tile(t, total_slots, p.tiles_n, G, s_slot, s_off);
@@ -911,9 +989,25 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 }
             }
             if (!ok) break;
-            ok = finish_tile<SWIGLU>(p, tmY, acc, tl, row, row_ok, col0, quarter, half, lane,
-                             sbase + L::kOutOff + (warp - EPI_WARP0) * L::kSlab, sbase + L::kXchgOff,
-                             xchg_bar(quarter), tile_i & 1u, L::kSubs);
+            const int64_t wrow0 = static_cast<int64_t>(tl.row0) + quarter * 32;
+            if (store_warp && (p.offsets == nullptr || wrow0 + 32 <= tl.row_end)) {
+                // stage the bf16 block for the store warp once it has read the
+                // previous one out of this warp's slab
+                const int w = warp - EPI_WARP0;
+                if (ntma > 0) {
+                    ok = __all_sync(0xFFFFFFFFu, wait_or_flag(st_free(w), (ntma - 1) & 1u));
+                    if (!ok) break;
+                }
+                stage_tile_bf16(acc, sbase + L::kOutOff + w * L::kSlab, lane);
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(st_full(w));
+                ntma++;
+            } else {
+                ok = finish_tile<SWIGLU>(p, tmY, acc, tl, row, row_ok, col0, quarter, half, lane,
+                                 sbase + L::kOutOff + (warp - EPI_WARP0) * L::kSlab, sbase + L::kXchgOff,
+                                 xchg_bar(quarter), tile_i & 1u, L::kSubs);
+            }
         }
         if (lane == 0) bulk_wait_group0();   // every store of this warp has landed
     }

@@ -64,7 +64,15 @@ constexpr uint32_t B_STAGE = BN * BK;   // 32 KiB
 constexpr uint32_t STAGE_BYTES = A_STAGE + B_STAGE;
 constexpr int NUM_THREADS = 384;
 constexpr int EPI_WARP0 = 4;
-constexpr int REGS_LOW = 56, REGS_HIGH = 224;   // 128*56 + 256*224 == 384*168
+// setmaxnreg split of the 384 x 168 registers a CTA is launched with: the
+// four control warps and the eight epilogue warps.  The control warps
+// (producer, MMA, store / loader, scale warp) spill at 56 registers in most
+// instances, which costs 5-10 %; the SwiGLU and per-column-B epilogues need
+// the 224.
+constexpr int REGS_LOW = 64, REGS_HIGH = 216;         // 128*64 + 256*216 <= 384*168
+constexpr int REGS_LOW_WIDE = 56, REGS_HIGH_WIDE = 224;   // 128*56 + 256*224 == 384*168
+static_assert(128 * REGS_LOW + 256 * REGS_HIGH <= 384 * 168, "register split");
+static_assert(128 * REGS_LOW_WIDE + 256 * REGS_HIGH_WIDE <= 384 * 168, "register split");
 constexpr int NUM_EPI_WARPS = 8;
 constexpr uint32_t TMEM_COLS = 512;
 #ifndef FP8BS_RASTER_M
@@ -456,6 +464,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const uint32_t sA = sbase;
     using L = GemmLayoutFor<SHORT_K>;
     constexpr int STAGES = L::kStages;
+    constexpr bool WIDE_EPI = SWIGLU || B_COL;   // epilogues that need 224 registers
+    constexpr int R_LOW = WIDE_EPI ? REGS_LOW_WIDE : REGS_LOW;
+    constexpr int R_HIGH = WIDE_EPI ? REGS_HIGH_WIDE : REGS_HIGH;
     const uint32_t sB = sbase + STAGES * A_STAGE;
     const uint32_t bars = sbase + L::kBarOff;
     auto full_bar = [&](int s) { return bars + 8u * s; };
@@ -560,7 +571,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const bool store_warp = !SWIGLU && !B_COL && L::kSubs == 4 && p.out_bf16 && !p.out_q && p.tma_store;
 
     if (warp < EPI_WARP0) {
-      asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(REGS_LOW));
+      asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(R_LOW));
       if (warp == 0) {
         // ------------------------------------------------------ producer
         if (lane == 0) {
@@ -840,7 +851,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
       }
     } else if (B_COL) {
-        asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(REGS_HIGH));
+        asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(R_HIGH));
         // ------------------------------ epilogue with per-column B scales
         // Every (row, column) needs its own product sa[row] * sb[col], so the
         // scales are read from shared memory each K block.  To keep that
@@ -936,7 +947,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             }
         }
     } else {
-        asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(REGS_HIGH));
+        asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(R_HIGH));
         // ----------------------------------------------------- epilogue
         const int quarter = warp & 3;           // TMEM lanes 32*quarter ..
         const int half = (warp - EPI_WARP0) >> 2;  // columns 128*half ..
@@ -1054,7 +1065,7 @@ constexpr int MX_SF_SLOTS = 4;                         // 16 columns each: SFA 4
 #define FP8BS_MPF 8
 #endif
 constexpr int MPF = FP8BS_MPF;                         // producer scale prefetch (K blocks)
-constexpr int MX_REGS_LOW = 88, MX_REGS_HIGH = 208;   // 128*88 + 256*208 == 384*168
+constexpr int MX_REGS_LOW = 96, MX_REGS_HIGH = 200;   // 128*96 + 256*200 <= 384*168 (88 / 208 spilled)
 
 // UE8M0 code of a power-of-two fp32 scale (its exponent field), in all 4 bytes
 __device__ __forceinline__ uint32_t ue8m0_word(float s) {
